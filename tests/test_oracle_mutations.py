@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in a copy of the oracle; some pin must fail.
+
+Each mutation is a textual edit of the oracle's source, executed as a fresh
+module on the CPU.  The real oracle is never modified.
+"""
+import importlib.util
+import os
+import types
+
+import pytest
+
+import oracle_pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "moe_oracle.py")
+
+MUTATIONS = {
+    "reversed_code_order": ("(w >> np.uint32(bits * pos))", "(w >> np.uint32(bits * (per - 1 - pos)))"),
+    "dropped_bias": ("return q * s_full + b_full", "return q * s_full"),
+    "wrong_group_map": ("s_full = np.repeat(s, GROUP, axis=1)", "s_full = np.tile(s, (1, GROUP))"),
+    "tie_to_higher_id": ("np.lexsort((order_ids, -lg", "np.lexsort((-order_ids, -lg"),
+    "ascending_topk": ("np.lexsort((order_ids, -lg[row]", "np.lexsort((order_ids, lg[row]"),
+    "gelu_cubic_term": ("0.044715 * z ** 3", "0.044715 * z ** 2"),
+    "gelu_sign": ("(1.0 + np.tanh(", "(1.0 - np.tanh("),
+    "dropped_shared": ("    y += shared_out\n", "    pass\n"),
+    "unweighted_routes": ("y += weights[:, j:j + 1] * outs[:, j]", "y += outs[:, j]"),
+    "softmax_perturbed": ("e = np.exp(lg - m)", "e = np.exp(lg - m) + 0.0 * m + 1e-3"),
+    "gate_up_swapped_in_geglu": ("return gelu_tanh(g) * u", "return gelu_tanh(u) * g"),
+    "unstable_sort": ("for p, e in enumerate(flat):", "for p, e in reversed(list(enumerate(flat))):"),
+    "rms_without_eps": ("np.mean(h * h, axis=1, keepdims=True) + eps", "np.mean(h * h, axis=1, keepdims=True)"),
+    "bf16_truncation": ("keep = keep + up.astype(np.uint64)", "keep = keep"),
+    "router_bias_dropped": ("logits = logits + np.asarray(logit_bias", "logits = logits + 0 * np.asarray(logit_bias"),
+}
+
+
+def _mutant(name):
+    old, new = MUTATIONS[name]
+    with open(ORACLE_SRC) as f:
+        src = f.read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    src = src.replace(old, new, 1)
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(src, f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name):
+    mod = _mutant(name)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mod)
+        except (AssertionError, ValueError, ZeroDivisionError, FloatingPointError, IndexError) as exc:
+            caught.append((pin.__name__, type(exc).__name__))
+    assert caught, f"no pin caught mutation {name}"
