@@ -1,0 +1,207 @@
+"""Python binding of libmoe_gb300 (include/moe.h): argument marshalling only.
+
+Every step of the MoE block runs in the CUDA library; this module turns
+torch tensors into device pointers and status codes into exceptions.  It
+fails loudly when the compiled library is missing: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from .build import LIB_PATH, build as build_library
+
+__all__ = [
+    "MoeError", "Dims", "QMat", "BlobLayout", "LayerWeights", "Moe", "load_library", "header_symbols",
+    "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_BAD_EXPERT_ID",
+    "MOE_ERR_TIMEOUT", "MOE_ERR_NONFINITE", "MOE_ERR_WORKSPACE", "build_library",
+]
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_BAD_EXPERT_ID = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_NONFINITE = 6
+MOE_ERR_WORKSPACE = 7
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("n_experts", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("group", ctypes.c_int)]
+
+
+class QMat(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p)]
+
+
+_BLOB_FIELDS = ("gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b", "down_q", "down_s", "down_b")
+
+
+class BlobLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in _BLOB_FIELDS]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("dims", Dims), ("router", QMat), ("experts", ctypes.c_void_p), ("expert_stride", ctypes.c_size_t),
+                ("layout", BlobLayout), ("shared", ctypes.c_void_p), ("logit_bias", ctypes.c_void_p)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """dlopen the in-tree library (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (bit_affine_quantized_gb300.build_library())")
+    lib = ctypes.CDLL(path)
+    P, I, Z, V = ctypes.POINTER, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    proto = {
+        "moe_status_string": (ctypes.c_char_p, [I]),
+        "moe_create": (I, [P(V)]),
+        "moe_destroy": (I, [V]),
+        "moe_check_weights": (I, [P(LayerWeights)]),
+        "moe_workspace_bytes": (Z, [P(Dims), I]),
+        "moe_router_topk": (I, [V, V, I, P(LayerWeights), V, V, V, V, Z, V]),
+        "moe_route_sort": (I, [V, V, I, P(Dims), V, V, V, V, V]),
+        "moe_expert_ffn": (I, [V, V, I, V, V, P(LayerWeights), I, V, V, Z, V]),
+        "moe_layer_forward": (I, [V, V, I, P(LayerWeights), V, V, V, V, V, Z, V]),
+        "moe_layer_forward_residual": (I, [V, V, I, P(LayerWeights), V, V, V, V, V, Z, V]),
+        "moe_selftest_wait_timeout": (I, [V, ctypes.c_ulonglong, V]),
+        "moe_get_error": (I, [V, P(I)]),
+    }
+    for name, (res, args) in proto.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _status_string(status: int) -> str:
+    try:
+        return load_library().moe_status_string(status).decode()
+    except Exception:  # library not loadable: still report the number
+        return "status"
+
+
+def header_symbols(path: str = HEADER) -> list[str]:
+    """Names of the functions include/moe.h declares."""
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def _ptr(t):
+    """Device (or host) address of a tensor, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_dims(hidden: int, inter: int, n_experts: int, top_k: int, group: int = 64) -> Dims:
+    return Dims(hidden, inter, n_experts, top_k, group)
+
+
+def make_layer_weights(dims: Dims, router_q: int, router_s: int, router_b: int, experts: int, expert_stride: int,
+                       layout: dict, shared: int, logit_bias=None) -> LayerWeights:
+    """LayerWeights from device addresses; `layout` maps gate_q .. down_b to byte offsets."""
+    return LayerWeights(dims, QMat(router_q, router_s, router_b), experts, expert_stride,
+                        BlobLayout(*[layout[n] for n in _BLOB_FIELDS]), shared, _ptr(logit_bias))
+
+
+class Moe:
+    """One library handle (device error word + router counter) on the current device."""
+
+    def __init__(self):
+        self.lib = load_library()
+        h = ctypes.c_void_p()
+        st = self.lib.moe_create(ctypes.byref(h))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_create")
+        self.h = h
+
+    def close(self):
+        if self.h:
+            self.lib.moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, st, what):
+        if st != MOE_OK:
+            raise MoeError(st, what)
+
+    def workspace_bytes(self, dims: Dims, n_tokens: int) -> int:
+        return int(self.lib.moe_workspace_bytes(ctypes.byref(dims), n_tokens))
+
+    def router_topk(self, x, n_tokens, w: LayerWeights, ids, weights, ws, logits=None, stream=None):
+        self._check(self.lib.moe_router_topk(self.h, _ptr(x), n_tokens, ctypes.byref(w), _ptr(logits), _ptr(ids),
+                                             _ptr(weights), _ptr(ws), ws.numel() * ws.element_size(),
+                                             _stream(stream)), "moe_router_topk")
+
+    def route_sort(self, ids, n_tokens, dims: Dims, counts, offsets, perm, pos, stream=None):
+        self._check(self.lib.moe_route_sort(self.h, _ptr(ids), n_tokens, ctypes.byref(dims), _ptr(counts),
+                                            _ptr(offsets), _ptr(perm), _ptr(pos), _stream(stream)), "moe_route_sort")
+
+    def expert_ffn(self, x, n_tokens, ids, weights, w: LayerWeights, y, ws, include_shared=True, stream=None):
+        self._check(self.lib.moe_expert_ffn(self.h, _ptr(x), n_tokens, _ptr(ids), _ptr(weights), ctypes.byref(w),
+                                            1 if include_shared else 0, _ptr(y), _ptr(ws),
+                                            ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn")
+
+    def layer_forward(self, x, n_tokens, w: LayerWeights, y, ws, ids_out=None, logits_out=None, weights_out=None,
+                      stream=None):
+        self._check(self.lib.moe_layer_forward(self.h, _ptr(x), n_tokens, ctypes.byref(w), _ptr(y), _ptr(ids_out),
+                                               _ptr(logits_out), _ptr(weights_out), _ptr(ws),
+                                               ws.numel() * ws.element_size(), _stream(stream)), "moe_layer_forward")
+
+    def layer_forward_residual(self, hidden, n_tokens, w: LayerWeights, ws, y_out=None, x_out=None, ids_out=None,
+                               logits_out=None, stream=None):
+        self._check(self.lib.moe_layer_forward_residual(self.h, _ptr(hidden), n_tokens, ctypes.byref(w), _ptr(y_out),
+                                                        _ptr(x_out), _ptr(ids_out), _ptr(logits_out), _ptr(ws),
+                                                        ws.numel() * ws.element_size(), _stream(stream)),
+                    "moe_layer_forward_residual")
+
+    def selftest_wait_timeout(self, limit_ns: int, stream=None):
+        self._check(self.lib.moe_selftest_wait_timeout(self.h, limit_ns, _stream(stream)), "moe_selftest_wait_timeout")
+
+    def get_error(self) -> int:
+        st = ctypes.c_int(0)
+        self._check(self.lib.moe_get_error(self.h, ctypes.byref(st)), "moe_get_error")
+        return st.value
+
+
+def layer_weights_from(dims: Dims, addr: dict) -> LayerWeights:
+    """LayerWeights from a dict with router_q/router_s/router_b/experts/stride/
+    shared/layout/logit_bias entries (device addresses and byte offsets)."""
+    return make_layer_weights(dims, addr["router_q"], addr["router_s"], addr["router_b"], addr["experts"],
+                              addr["stride"], addr["layout"], addr["shared"], addr.get("logit_bias"))

@@ -1,0 +1,356 @@
+// C ABI of the MoE block: argument checks, workspace carving, launches.
+// Declarations and the contract of every call: include/moe.h.
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+#include "moe.h"
+
+struct moe_handle {
+  int device;
+  unsigned *dwords;  // [0] device error bits, [1] router ticket counter
+  bool pdl;
+  int prefetch_max;  // bytes; 0 disables the L2 prefetch of selected experts
+};
+
+namespace {
+
+constexpr size_t kSmemCap = 227 * 1024;
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+moe::Dims to_dims(const moe_dims &d, int T) { return moe::Dims{d.hidden, d.inter, d.n_experts, d.top_k, T}; }
+
+int check_dims(const moe_dims *d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->group != 64) return MOE_ERR_UNSUPPORTED;
+  if (d->hidden < 64 || d->hidden > 4096 || d->hidden % 64) return MOE_ERR_UNSUPPORTED;
+  if (d->inter < 64 || d->inter > 2048 || d->inter % 64) return MOE_ERR_UNSUPPORTED;
+  if (d->top_k < 1 || d->top_k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (d->n_experts < d->top_k || d->n_experts > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  const moe::Dims dd = to_dims(*d, moe::kMaxTokens);
+  if (moe::gateup_smem(dd, 8) > kSmemCap || moe::down_grouped_smem(dd) > kSmemCap ||
+      moe::router_smem(dd, 8) > 200 * 1024)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_tokens(int T) { return (T >= 1 && T <= moe::kMaxTokens) ? MOE_OK : MOE_ERR_INVALID_ARG; }
+
+size_t blob_extent(const moe_layer_weights &w) {
+  const size_t H = w.dims.hidden, I = w.dims.inter;
+  const size_t q = I * H / 2, sb = I * (H / 64) * 2;
+  const size_t ends[9] = {w.layout.gate_q + q, w.layout.gate_s + sb, w.layout.gate_b + sb,
+                          w.layout.up_q + q,   w.layout.up_s + sb,   w.layout.up_b + sb,
+                          w.layout.down_q + q, w.layout.down_s + sb, w.layout.down_b + sb};
+  return *std::max_element(ends, ends + 9);
+}
+
+struct WsLayout {
+  size_t logits, ids, wts, counts, offsets, perm, pos, act_e, act_beg, act_cnt, n_act, xn, h, o, total;
+};
+
+WsLayout ws_layout(const moe_dims &d, int T) {
+  const size_t H = d.hidden, I = d.inter, E = d.n_experts, k = d.top_k;
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.logits = take((size_t)T * E * 4);
+  L.ids = take((size_t)T * k * 4);
+  L.wts = take((size_t)T * k * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take((size_t)T * k * 4);
+  L.pos = take((size_t)T * k * 4);
+  L.act_e = take((E + 1) * 4);
+  L.act_beg = take((E + 1) * 4);
+  L.act_cnt = take((E + 1) * 4);
+  L.n_act = take(4);
+  L.xn = take((size_t)T * H * 2);
+  L.h = take(((size_t)T * k + T) * I * 2);
+  L.o = moe::use_down_decode(to_dims(d, T)) ? off : take(((size_t)T * k + T) * H * 4);
+  L.total = off;
+  return L;
+}
+
+moe::Routing routing_in(uint8_t *ws, const WsLayout &L) {
+  moe::Routing r;
+  r.ids = (int32_t *)(ws + L.ids);
+  r.wts = (float *)(ws + L.wts);
+  r.counts = (int32_t *)(ws + L.counts);
+  r.offsets = (int32_t *)(ws + L.offsets);
+  r.perm = (int32_t *)(ws + L.perm);
+  r.pos = (int32_t *)(ws + L.pos);
+  r.act_e = (int32_t *)(ws + L.act_e);
+  r.act_beg = (int32_t *)(ws + L.act_beg);
+  r.act_cnt = (int32_t *)(ws + L.act_cnt);
+  r.n_act = (int32_t *)(ws + L.n_act);
+  return r;
+}
+
+int check_weights_impl(const moe_layer_weights *w) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  int st = check_dims(&w->dims);
+  if (st) return st;
+  const void *ptrs[6] = {w->router.q, w->router.scales, w->router.biases, w->experts, w->shared, nullptr};
+  for (int i = 0; i < 5; ++i)
+    if (!ptrs[i] || !aligned(ptrs[i], 16)) return MOE_ERR_INVALID_ARG;
+  if (w->logit_bias && !aligned(w->logit_bias, 4)) return MOE_ERR_INVALID_ARG;
+  const size_t offs[9] = {w->layout.gate_q, w->layout.gate_s, w->layout.gate_b, w->layout.up_q, w->layout.up_s,
+                          w->layout.up_b,   w->layout.down_q, w->layout.down_s, w->layout.down_b};
+  for (size_t o : offs)
+    if (o % 256) return MOE_ERR_INVALID_ARG;
+  if (w->expert_stride % 256 || w->expert_stride < blob_extent(*w)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe::LayerPtrs layer_ptrs(const moe_layer_weights &w) {
+  moe::LayerPtrs p;
+  p.router_q = (const uint8_t *)w.router.q;
+  p.router_s = (const uint16_t *)w.router.scales;
+  p.router_b = (const uint16_t *)w.router.biases;
+  p.experts = (const uint8_t *)w.experts;
+  p.stride = w.expert_stride;
+  p.shared = (const uint8_t *)w.shared;
+  p.off = moe::Blob{w.layout.gate_q, w.layout.gate_s, w.layout.gate_b, w.layout.up_q,  w.layout.up_s,
+                    w.layout.up_b,   w.layout.down_q, w.layout.down_s, w.layout.down_b};
+  p.blob_bytes = blob_extent(w);
+  p.logit_bias = w.logit_bias;
+  return p;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int check_ws(const moe_dims &d, int T, const void *ws, size_t ws_bytes) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(d, T).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int run_router(moe_handle *h, const moe_layer_weights *w, int T, const void *x, void *hres, void *x_out,
+               float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(w->dims, T);
+  moe::RouterArgs a;
+  a.w = layer_ptrs(*w);
+  a.d = to_dims(w->dims, T);
+  a.x = (const uint16_t *)x;
+  a.hres = (uint16_t *)hres;
+  a.xn = (uint16_t *)(ws + L.xn);
+  a.xn_user = (uint16_t *)x_out;
+  a.logits = logits ? logits : (float *)(ws + L.logits);
+  a.ids_user = ids;
+  a.wts_user = wts;
+  a.r = routing_in(ws, L);
+  a.counter = h->dwords + 1;
+  a.err = h->dwords;
+  a.normalize = hres != nullptr;
+  a.prefetch_bytes_max = h->prefetch_max;
+  return cuda_status(moe::launch_router(a, st, h->pdl));
+}
+
+int run_ffn(moe_handle *h, const moe_layer_weights *w, int T, const void *x, const moe::Routing &r, int include_shared,
+            void *y, void *hres, uint8_t *ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(w->dims, T);
+  moe::FfnArgs a;
+  a.w = layer_ptrs(*w);
+  a.d = to_dims(w->dims, T);
+  a.x = (const uint16_t *)x;
+  a.r = r;
+  a.hbuf = (__half *)(ws + L.h);
+  a.obuf = (float *)(ws + L.o);
+  a.y = (uint16_t *)y;
+  a.hres = (uint16_t *)hres;
+  a.include_shared = include_shared;
+  a.err = h->dwords;
+  cudaError_t e = moe::launch_gateup(a, st, h->pdl);
+  if (e == cudaSuccess) e = moe::launch_down(a, st, h->pdl);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id out of range (skipped on the device)";
+    case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
+    case MOE_ERR_NONFINITE: return "non-finite router logit or activation";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int moe_create(moe_handle **out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+  if (moe::router_set_attributes() != cudaSuccess || moe::ffn_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+  moe_handle *h = (moe_handle *)calloc(1, sizeof(moe_handle));
+  if (!h) return MOE_ERR_CUDA;
+  h->device = dev;
+  if (cudaMalloc(&h->dwords, 64 * sizeof(unsigned)) != cudaSuccess) {
+    free(h);
+    return MOE_ERR_CUDA;
+  }
+  if (cudaMemset(h->dwords, 0, 64 * sizeof(unsigned)) != cudaSuccess) {
+    cudaFree(h->dwords);
+    free(h);
+    return MOE_ERR_CUDA;
+  }
+  const char *pdl = getenv("MOE_PDL");
+  h->pdl = !(pdl && pdl[0] == '0');
+  const char *pf = getenv("MOE_L2_PREFETCH_MB");
+  h->prefetch_max = pf ? atoi(pf) * (1 << 20) : 64 * (1 << 20);
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_destroy(moe_handle *h) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  const cudaError_t e = cudaFree(h->dwords);
+  free(h);
+  return cuda_status(e);
+}
+
+int moe_check_weights(const moe_layer_weights *w) { return check_weights_impl(w); }
+
+size_t moe_workspace_bytes(const moe_dims *dims, int n_tokens) {
+  if (check_dims(dims) != MOE_OK || check_tokens(n_tokens) != MOE_OK) return 0;
+  return ws_layout(*dims, n_tokens).total;
+}
+
+int moe_router_topk(moe_handle *h, const void *x, int n_tokens, const moe_layer_weights *w, float *logits,
+                    int32_t *ids, float *weights, void *ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!h || !x || !ids || !weights) return MOE_ERR_INVALID_ARG;
+  int st = check_weights_impl(w);
+  if (st) return st;
+  if ((st = check_tokens(n_tokens))) return st;
+  if (!aligned(x, 16) || (logits && !aligned(logits, 16))) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
+  return run_router(h, w, n_tokens, x, nullptr, nullptr, logits, ids, weights, (uint8_t *)ws, (cudaStream_t)stream);
+}
+
+int moe_route_sort(moe_handle *h, const int32_t *ids, int n_tokens, const moe_dims *dims, int32_t *counts,
+                   int32_t *offsets, int32_t *perm, int32_t *pos, moe_stream_t stream) {
+  if (!h || !ids || !counts || !offsets || !perm || !pos) return MOE_ERR_INVALID_ARG;
+  int st = check_dims(dims);
+  if (st) return st;
+  if ((st = check_tokens(n_tokens))) return st;
+  moe::SortArgs a;
+  a.ids = ids;
+  a.T = n_tokens;
+  a.k = dims->top_k;
+  a.E = dims->n_experts;
+  memset(&a.r, 0, sizeof(a.r));
+  a.r.counts = counts;
+  a.r.offsets = offsets;
+  a.r.perm = perm;
+  a.r.pos = pos;
+  a.include_shared = 0;
+  a.err = h->dwords;
+  return cuda_status(moe::launch_sort(a, (cudaStream_t)stream, h->pdl));
+}
+
+int moe_expert_ffn(moe_handle *h, const void *x, int n_tokens, const int32_t *ids, const float *weights,
+                   const moe_layer_weights *w, int include_shared, void *y, void *ws, size_t ws_bytes,
+                   moe_stream_t stream) {
+  if (!h || !x || !ids || !weights || !y) return MOE_ERR_INVALID_ARG;
+  int st = check_weights_impl(w);
+  if (st) return st;
+  if ((st = check_tokens(n_tokens))) return st;
+  if (!aligned(x, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
+  uint8_t *wsb = (uint8_t *)ws;
+  const WsLayout L = ws_layout(w->dims, n_tokens);
+  moe::Routing r = routing_in(wsb, L);
+  r.ids = const_cast<int32_t *>(ids);
+  r.wts = const_cast<float *>(weights);
+  moe::SortArgs sa;
+  sa.ids = ids;
+  sa.T = n_tokens;
+  sa.k = w->dims.top_k;
+  sa.E = w->dims.n_experts;
+  sa.r = r;
+  sa.include_shared = include_shared ? 1 : 0;
+  sa.err = h->dwords;
+  cudaError_t e = moe::launch_sort(sa, (cudaStream_t)stream, h->pdl);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return run_ffn(h, w, n_tokens, x, r, include_shared ? 1 : 0, y, nullptr, wsb, (cudaStream_t)stream);
+}
+
+int moe_layer_forward(moe_handle *h, const void *x, int n_tokens, const moe_layer_weights *w, void *y,
+                      int32_t *ids_out, float *logits_out, float *weights_out, void *ws, size_t ws_bytes,
+                      moe_stream_t stream) {
+  if (!h || !x || !y) return MOE_ERR_INVALID_ARG;
+  int st = check_weights_impl(w);
+  if (st) return st;
+  if ((st = check_tokens(n_tokens))) return st;
+  if (!aligned(x, 16) || !aligned(y, 16) || (logits_out && !aligned(logits_out, 16))) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
+  uint8_t *wsb = (uint8_t *)ws;
+  if ((st = run_router(h, w, n_tokens, x, nullptr, nullptr, logits_out, ids_out, weights_out, wsb,
+                       (cudaStream_t)stream)))
+    return st;
+  return run_ffn(h, w, n_tokens, x, routing_in(wsb, ws_layout(w->dims, n_tokens)), 1, y, nullptr, wsb,
+                 (cudaStream_t)stream);
+}
+
+int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens, const moe_layer_weights *w, void *y_out,
+                               void *x_out, int32_t *ids_out, float *logits_out, void *ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  if (!h || !hidden) return MOE_ERR_INVALID_ARG;
+  int st = check_weights_impl(w);
+  if (st) return st;
+  if ((st = check_tokens(n_tokens))) return st;
+  if (!aligned(hidden, 16) || (y_out && !aligned(y_out, 16)) || (x_out && !aligned(x_out, 16)) ||
+      (logits_out && !aligned(logits_out, 16)))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
+  uint8_t *wsb = (uint8_t *)ws;
+  const WsLayout L = ws_layout(w->dims, n_tokens);
+  if ((st = run_router(h, w, n_tokens, nullptr, hidden, x_out, logits_out, ids_out, nullptr, wsb,
+                       (cudaStream_t)stream)))
+    return st;
+  return run_ffn(h, w, n_tokens, wsb + L.xn, routing_in(wsb, L), 1, y_out, hidden, wsb, (cudaStream_t)stream);
+}
+
+int moe_selftest_wait_timeout(moe_handle *h, unsigned long long limit_ns, moe_stream_t stream) {
+  if (!h || limit_ns == 0 || limit_ns > 2000000000ull) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_wait_timeout(h->dwords, limit_ns, (cudaStream_t)stream));
+}
+
+int moe_get_error(moe_handle *h, int *status) {
+  if (!h || !status) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpy(&bits, h->dwords, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(h->dwords, 0, sizeof(unsigned)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (bits & moe::kErrTimeout)
+    *status = MOE_ERR_TIMEOUT;
+  else if (bits & moe::kErrBadId)
+    *status = MOE_ERR_BAD_EXPERT_ID;
+  else if (bits & moe::kErrNonFinite)
+    *status = MOE_ERR_NONFINITE;
+  else
+    *status = MOE_OK;
+  return MOE_OK;
+}
+
+}  // extern "C"

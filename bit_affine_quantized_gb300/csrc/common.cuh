@@ -1,0 +1,201 @@
+// Device helpers shared by the MoE kernels: PTX wrappers for mbarriers, bulk
+// (TMA 1-D) copies, L2 prefetch, programmatic dependent launch and the
+// legacy-path mma.sync used for the small-N (few tokens per expert) tiles;
+// the packed-code -> tensor-core operand conversions; and the parameter
+// blocks the host fills.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kGroup = 64;        // quantisation group along K
+constexpr int kMaxTokens = 128;   // chunk bound of one call
+constexpr int kMaxTopK = 8;
+constexpr int kMaxExperts = 128;
+constexpr int kSharedSlot = -1;   // expert id used for the shared expert's slot
+
+// device error bits (OR-ed into the handle's error word)
+constexpr unsigned kErrBadId = 1u;
+constexpr unsigned kErrTimeout = 2u;
+constexpr unsigned kErrNonFinite = 4u;
+
+// bounded waits give up after this many nanoseconds
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ------------------------------------------------------------------ params
+struct Blob {
+  size_t gate_q, gate_s, gate_b, up_q, up_s, up_b, down_q, down_s, down_b;
+};
+
+// Token/expert grouping produced by the router (or by the sort kernel).
+// Positions [0, n_valid) hold routed pairs in (expert, pair index) order;
+// positions [T*k, T*k + T) hold the shared expert's rows (row t = token t).
+struct Routing {
+  int32_t *ids;        // [T*k]
+  float *wts;          // [T*k]
+  int32_t *counts;     // [E]
+  int32_t *offsets;    // [E+1]
+  int32_t *perm;       // [T*k]  sorted position -> pair index
+  int32_t *pos;        // [T*k]  pair index -> sorted position (-1: dropped)
+  int32_t *act_e;      // [E+1]  expert of active slot a (kSharedSlot = shared)
+  int32_t *act_beg;    // [E+1]  first position of slot a
+  int32_t *act_cnt;    // [E+1]  rows of slot a
+  int32_t *n_act;      // [1]
+};
+
+struct LayerPtrs {
+  const uint8_t *router_q;      // [E, H] bytes
+  const uint16_t *router_s;     // [E, H/64] bf16
+  const uint16_t *router_b;     // [E, H/64] bf16
+  const uint8_t *experts;       // E blobs
+  size_t stride;
+  const uint8_t *shared;        // shared blob
+  Blob off;
+  size_t blob_bytes;            // extent of one blob's sub-tensors (max end offset)
+  const float *logit_bias;      // nullable [E]
+};
+
+struct Dims {
+  int H, I, E, k, T;
+};
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase with the given parity; false after limit_ns of
+// global time (or 2^24 polls, whichever comes first).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 31u && global_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// D(16x8, f32) += A(16x16) * B(16x8), bf16 operands.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Same with f16 operands.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------ codes
+// Two 4-bit codes of word w -> bf16x2 {128 + q_i, 128 + q_{i+4}}, exact.
+// 0x4300 is bf16 128.0, whose unit in the last place is 1, so OR-ing a
+// code 0..15 into the low mantissa bits yields 128 + code.
+template <int i>
+__device__ __forceinline__ uint32_t codes_bf16_plus128(uint32_t w) {
+  return ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+}
+// Two 4-bit codes -> f16x2 {q_i, q_{i+4}}, exact: 0x6400 is f16 1024.0 with
+// unit last place 1; subtracting 1024 leaves the code.
+template <int i>
+__device__ __forceinline__ uint32_t codes_f16(uint32_t w) {
+  const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64006400u));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// float -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Operand order inside one 64-wide group.  The tensor-core fragments take
+// the 4-bit codes of a thread's two packed words in the order produced by
+// codes_*<i>: pair i of word w holds codes (i, i+4).  The activation vector
+// is stored in shared memory permuted so that each B fragment (4 values) is
+// one 8-byte load.  Slot j = 16c + 4s + m of a group holds element
+// 16c + 8(s>>1) + 2(s&1) + {0,4,1,5}[m].
+// Builds the 16 permuted values of quarter c from its 16 natural values
+// (8 words, each two 16-bit elements).
+__device__ __forceinline__ void permute_quarter(const uint32_t (&in)[8], uint32_t (&out)[8]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {     // s>>1
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {   // s&1
+      const uint32_t a = in[4 * h + e];      // elements 8h+2e, 8h+2e+1
+      const uint32_t b = in[4 * h + e + 2];  // elements 8h+2e+4, 8h+2e+5
+      out[4 * h + 2 * e + 0] = __byte_perm(a, b, 0x5410);  // (8h+2e,   8h+2e+4)
+      out[4 * h + 2 * e + 1] = __byte_perm(a, b, 0x7632);  // (8h+2e+1, 8h+2e+5)
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ void set_error(unsigned *err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+}  // namespace moe

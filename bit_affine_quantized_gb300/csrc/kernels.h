@@ -1,0 +1,81 @@
+// Host-side launchers of the MoE kernels (defined next to each kernel).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct RouterArgs {
+  LayerPtrs w;
+  Dims d;
+  const uint16_t *x;       // bf16 [T, H] block input (normalize == 0)
+  uint16_t *hres;          // bf16 [T, H] residual stream (normalize == 1)
+  uint16_t *xn;            // bf16 [T, H] normalised input out (normalize == 1)
+  uint16_t *xn_user;       // nullable copy of xn
+  float *logits;           // fp32 [T, E]
+  int32_t *ids_user;       // nullable copies of the routing
+  float *wts_user;
+  Routing r;
+  unsigned *counter;       // last-block ticket, zero between launches
+  unsigned *err;
+  int normalize;
+  int prefetch_bytes_max;  // L2-prefetch the selected experts if their total fits
+};
+
+struct FfnArgs {
+  LayerPtrs w;
+  Dims d;
+  const uint16_t *x;       // bf16 [T, H] block input
+  Routing r;
+  __half *hbuf;            // fp16 [T*k + T, I]
+  float *obuf;             // fp32 [T*k + T, H] (grouped down path)
+  uint16_t *y;             // nullable bf16 [T, H]
+  uint16_t *hres;          // nullable bf16 [T, H]: hres <- bf16(hres + y)
+  int include_shared;
+  unsigned *err;
+};
+
+struct SortArgs {
+  const int32_t *ids;
+  int T, k, E;
+  Routing r;               // counts/offsets/perm/pos required; act_* nullable
+  int include_shared;
+  unsigned *err;
+};
+
+// smem budgets (bytes) for a given shape; 0 = shape not supported by that kernel
+size_t router_smem(const Dims &d, int tb);
+size_t gateup_smem(const Dims &d, int tt);
+size_t down_decode_smem(const Dims &d);
+size_t down_grouped_smem(const Dims &d);
+
+cudaError_t router_set_attributes();
+cudaError_t ffn_set_attributes();
+cudaError_t launch_router(const RouterArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_sort(const SortArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_down(const FfnArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_wait_timeout(unsigned *err, unsigned long long limit_ns, cudaStream_t st);
+bool use_down_decode(const Dims &d);
+
+// generic launch with optional programmatic dependent launch
+template <typename Kern, typename Arg>
+cudaError_t launch_k(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, const Arg &arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
+}  // namespace moe

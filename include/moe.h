@@ -1,0 +1,205 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) mixture-of-experts FFN block with
+ * MLX-style group-64 affine quantised weights.
+ *
+ * The block (page "TurboFieldfare - System design"):
+ *   1. router: logits[t, e] = sum_k W_r[e, k] x[t, k], W_r 8-bit affine,
+ *      no softcap (section "Why the runtime has this shape"; section
+ *      "Decode", router description);
+ *   2. top-k (k = 8 of E = 128) with ties to the lower expert id, softmax
+ *      over the k selected logits (section "Decode");
+ *   3. per selected expert a 4-bit affine GeGLU FFN
+ *      o = W_down (gelu_tanh(W_gate x) * (W_up x)) (section "Metal
+ *      execution": fused affine decode + GeGLU + weighted reduction);
+ *   4. y = sum_j w_j o_j + o_shared, the dense shared expert added with no
+ *      routing weight (section "Why the runtime has this shape").
+ * Prefill handles chunks of at most 128 rows (section "Prefill"), so every
+ * call takes 1 <= n_tokens <= 128.
+ *
+ * Quantised matrix format (section "Why the runtime has this shape"): a
+ * matrix W[N, K] is three arrays
+ *   q      : packed codes, row-major, little-endian uint32 words; code i of a
+ *            row at bits 4*(i%8) of word i/8 (4-bit) or 8*(i%4) of word i/4
+ *            (8-bit, i.e. plain byte order);
+ *   scales : bf16 [N, K/64], row-major;
+ *   biases : bf16 [N, K/64], row-major;
+ * and W[n, k] = q[n, k] * scales[n, k/64] + biases[n, k/64].
+ *
+ * Expert storage (section ".gturbo directory": fixed-stride, page-aligned
+ * expert blobs whose sub-tensors sit at their own offsets): routed expert e
+ * is the blob at experts + e * expert_stride; inside a blob the nine
+ * sub-tensors (gate/up [I, H], down [H, I]; q, scales, biases each) sit at
+ * the byte offsets of moe_blob_layout.  The shared expert is one more blob
+ * with the same layout.
+ *
+ * Conventions for every call
+ *   - Returns MOE_OK (0) or a MOE_ERR_* code; nothing throws across the ABI.
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never frees them.  The workspace `ws` is caller-owned device
+ *     memory of at least moe_workspace_bytes() bytes, 256-byte aligned, and
+ *     must not be shared by calls that may run concurrently.
+ *   - Launches are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream); no call synchronises the host except
+ *     moe_get_error.  Inputs must stay valid until the stream reaches the
+ *     call.
+ *   - Arguments are checked on the host before anything is launched:
+ *     null pointers, n_tokens outside [1, 128], dims the kernels do not
+ *     support, pointers not 16-byte aligned (tensor data) or offsets not
+ *     256-byte aligned -> MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED and no
+ *     launch.  Faults found on the device (an expert id out of range in
+ *     moe_expert_ffn / moe_route_sort, non-finite router logits) never trap:
+ *     the offending item is skipped and a device error word is set, read
+ *     back by moe_get_error.
+ *   - A handle may be used from one stream at a time (it owns the device
+ *     error word and the router's completion counter).
+ */
+#ifndef MOE_AFFINE_H
+#define MOE_AFFINE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* == cudaStream_t */
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size or alignment          */
+  MOE_ERR_UNSUPPORTED = 2,   /* dims outside what the kernels implement       */
+  MOE_ERR_CUDA = 3,          /* a CUDA runtime call failed                    */
+  MOE_ERR_BAD_EXPERT_ID = 4, /* device: expert id outside [0, E) was skipped  */
+  MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up                */
+  MOE_ERR_NONFINITE = 6,     /* device: a router logit was NaN or infinite    */
+  MOE_ERR_WORKSPACE = 7      /* workspace smaller than moe_workspace_bytes    */
+};
+
+/* Shapes.  Supported: group == 64; hidden, inter multiples of 64 with
+ * 64 <= hidden <= 4096 and 64 <= inter <= 2048; 1 <= top_k <= 8;
+ * top_k <= n_experts <= 128.  The target workload is hidden 2816,
+ * inter 704, 128 experts, top-8. */
+typedef struct {
+  int hidden;    /* H: model width, input/output features of the block      */
+  int inter;     /* I: expert intermediate width                            */
+  int n_experts; /* E: routed experts                                       */
+  int top_k;     /* k: experts selected per token                           */
+  int group;     /* quantisation group along K; must be 64                  */
+} moe_dims;
+
+/* One quantised matrix: device pointers to codes, scales, biases. */
+typedef struct {
+  const void *q;
+  const void *scales;
+  const void *biases;
+} moe_qmat;
+
+/* Byte offsets of the nine sub-tensors inside one expert blob; each must be
+ * a multiple of 256. */
+typedef struct {
+  size_t gate_q, gate_s, gate_b;
+  size_t up_q, up_s, up_b;
+  size_t down_q, down_s, down_b;
+} moe_blob_layout;
+
+/* Weights of one MoE layer (all device pointers). */
+typedef struct {
+  moe_dims dims;
+  moe_qmat router;          /* 8-bit [E, H]                                   */
+  const void *experts;      /* E routed blobs, fixed stride                   */
+  size_t expert_stride;     /* bytes between blobs; multiple of 256           */
+  moe_blob_layout layout;   /* sub-tensor offsets (routed and shared blobs)   */
+  const void *shared;       /* the shared expert's blob                       */
+  const float *logit_bias;  /* nullable [E]: added to the logits before top-k */
+} moe_layer_weights;
+
+typedef struct moe_handle moe_handle;
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_string(int status);
+
+/* Create / destroy a handle on the current CUDA device.  moe_create
+ * allocates a few bytes of device memory (error word, counters) and sets
+ * kernel attributes; it is the only call that allocates. */
+int moe_create(moe_handle **out);
+int moe_destroy(moe_handle *h);
+
+/* Host-side validation of a layer description (no device access). */
+int moe_check_weights(const moe_layer_weights *w);
+
+/* Workspace bytes needed by moe_router_topk / moe_expert_ffn /
+ * moe_layer_forward / moe_layer_forward_residual for n_tokens rows;
+ * 0 if dims are unsupported or n_tokens is outside [1, 128]. */
+size_t moe_workspace_bytes(const moe_dims *dims, int n_tokens);
+
+/* Steps 1-2 (router projection, top-k, softmax weights).
+ *   x        bf16 [T, H] row-major, the block input (already normalised)
+ *   logits   nullable fp32 [T, E]: raw logits + logit_bias
+ *   ids      int32 [T, k]: selected experts, by descending logit, ties to
+ *            the lower id
+ *   weights  fp32 [T, k]: softmax over the selected logits
+ * Also leaves the token->expert grouping of step 3 in the workspace. */
+int moe_router_topk(moe_handle *h, const void *x, int n_tokens, const moe_layer_weights *w,
+                    float *logits, int32_t *ids, float *weights, void *ws, size_t ws_bytes,
+                    moe_stream_t stream);
+
+/* Step 3 on its own: stable counting sort of the pairs p = t*k + j by
+ * expert id (section "Prefill": token/expert pairs grouped per expert).
+ *   ids      int32 [T, k] device
+ *   counts   int32 [E]       pairs per expert
+ *   offsets  int32 [E + 1]   exclusive prefix sums of counts
+ *   perm     int32 [T*k]     pair index at each sorted position
+ *   pos      int32 [T*k]     sorted position of each pair (-1 if its id was
+ *                            out of range; such pairs are dropped and
+ *                            MOE_ERR_BAD_EXPERT_ID is recorded)
+ * Runs one thread block; needs no workspace. */
+int moe_route_sort(moe_handle *h, const int32_t *ids, int n_tokens, const moe_dims *dims,
+                   int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *pos,
+                   moe_stream_t stream);
+
+/* Steps 3-4 with caller-given routing (e.g. forced ids).
+ *   x        bf16 [T, H];  ids int32 [T, k];  weights fp32 [T, k]
+ *   include_shared  1: add the shared expert; 0: routed sum only
+ *   y        bf16 [T, H] output
+ * Out-of-range ids are skipped on the device (MOE_ERR_BAD_EXPERT_ID). */
+int moe_expert_ffn(moe_handle *h, const void *x, int n_tokens, const int32_t *ids,
+                   const float *weights, const moe_layer_weights *w, int include_shared, void *y,
+                   void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole block, steps 1-4: y = MoE(x).
+ *   x bf16 [T, H] in;  y bf16 [T, H] out;
+ *   ids_out (int32 [T, k]), logits_out (fp32 [T, E]), weights_out
+ *   (fp32 [T, k]) are nullable copies of the routing. */
+int moe_layer_forward(moe_handle *h, const void *x, int n_tokens, const moe_layer_weights *w,
+                      void *y, int32_t *ids_out, float *logits_out, float *weights_out, void *ws,
+                      size_t ws_bytes, moe_stream_t stream);
+
+/* One layer of a residual stack (the decode/prefill harness around the
+ * block): x = bf16(h / sqrt(mean(h^2) + 1e-6)) (rmsnorm without scale, as
+ * the router's input normalisation in section "Decode"); y = MoE(x);
+ * h <- bf16(h + y) in place.
+ *   hidden   bf16 [T, H] in/out
+ *   y_out    nullable bf16 [T, H]: the block output before the add
+ *   x_out    nullable bf16 [T, H]: the normalised block input */
+int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
+                               const moe_layer_weights *w, void *y_out, void *x_out,
+                               int32_t *ids_out, float *logits_out, void *ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
+/* Self-test of the device-side bounded waits (failure detection without a
+ * GPU fault): launches one thread that waits on a barrier nothing ever
+ * completes; after limit_ns (1 .. 2e9 ns) of device time it gives up and
+ * records MOE_ERR_TIMEOUT in the error word, which moe_get_error then
+ * reports.  Every wait in the kernels above uses the same bounded wait. */
+int moe_selftest_wait_timeout(moe_handle *h, unsigned long long limit_ns, moe_stream_t stream);
+
+/* Waits for all work on the device, then returns (in *status) the first
+ * device-side error recorded since the last call (MOE_OK if none) and
+ * clears it.  The return value reports failures of the call itself. */
+int moe_get_error(moe_handle *h, int *status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_AFFINE_H */

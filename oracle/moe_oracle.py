@@ -211,28 +211,37 @@ def moe_block(x_bits, router: dict, get_expert, shared: dict, k: int, logit_bias
 
     Returns dict: logits [T,E], ids [T,k], weights [T,k], y [T,H] float64,
     y_bf16 bits [T,H]."""
-    x = bf16_to_f64(x_bits)
-    t_count = x.shape[0]
     logits = router_logits(x_bits, router, logit_bias)
     if ids is None:
         ids = select_top_k(logits, k)
     ids = np.asarray(ids, dtype=np.int64)
     weights = routing_weights(logits, ids)
+    y = expert_mix(x_bits, ids, weights, get_expert, shared)
+    return {"logits": logits, "ids": ids, "weights": weights, "y": y, "y_bf16": f64_to_bf16(y)}
 
-    # o[t, j] = FFN_{ids[t, j]}(x_t); each distinct expert expanded once.
+
+def expert_mix(x_bits, ids, weights, get_expert, shared=None) -> np.ndarray:
+    """y[t] = sum_j weights[t, j] * FFN_{ids[t, j]}(x_t)  (+ FFN_shared(x_t)).
+
+    Sum in selection order j, then the shared term (omitted if shared is
+    None).  Each distinct expert is expanded once.  float64 [T, H]."""
+    x = bf16_to_f64(x_bits)
+    ids = np.asarray(ids, dtype=np.int64)
+    weights = np.asarray(weights, dtype=np.float64)
+    t_count, k = ids.shape
     h_dim = x.shape[1]
     outs = np.zeros((t_count, k, h_dim), dtype=np.float64)
     for e in np.unique(ids):
         rows, cols = np.nonzero(ids == e)
         dense = dense_expert(get_expert(int(e)))
         outs[rows, cols] = expert_ffn(x[rows], dense)
-    shared_out = expert_ffn(x, dense_expert(shared))
-
     y = np.zeros((t_count, h_dim), dtype=np.float64)
     for j in range(k):
         y += weights[:, j:j + 1] * outs[:, j]
-    y += shared_out
-    return {"logits": logits, "ids": ids, "weights": weights, "y": y, "y_bf16": f64_to_bf16(y)}
+    if shared is not None:
+        shared_out = expert_ffn(x, dense_expert(shared))
+        y += shared_out
+    return y
 
 
 def rmsnorm_no_scale(h_bits, eps: float = RMS_EPS) -> np.ndarray:

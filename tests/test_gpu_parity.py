@@ -1,0 +1,237 @@
+"""CUDA path vs the float64 oracle, through the C ABI, on a GB300.
+
+Decisions taken in floating point (the top-k) are checked on the GPU's own
+fp32 logits: ids must equal the oracle's top-k of those logits bit for bit.
+Values (logits, routing weights, outputs) are checked against the oracle at
+the block's tolerance (numerics.py).  Outputs are compared with the oracle
+run on the GPU's ids (teacher forcing), so a near-tie that flips the
+selection cannot hide an arithmetic error or fake one."""
+import numpy as np
+import pytest
+
+import bit_affine_quantized_gb300 as bq
+from gpu_layers import (E, H, I, K, HostExperts, hidden, oracle_layer, run_layer, to_dev_bf16, from_dev_bf16,
+                        weights_of, workspace)
+from numerics import assert_close, bf16_bits_to_f64
+from oracle import moe_oracle as O
+from synth.device import DeviceLayer
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    bq.build_library()
+    m = bq.Moe()
+    yield m
+    m.close()
+
+
+@pytest.fixture(scope="module")
+def layer0():
+    return DeviceLayer(0, H, I, E)
+
+
+@pytest.fixture(scope="module")
+def layer0_zipf():
+    return DeviceLayer(0, H, I, E, zipf=True)
+
+
+def _check_routing(out, layer, x_bits, k):
+    ids, logits = out["ids"], out["logits"]
+    assert np.array_equal(ids, O.select_top_k(logits, k)), "ids differ from the top-k of the GPU's own logits"
+    ref_logits = O.router_logits(x_bits, layer.host_router(), layer.host_logit_bias())
+    assert_close(logits, ref_logits, "logits")
+    assert_close(out["weights"], O.routing_weights(logits.astype(np.float64), ids), "routing weights")
+
+
+@pytest.mark.parametrize("n_tokens,zipf", [(1, False), (13, False), (64, False), (100, True), (128, True)],
+                         ids=["decode", "ragged13", "batch64-uniform", "ragged100-zipf", "prefill128-zipf"])
+def test_layer_forward(moe, layer0, layer0_zipf, n_tokens, zipf):
+    layer = layer0_zipf if zipf else layer0
+    x = hidden(0, n_tokens, n_tokens)
+    out = run_layer(moe, layer, x)
+    assert out["status"] == bq.MOE_OK
+    _check_routing(out, layer, x, K)
+    ref = oracle_layer(layer, x, K, out["ids"])
+    assert_close(bf16_bits_to_f64(out["y"]), ref["y"], f"y (T={n_tokens})")
+
+
+def test_zipf_skews_routing(moe, layer0_zipf):
+    out = run_layer(moe, layer0_zipf, hidden(0, 7, 128))
+    counts = np.bincount(out["ids"].reshape(-1), minlength=E)
+    assert counts.max() >= 30 and (counts == 0).sum() >= 1
+
+
+def test_route_sort_bit_exact(moe, layer0):
+    rng = np.random.default_rng(5)
+    for n_tokens in (1, 7, 64, 128):
+        ids_np = np.stack([rng.permutation(E)[:K] for _ in range(n_tokens)]).astype(np.int32)
+        ids = torch.from_numpy(ids_np).cuda()
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        perm = torch.empty(n_tokens * K, dtype=torch.int32, device="cuda")
+        pos = torch.empty(n_tokens * K, dtype=torch.int32, device="cuda")
+        moe.route_sort(ids, n_tokens, weights_of(layer0).dims, counts, offsets, perm, pos)
+        torch.cuda.synchronize()
+        rc, ro, rp, rq = O.route_sort(ids_np, E)
+        assert np.array_equal(counts.cpu().numpy(), rc)
+        assert np.array_equal(offsets.cpu().numpy(), ro)
+        assert np.array_equal(perm.cpu().numpy(), rp)
+        assert np.array_equal(pos.cpu().numpy(), rq)
+        assert moe.get_error() == bq.MOE_OK
+
+
+def test_route_sort_drops_bad_ids(moe, layer0):
+    ids_np = np.array([[3, 200, 5, -1, 3, 9, 127, 0]], dtype=np.int32).repeat(3, axis=0)
+    ids = torch.from_numpy(ids_np).cuda()
+    n = ids_np.size
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    pos = torch.empty(n, dtype=torch.int32, device="cuda")
+    moe.route_sort(ids, 3, weights_of(layer0).dims, counts, offsets, perm, pos)
+    torch.cuda.synchronize()
+    assert moe.get_error() == bq.MOE_ERR_BAD_EXPERT_ID
+    # reference: out-of-range ids as one extra expert sorted last
+    flat = ids_np.reshape(-1).astype(np.int64)
+    mapped = np.where((flat < 0) | (flat >= E), E, flat).reshape(ids_np.shape)
+    rc, ro, rp, rq = O.route_sort(mapped, E + 1)
+    kept = int(ro[E])
+    assert np.array_equal(counts.cpu().numpy(), rc[:E])
+    assert np.array_equal(offsets.cpu().numpy(), ro[:E + 1])
+    assert np.array_equal(perm.cpu().numpy()[:kept], rp[:kept])
+    want_pos = np.where(mapped.reshape(-1) == E, -1, rq)
+    assert np.array_equal(pos.cpu().numpy(), want_pos)
+
+
+@pytest.mark.parametrize("include_shared", [True, False])
+@pytest.mark.parametrize("n_tokens", [1, 5, 40])
+def test_expert_ffn_forced_routing(moe, layer0, n_tokens, include_shared):
+    rng = np.random.default_rng(n_tokens)
+    ids_np = np.stack([rng.permutation(E)[:K] for _ in range(n_tokens)]).astype(np.int32)
+    if n_tokens > 1:
+        ids_np[1, 3] = ids_np[1, 0]            # a token that picks one expert twice
+    w_np = rng.uniform(0.0, 1.0, size=(n_tokens, K)).astype(np.float32)
+    x_bits = hidden(3, n_tokens, n_tokens)
+    w = weights_of(layer0)
+    x = to_dev_bf16(x_bits)
+    y = torch.empty_like(x)
+    ws = workspace(moe, w, n_tokens)
+    moe.expert_ffn(x, n_tokens, torch.from_numpy(ids_np).cuda(), torch.from_numpy(w_np).cuda(), w, y, ws,
+                   include_shared=include_shared)
+    torch.cuda.synchronize()
+    assert moe.get_error() == bq.MOE_OK
+    ref = O.expert_mix(x_bits, ids_np, w_np.astype(np.float64), HostExperts(layer0),
+                       layer0.host_shared() if include_shared else None)
+    assert_close(bf16_bits_to_f64(from_dev_bf16(y)), ref, "expert_ffn y")
+
+
+def test_expert_ffn_skips_bad_ids(moe, layer0):
+    n_tokens = 4
+    rng = np.random.default_rng(11)
+    ids_np = np.stack([rng.permutation(E)[:K] for _ in range(n_tokens)]).astype(np.int32)
+    ids_np[0, 2] = 128
+    ids_np[2, 7] = -3
+    w_np = rng.uniform(0.1, 1.0, size=(n_tokens, K)).astype(np.float32)
+    x_bits = hidden(4, 0, n_tokens)
+    w = weights_of(layer0)
+    x = to_dev_bf16(x_bits)
+    y = torch.empty_like(x)
+    ws = workspace(moe, w, n_tokens)
+    moe.expert_ffn(x, n_tokens, torch.from_numpy(ids_np).cuda(), torch.from_numpy(w_np).cuda(), w, y, ws)
+    torch.cuda.synchronize()
+    assert moe.get_error() == bq.MOE_ERR_BAD_EXPERT_ID
+    bad = (ids_np < 0) | (ids_np >= E)
+    ref = O.expert_mix(x_bits, np.where(bad, 0, ids_np), np.where(bad, 0.0, w_np.astype(np.float64)),
+                       HostExperts(layer0), layer0.host_shared())
+    assert_close(bf16_bits_to_f64(from_dev_bf16(y)), ref, "y with dropped pairs")
+
+
+def test_router_topk_entry(moe, layer0_zipf):
+    n_tokens = 33
+    x_bits = hidden(5, 0, n_tokens)
+    w = weights_of(layer0_zipf)
+    ids = torch.empty((n_tokens, K), dtype=torch.int32, device="cuda")
+    wts = torch.empty((n_tokens, K), dtype=torch.float32, device="cuda")
+    logits = torch.empty((n_tokens, E), dtype=torch.float32, device="cuda")
+    moe.router_topk(to_dev_bf16(x_bits), n_tokens, w, ids, wts, workspace(moe, w, n_tokens), logits=logits)
+    torch.cuda.synchronize()
+    out = {"ids": ids.cpu().numpy(), "logits": logits.cpu().numpy(), "weights": wts.cpu().numpy()}
+    _check_routing(out, layer0_zipf, x_bits, K)
+
+
+def test_residual_stack_teacher_forced(moe):
+    layers = [DeviceLayer(s, H, I, E) for s in (0, 1, 2)]
+    for n_tokens in (1, 8):
+        h_bits = hidden(1000, 0, n_tokens, rms=False)
+        h = to_dev_bf16(h_bits)
+        ws = workspace(moe, weights_of(layers[0]), n_tokens)
+        for layer in layers:
+            w = weights_of(layer)
+            h_in = from_dev_bf16(h)
+            y = torch.empty_like(h)
+            xo = torch.empty_like(h)
+            ids = torch.empty((n_tokens, K), dtype=torch.int32, device="cuda")
+            logits = torch.empty((n_tokens, E), dtype=torch.float32, device="cuda")
+            moe.layer_forward_residual(h, n_tokens, w, ws, y_out=y, x_out=xo, ids_out=ids, logits_out=logits)
+            torch.cuda.synchronize()
+            assert moe.get_error() == bq.MOE_OK
+            x_gpu = from_dev_bf16(xo)
+            x_ref = O.rmsnorm_no_scale(h_in)
+            diff = np.abs(x_gpu.astype(np.int32) - x_ref.astype(np.int32))
+            assert diff.max() <= 1 and (diff > 0).mean() < 1e-3, "rmsnorm differs by more than rounding"
+            ids_np = ids.cpu().numpy()
+            assert np.array_equal(ids_np, O.select_top_k(logits.cpu().numpy(), K))
+            ref = oracle_layer(layer, x_gpu, K, ids_np)
+            y_gpu = from_dev_bf16(y)
+            assert_close(bf16_bits_to_f64(y_gpu), ref["y"], "stack layer y")
+            assert np.array_equal(from_dev_bf16(h), O.residual_add(h_in, y_gpu))
+
+
+@pytest.mark.parametrize("n_tokens", [1, 128])
+def test_deterministic(moe, layer0_zipf, n_tokens):
+    x = hidden(9, 0, n_tokens)
+    a = run_layer(moe, layer0_zipf, x)
+    b = run_layer(moe, layer0_zipf, x)
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["ids"], b["ids"])
+    assert np.array_equal(a["logits"].view(np.uint32), b["logits"].view(np.uint32))
+
+
+@pytest.mark.parametrize("hidden_dim,inter,n_experts,k,n_tokens", [
+    (128, 64, 8, 2, 1), (128, 64, 8, 2, 33), (256, 128, 4, 4, 5), (192, 128, 16, 8, 17), (64, 64, 1, 1, 3),
+])
+def test_small_shapes(moe, hidden_dim, inter, n_experts, k, n_tokens):
+    layer = DeviceLayer(7, hidden_dim, inter, n_experts, zipf=n_experts >= 8)
+    x = hidden(7, n_tokens, n_tokens, hidden_dim)
+    out = run_layer(moe, layer, x, k)
+    assert out["status"] == bq.MOE_OK
+    _check_routing(out, layer, x, k)
+    ref = oracle_layer(layer, x, k, out["ids"])
+    assert_close(bf16_bits_to_f64(out["y"]), ref["y"], "small-shape y")
+
+
+def test_argument_errors(moe, layer0):
+    w = weights_of(layer0)
+    x = to_dev_bf16(hidden(0, 0, 2))
+    y = torch.empty_like(x)
+    ws = workspace(moe, w, 2)
+    for n in (0, 129):
+        with pytest.raises(bq.MoeError) as ei:
+            moe.layer_forward(x, n, w, y, ws)
+        assert ei.value.status == bq.MOE_ERR_INVALID_ARG
+    with pytest.raises(bq.MoeError) as ei:
+        moe.layer_forward(x, 2, w, y, ws[:1024])
+    assert ei.value.status == bq.MOE_ERR_WORKSPACE
+    with pytest.raises(bq.MoeError) as ei:
+        moe.layer_forward(x.view(-1)[1:], 1, w, y, ws)
+    assert ei.value.status == bq.MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert moe.get_error() == bq.MOE_OK
+
+
+def test_bounded_wait_reports_timeout(moe):
+    moe.selftest_wait_timeout(5_000_000)
+    assert moe.get_error() == bq.MOE_ERR_TIMEOUT
+    assert moe.get_error() == bq.MOE_OK     # cleared by the read
