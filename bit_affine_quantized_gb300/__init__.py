@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH):
         "moe_layer_forward": (I, [V, V, I, P(LayerWeights), V, V, V, V, V, Z, V]),
         "moe_layer_forward_residual": (I, [V, V, I, P(LayerWeights), V, V, V, V, V, Z, V]),
         "moe_selftest_wait_timeout": (I, [V, ctypes.c_ulonglong, V]),
+        "moe_set_trace": (I, [V, V, I]),
         "moe_get_error": (I, [V, P(I)]),
     }
     for name, (res, args) in proto.items():
@@ -190,6 +191,10 @@ class Moe:
                                                         _ptr(x_out), _ptr(ids_out), _ptr(logits_out), _ptr(ws),
                                                         ws.numel() * ws.element_size(), _stream(stream)),
                     "moe_layer_forward_residual")
+
+    def set_trace(self, buffer=None, n_launches: int = 0):
+        """Record per-launch device timestamps into `buffer` (u64 x 4 x n)."""
+        self._check(self.lib.moe_set_trace(self.h, _ptr(buffer), n_launches), "moe_set_trace")
 
     def selftest_wait_timeout(self, limit_ns: int, stream=None):
         self._check(self.lib.moe_selftest_wait_timeout(self.h, limit_ns, _stream(stream)), "moe_selftest_wait_timeout")

@@ -13,7 +13,21 @@ struct moe_handle {
   unsigned *dwords;  // [0] device error bits, [1] router ticket counter
   bool pdl;
   int prefetch_max;  // bytes; 0 disables the L2 prefetch of selected experts
+  unsigned long long *trace;  // caller's trace buffer (nullable)
+  int trace_groups;           // 4-slot groups in it
+  int trace_next;             // next group handed to a launch
 };
+
+namespace {
+// Trace slots of the next `n` launches (null when tracing is off).
+unsigned long long *take_trace(moe_handle *h, int n) {
+  if (!h->trace || h->trace_groups < n) return nullptr;
+  if (h->trace_next + n > h->trace_groups) h->trace_next = 0;
+  unsigned long long *p = h->trace + 4 * (size_t)h->trace_next;
+  h->trace_next += n;
+  return p;
+}
+}  // namespace
 
 namespace {
 
@@ -151,6 +165,7 @@ int run_router(moe_handle *h, const moe_layer_weights *w, int T, const void *x, 
   a.r = routing_in(ws, L);
   a.counter = h->dwords + 1;
   a.err = h->dwords;
+  a.trace = take_trace(h, 1);
   a.normalize = hres != nullptr;
   a.prefetch_bytes_max = h->prefetch_max;
   return cuda_status(moe::launch_router(a, st, h->pdl));
@@ -169,8 +184,12 @@ int run_ffn(moe_handle *h, const moe_layer_weights *w, int T, const void *x, con
   a.y = (uint16_t *)y;
   a.hres = (uint16_t *)hres;
   a.include_shared = include_shared;
+  // W_down of the selected experts fits L2 comfortably only for small T
+  a.prefetch_down = h->prefetch_max > 0 && (size_t)(w->dims.top_k * T + 1) * blob_extent(*w) <= (size_t)h->prefetch_max;
   a.err = h->dwords;
+  a.trace = take_trace(h, 1);
   cudaError_t e = moe::launch_gateup(a, st, h->pdl);
+  a.trace = take_trace(h, 2);  // down (+ combine)
   if (e == cudaSuccess) e = moe::launch_down(a, st, h->pdl);
   return cuda_status(e);
 }
@@ -265,6 +284,7 @@ int moe_route_sort(moe_handle *h, const int32_t *ids, int n_tokens, const moe_di
   a.r.pos = pos;
   a.include_shared = 0;
   a.err = h->dwords;
+  a.trace = take_trace(h, 1);
   return cuda_status(moe::launch_sort(a, (cudaStream_t)stream, h->pdl));
 }
 
@@ -290,6 +310,7 @@ int moe_expert_ffn(moe_handle *h, const void *x, int n_tokens, const int32_t *id
   sa.r = r;
   sa.include_shared = include_shared ? 1 : 0;
   sa.err = h->dwords;
+  sa.trace = take_trace(h, 1);
   cudaError_t e = moe::launch_sort(sa, (cudaStream_t)stream, h->pdl);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return run_ffn(h, w, n_tokens, x, r, include_shared ? 1 : 0, y, nullptr, wsb, (cudaStream_t)stream);
@@ -329,6 +350,14 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens, const 
                        (cudaStream_t)stream)))
     return st;
   return run_ffn(h, w, n_tokens, wsb + L.xn, routing_in(wsb, L), 1, y_out, hidden, wsb, (cudaStream_t)stream);
+}
+
+int moe_set_trace(moe_handle *h, unsigned long long *buffer, int n_launches) {
+  if (!h || (buffer && n_launches < 1) || (buffer && !aligned(buffer, 8))) return MOE_ERR_INVALID_ARG;
+  h->trace = buffer;
+  h->trace_groups = buffer ? n_launches : 0;
+  h->trace_next = 0;
+  return MOE_OK;
 }
 
 int moe_selftest_wait_timeout(moe_handle *h, unsigned long long limit_ns, moe_stream_t stream) {

@@ -198,4 +198,16 @@ __device__ __forceinline__ void set_error(unsigned *err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }
 
+// Optional launch trace (null when tracing is off).  Each launch owns 4
+// u64 slots, all combined with atomicMax so a zeroed buffer is the reset
+// state: [0] ~first block entry, [1] ~first block past the dependency wait,
+// [2] last block with its weights in shared memory, [3] last block exit.
+enum TraceSlot { kTrEntry = 0, kTrWaited = 1, kTrLoaded = 2, kTrExit = 3 };
+__device__ __forceinline__ void trace_min(unsigned long long *tr, int slot) {
+  if (tr) atomicMax(tr + slot, ~global_ns());
+}
+__device__ __forceinline__ void trace_max(unsigned long long *tr, int slot) {
+  if (tr) atomicMax(tr + slot, global_ns());
+}
+
 }  // namespace moe

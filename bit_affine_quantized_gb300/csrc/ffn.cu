@@ -34,8 +34,9 @@
 namespace moe {
 
 namespace {
-constexpr int kThreads = 128;
-constexpr int kWarps = 4;
+constexpr int kThreads = 256;  // gate/up and single-token down blocks
+constexpr int kWarps = 8;
+constexpr int kDgThreads = 128;  // grouped down: 4 warps x 16 rows
 constexpr int kRows = 16;      // rows of one mma tile
 constexpr int kDownRows = 64;  // output rows per grouped-down block
 constexpr int kTokTile = 8;    // tokens per mma N
@@ -118,13 +119,17 @@ __device__ __forceinline__ float hi_f16(uint32_t w) { return __half2float(__usho
 // Stages one 64-wide group of a 16-bit activation row into the permuted
 // shared-memory order and returns the group's sum (fp32, element order).
 template <bool kHalf>
-__device__ __forceinline__ float stage_group(const uint16_t *src_row, int g, uint8_t *dst_row) {
+__device__ __forceinline__ float stage_group(const uint16_t *__restrict__ src_row, int g, uint8_t *__restrict__ dst_row) {
   const uint4 *src = reinterpret_cast<const uint4 *>(src_row + g * kGroup);
   uint2 *dst = reinterpret_cast<uint2 *>(dst_row + g * 128);
+  // all eight 16-byte loads in flight before any shared-memory store
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + i);
   float sum = 0.f;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const uint4 v0 = src[2 * c], v1 = src[2 * c + 1];
+    const uint4 v0 = v[2 * c], v1 = v[2 * c + 1];
     const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     uint32_t out[8];
     permute_quarter(in, out);
@@ -202,17 +207,46 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(const FfnArgs a) {
     }
   };
 
+  // Decode: this block also warms L2 with its share (1/gridDim.x of the
+  // rows) of the same expert's W_down, so the down kernel reads from L2
+  // while the HBM keeps streaming.  Ranges are rounded inwards to 16 bytes.
+  auto prefetch_down = [&](const uint8_t *blob) {
+    if (!a.prefetch_down || warp != 1 || lane != 0) return;
+    const int GI = I / kGroup;
+    const int per = (H + gridDim.x - 1) / gridDim.x;
+    const int nb = blockIdx.x * per, ne = min(H, nb + per);
+    if (nb >= ne) return;
+    const size_t ranges[3][2] = {{a.w.off.down_q + (size_t)nb * (I / 2), (size_t)(ne - nb) * (I / 2)},
+                                 {a.w.off.down_s + (size_t)nb * GI * 2, (size_t)(ne - nb) * GI * 2},
+                                 {a.w.off.down_b + (size_t)nb * GI * 2, (size_t)(ne - nb) * GI * 2}};
+    for (int i = 0; i < 3; ++i) {
+      const uintptr_t s0 = ((uintptr_t)(blob + ranges[i][0]) + 15) & ~(uintptr_t)15;
+      const uintptr_t s1 = ((uintptr_t)(blob + ranges[i][0] + ranges[i][1])) & ~(uintptr_t)15;
+      for (uintptr_t p = s0; p < s1; p += 65536)
+        prefetch_l2(reinterpret_cast<const void *>(p), (uint32_t)min((uintptr_t)65536, s1 - p));
+    }
+  };
+
   // The shared expert (slot 0) needs no routing: start its copies before
   // waiting on the previous kernel.
+  const bool tracer = blockIdx.x == 0 && blockIdx.y == 0 && tid == 0;
+  if (tracer) trace_min(a.trace, kTrEntry);
   const bool early = a.include_shared && slot == 0;
-  if (early) issue(a.w.shared);
+  if (early) {
+    issue(a.w.shared);
+    prefetch_down(a.w.shared);
+  }
   pdl_wait();
+  if (tracer) trace_min(a.trace, kTrWaited);
   const int nact = a.r.n_act[0];
   if (slot >= nact) return;
   const int e = a.r.act_e[slot];
   const int beg = a.r.act_beg[slot];
   const int cnt = a.r.act_cnt[slot];
-  if (!early) issue(slot_blob(a, e));
+  if (!early) {
+    issue(slot_blob(a, e));
+    prefetch_down(slot_blob(a, e));
+  }
   pdl_launch_dependents();
 
   const int r = lane >> 2, c = lane & 3;
@@ -234,6 +268,7 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(const FfnArgs a) {
     __syncthreads();
     if (!ready) {
       if (!block_wait(bar, 0, a.err)) return;
+      if (tid == 0) trace_max(a.trace, kTrLoaded);
       for (int it = tid; it < 2 * kRows * G; it += kThreads) {
         const int m = it / (kRows * G), rem = it - m * kRows * G;
         const float s = bf16_bits_to_float(sraw[(2 * m) * kRows * G + rem]);
@@ -311,6 +346,7 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(const FfnArgs a) {
     }
     __syncthreads();
   }
+  if (tid == 0) trace_max(a.trace, kTrExit);
 }
 
 // ------------------------------------------------------------------ down, T == 1
@@ -356,12 +392,15 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(const FfnArgs a) 
     }
   };
 
+  const bool tracer = blockIdx.x == 0 && tid == 0;
+  if (tracer) trace_min(a.trace, kTrEntry);
   if (a.include_shared && warp == 0) {
     if (lane == 0) mbar_arrive_expect_tx(&bar[0], tile_tx);
     __syncwarp();
     for (int ci = lane; ci < nq + 2; ci += 32) copy_one(k, a.w.shared, ci, &bar[0]);
   }
   pdl_wait();
+  if (tracer) trace_min(a.trace, kTrWaited);
   const int n_valid = a.r.offsets[E];
   const int a0 = a.include_shared ? 1 : 0;
   if (warp == 0 && n_valid > 0) {
@@ -391,6 +430,7 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(const FfnArgs a) 
   __syncthreads();
   if (a.include_shared && !block_wait(&bar[0], 0, a.err)) return;
   if (n_valid > 0 && !block_wait(&bar[1], 0, a.err)) return;
+  if (tid == 0) trace_max(a.trace, kTrLoaded);
   for (int it = tid; it < nslot * kRows * GI; it += kThreads) {
     const int s = it / (kRows * GI), rem = it - s * kRows * GI;
     if (s < n_valid || (s == k && a.include_shared)) {
@@ -445,11 +485,12 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(const FfnArgs a) 
     if (a.y) a.y[n0 + tid] = yb;
     if (a.hres) a.hres[n0 + tid] = float_to_bf16_bits(bf16_bits_to_float(a.hres[n0 + tid]) + bf16_bits_to_float(yb));
   }
+  if (tid == 0) trace_max(a.trace, kTrExit);
   (void)H;
 }
 
 // ------------------------------------------------------------------ down, grouped
-__global__ void __launch_bounds__(kThreads) down_grouped_kernel(const FfnArgs a) {
+__global__ void __launch_bounds__(kDgThreads) down_grouped_kernel(const FfnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = a.d.H, I = a.d.I, k = a.d.k;
   const int GI = I / kGroup;
@@ -488,9 +529,12 @@ __global__ void __launch_bounds__(kThreads) down_grouped_kernel(const FfnArgs a)
       }
     }
   };
+  const bool tracer = blockIdx.x == 0 && blockIdx.y == 0 && tid == 0;
+  if (tracer) trace_min(a.trace, kTrEntry);
   const bool early = a.include_shared && slot == 0;
   if (early) issue(a.w.shared);
   pdl_wait();
+  if (tracer) trace_min(a.trace, kTrWaited);
   const int nact = a.r.n_act[0];
   if (slot >= nact) return;
   const int e = a.r.act_e[slot];
@@ -504,7 +548,7 @@ __global__ void __launch_bounds__(kThreads) down_grouped_kernel(const FfnArgs a)
   bool ready = false;
   for (int j0 = 0; j0 < cnt; j0 += kTokTile) {
     const int nt = min(kTokTile, cnt - j0);
-    for (int it = tid; it < nt * GI; it += kThreads) {
+    for (int it = tid; it < nt * GI; it += kDgThreads) {
       const int n = it / GI, g = it - n * GI;
       shs[n * GI + g] = stage_group<true>(reinterpret_cast<const uint16_t *>(a.hbuf) + (size_t)(beg + j0 + n) * I,
                                           g, sh + n * L.hp);
@@ -512,7 +556,8 @@ __global__ void __launch_bounds__(kThreads) down_grouped_kernel(const FfnArgs a)
     __syncthreads();
     if (!ready) {
       if (!block_wait(bar, 0, a.err)) return;
-      for (int it = tid; it < kDownRows * GI; it += kThreads) {
+      if (tid == 0) trace_max(a.trace, kTrLoaded);
+      for (int it = tid; it < kDownRows * GI; it += kDgThreads) {
         ssb[it] = make_float2(bf16_bits_to_float(sraw[it]), bf16_bits_to_float(sraw[kDownRows * GI + it]));
       }
       __syncthreads();
@@ -558,6 +603,7 @@ __global__ void __launch_bounds__(kThreads) down_grouped_kernel(const FfnArgs a)
     }
     __syncthreads();
   }
+  if (tid == 0) trace_max(a.trace, kTrExit);
   (void)k;
 }
 
@@ -565,8 +611,11 @@ __global__ void __launch_bounds__(kThreads) down_grouped_kernel(const FfnArgs a)
 __global__ void __launch_bounds__(256) combine_kernel(const FfnArgs a) {
   const int H = a.d.H, k = a.d.k, T = a.d.T;
   const int t = blockIdx.x;
+  const bool tracer = t == 0 && threadIdx.x == 0;
+  if (tracer) trace_min(a.trace, kTrEntry);
   pdl_wait();
   pdl_launch_dependents();
+  if (tracer) trace_min(a.trace, kTrWaited);
   int pos[kMaxTopK];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) pos[j] = j < k ? a.r.pos[t * k + j] : -1;
@@ -603,6 +652,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const FfnArgs a) {
           make_uint2((uint32_t)nb[0] | ((uint32_t)nb[1] << 16), (uint32_t)nb[2] | ((uint32_t)nb[3] << 16));
     }
   }
+  if (threadIdx.x == 0) trace_max(a.trace, kTrExit);
 }
 
 // ------------------------------------------------------------------ host side
@@ -629,9 +679,11 @@ cudaError_t launch_down(const FfnArgs &a, cudaStream_t st, bool pdl) {
   if (use_down_decode(a.d))
     return launch_k(down_decode_kernel, dim3(a.d.H / kRows), dim3(kThreads), down_decode_smem(a.d), st, pdl, a);
   cudaError_t e = launch_k(down_grouped_kernel, dim3(a.d.H / kDownRows, max_slots(a.d, a.include_shared)),
-                           dim3(kThreads), down_grouped_smem(a.d), st, pdl, a);
+                           dim3(kDgThreads), down_grouped_smem(a.d), st, pdl, a);
   if (e != cudaSuccess) return e;
-  return launch_k(combine_kernel, dim3(a.d.T), dim3(256), 0, st, pdl, a);
+  FfnArgs c = a;
+  if (c.trace) c.trace += 4;  // the combine launch traces into the next slot group
+  return launch_k(combine_kernel, dim3(a.d.T), dim3(256), 0, st, pdl, c);
 }
 
 cudaError_t ffn_set_attributes() {

@@ -22,6 +22,7 @@ struct RouterArgs {
   Routing r;
   unsigned *counter;       // last-block ticket, zero between launches
   unsigned *err;
+  unsigned long long *trace;  // nullable: 4 trace slots of this launch (common.cuh)
   int normalize;
   int prefetch_bytes_max;  // L2-prefetch the selected experts if their total fits
 };
@@ -36,7 +37,9 @@ struct FfnArgs {
   uint16_t *y;             // nullable bf16 [T, H]
   uint16_t *hres;          // nullable bf16 [T, H]: hres <- bf16(hres + y)
   int include_shared;
+  int prefetch_down;       // gate/up blocks warm L2 with the selected W_down
   unsigned *err;
+  unsigned long long *trace;  // nullable: 4 trace slots of this launch (common.cuh)
 };
 
 struct SortArgs {
@@ -45,6 +48,7 @@ struct SortArgs {
   Routing r;               // counts/offsets/perm/pos required; act_* nullable
   int include_shared;
   unsigned *err;
+  unsigned long long *trace;  // nullable: 4 trace slots of this launch (common.cuh)
 };
 
 // smem budgets (bytes) for a given shape; 0 = shape not supported by that kernel

@@ -139,6 +139,75 @@ __device__ void group_pairs(const int32_t *ids, int T, int k, int E, const Routi
   }
 }
 
+// Same result as group_pairs for n = T*k <= 32 pairs, computed by one warp
+// with shuffles only (the decode path: no block-wide barriers).  Lane p owns
+// pair p.
+__device__ void group_pairs_warp(const int32_t *ids, int T, int k, int E, const Routing &r, int include_shared,
+                                 unsigned *err) {
+  const int lane = threadIdx.x & 31;
+  const int n = T * k;
+  const int e = lane < n ? ids[lane] : -1;
+  const bool valid = lane < n && e >= 0 && e < E;
+  if (__any_sync(0xffffffffu, lane < n && !valid) && lane == 0) set_error(err, kErrBadId);
+  const int key = valid ? e : 0x40000000 + lane;  // invalid pairs sort after every expert
+  // stable rank: pairs with a smaller key, or the same key and a smaller index
+  int rank = 0, nvalid = 0;
+  for (int q = 0; q < n; ++q) {
+    const int kq = __shfl_sync(0xffffffffu, key, q);
+    rank += (kq < key) || (kq == key && q < lane);
+    nvalid += kq < 0x40000000;
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const bool leader = valid && (__popc(peers & lanemask_lt()) == 0);
+  // distinct experts below mine (for the active-slot index)
+  int below = 0;
+  for (int q = 0; q < n; ++q) {
+    const int kq = __shfl_sync(0xffffffffu, key, q);
+    const bool lq = __shfl_sync(0xffffffffu, leader, q);
+    below += lq && kq < key;
+  }
+  // every lane runs the same trip count: the shuffles need the whole warp
+  for (int x0 = 0; x0 < E; x0 += 32) {
+    const int x = x0 + lane;
+    int c = 0, lt = 0;
+    for (int q = 0; q < n; ++q) {
+      const int kq = __shfl_sync(0xffffffffu, key, q);
+      c += kq == x;
+      lt += kq < x;
+    }
+    if (x < E) {
+      r.counts[x] = c;
+      r.offsets[x] = lt;
+    }
+  }
+  if (lane == 0) r.offsets[E] = nvalid;
+  if (lane < n) {
+    if (valid) {
+      r.perm[rank] = lane;
+      r.pos[lane] = rank;
+    } else {
+      r.pos[lane] = -1;
+    }
+  }
+  if (r.act_e != nullptr) {
+    const int a0 = include_shared ? 1 : 0;
+    if (leader) {
+      r.act_e[a0 + below] = e;
+      r.act_beg[a0 + below] = rank;
+      r.act_cnt[a0 + below] = __popc(peers);
+    }
+    const int ndist = __popc(__ballot_sync(0xffffffffu, leader));
+    if (lane == 0) {
+      if (include_shared) {
+        r.act_e[0] = kSharedSlot;
+        r.act_beg[0] = T * k;
+        r.act_cnt[0] = T;
+      }
+      r.n_act[0] = a0 + ndist;
+    }
+  }
+}
+
 // -------------------------------------------------------------- top-k
 __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -221,10 +290,14 @@ __device__ void topk_token(const float *logits_row, int E, int k, int32_t *ids_o
 }
 
 // -------------------------------------------------------------- router
+// Up to kMaxRouterWords 32-bit code words per lane (H <= 4096).
+constexpr int kMaxRouterWords = 32;
+constexpr int kMaxVec = 2;  // 16-byte activation vectors per thread (H <= 4096)
+
 template <int TB>
 __global__ void __launch_bounds__(kThreads) router_kernel(const RouterArgs a) {
   extern __shared__ __align__(16) float sx[];  // [TB][H] fp32 copy of the inputs
-  __shared__ float s_red[kWarps];
+  __shared__ float s_red[TB][kWarps];
   __shared__ float s_inv[TB];
   __shared__ int s_last;
   const int H = a.d.H, E = a.d.E, T = a.d.T, k = a.d.k, G = H / kGroup;
@@ -232,90 +305,136 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterArgs a) {
   const int t0 = blockIdx.y * TB;
   const int tb = min(TB, T - t0);
   const int nblocks = gridDim.x * gridDim.y;
-  const int bid = blockIdx.y * gridDim.x + blockIdx.x;
+  const int nwords = H / 4;  // code words per row
 
-  // Weights never change between launches: warm L2 with this block's share
-  // of the shared expert before waiting on the previous kernel.
-  if (a.prefetch_bytes_max > 0 && tid == 0) {
-    const size_t blob_bytes = a.w.blob_bytes;
-    const size_t chunk = ((blob_bytes + nblocks - 1) / nblocks + 15) & ~(size_t)15;
-    const size_t beg = (size_t)bid * chunk;
-    const size_t end = min(blob_bytes, beg + chunk);
-    for (size_t o = beg; o < end; o += 32768) prefetch_l2(a.w.shared + o, (uint32_t)min((size_t)32768, end - o));
-  }
-  pdl_wait();
-  pdl_launch_dependents();
-
-  if (a.normalize) {
-    // rmsnorm without scale of each token of the tile (fixed-order sums)
-    for (int n = 0; n < tb; ++n) {
-      const uint16_t *hrow = a.hres + (size_t)(t0 + n) * H;
-      float ss = 0.f;
-      for (int i = tid; i < H; i += kThreads) {
-        const float v = bf16_bits_to_float(hrow[i]);
-        ss = fmaf(v, v, ss);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      if (lane == 0) s_red[warp] = ss;
-      __syncthreads();
-      if (tid == 0) {
-        float tot = 0.f;
-        for (int w = 0; w < kWarps; ++w) tot += s_red[w];
-        s_inv[n] = 1.0f / sqrtf(tot / (float)H + 1e-6f);
-      }
-      __syncthreads();
-    }
-    for (int n = 0; n < tb; ++n) {
-      const size_t rowoff = (size_t)(t0 + n) * H;
-      for (int i = tid; i < H; i += kThreads) {
-        const uint16_t xb = float_to_bf16_bits(bf16_bits_to_float(a.hres[rowoff + i]) * s_inv[n]);
-        sx[n * H + i] = bf16_bits_to_float(xb);
-        if (blockIdx.x == 0) {
-          a.xn[rowoff + i] = xb;
-          if (a.xn_user) a.xn_user[rowoff + i] = xb;
-        }
-      }
-    }
-  } else {
-    for (int n = 0; n < tb; ++n) {
-      const size_t rowoff = (size_t)(t0 + n) * H;
-      for (int i = tid; i < H; i += kThreads) sx[n * H + i] = bf16_bits_to_float(a.x[rowoff + i]);
-    }
-  }
-  __syncthreads();
-
-  // logits of expert e (one warp) for the tile's tokens: w = q*s + b in
-  // fp32, dotted with x; lane l covers codes 4l + 128m.
+  // Router weights never change: pull this warp's expert row into registers
+  // before waiting on the previous kernel.
+  const bool tracer = blockIdx.x == 0 && blockIdx.y == 0 && tid == 0;
+  if (tracer) trace_min(a.trace, kTrEntry);
   const int e = blockIdx.x * kExpertsPerBlock + warp;
-  float acc[TB];
-#pragma unroll
-  for (int n = 0; n < TB; ++n) acc[n] = 0.f;
+  uint32_t wq[kMaxRouterWords], wsb[kMaxRouterWords];
   if (e < E) {
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.w.router_q + (size_t)e * H);
     const uint16_t *srow = a.w.router_s + (size_t)e * G;
     const uint16_t *brow = a.w.router_b + (size_t)e * G;
-    for (int c = lane; c < H / 4; c += 32) {
-      const uint32_t wd = __ldg(qrow + c);
-      const int g = c >> 4;
-      const float s = bf16_bits_to_float(__ldg(srow + g));
-      const float b = bf16_bits_to_float(__ldg(brow + g));
-      float w4[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float q = __uint_as_float(0x4B000000u | ((wd >> (8 * i)) & 0xFFu)) - 8388608.0f;
-        w4[i] = fmaf(q, s, b);
+    for (int m = 0; m < kMaxRouterWords; ++m) {
+      const int c = lane + 32 * m;
+      if (c < nwords) {
+        wq[m] = __ldg(qrow + c);
+        wsb[m] = (uint32_t)__ldg(srow + (c >> 4)) | ((uint32_t)__ldg(brow + (c >> 4)) << 16);
+      }
+    }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tracer) trace_min(a.trace, kTrWaited);
+
+  // stage the tile's inputs (fp32) -- all loads first, then the stores
+  const int nvec = H / 8;
+  uint4 u[TB][kMaxVec];
+#pragma unroll
+  for (int n = 0; n < TB; ++n)
+#pragma unroll
+    for (int v = 0; v < kMaxVec; ++v) {
+      const int idx = tid + kThreads * v;
+      if (n < tb && idx < nvec) {
+        const uint16_t *src = (a.normalize ? a.hres : a.x) + (size_t)(t0 + n) * H;
+        u[n][v] = *reinterpret_cast<const uint4 *>(src + 8 * idx);
+      }
+    }
+  if (a.normalize) {
+    // rmsnorm without scale (fixed-order sums)
+#pragma unroll
+    for (int n = 0; n < TB; ++n) {
+      float ss = 0.f;
+#pragma unroll
+      for (int v = 0; v < kMaxVec; ++v) {
+        const int idx = tid + kThreads * v;
+        if (n < tb && idx < nvec) {
+          const uint32_t w4[4] = {u[n][v].x, u[n][v].y, u[n][v].z, u[n][v].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+          }
+        }
       }
 #pragma unroll
-      for (int n = 0; n < TB; ++n) {
-        if (n < tb) {
-          const float4 xv = *reinterpret_cast<const float4 *>(sx + n * H + 4 * c);
-          float t = acc[n];
-          t = fmaf(w4[0], xv.x, t);
-          t = fmaf(w4[1], xv.y, t);
-          t = fmaf(w4[2], xv.z, t);
-          t = fmaf(w4[3], xv.w, t);
-          acc[n] = t;
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if (lane == 0) s_red[n][warp] = ss;
+    }
+    __syncthreads();
+    if (tid < tb) {
+      float tot = 0.f;
+      for (int w = 0; w < kWarps; ++w) tot += s_red[tid][w];
+      s_inv[tid] = 1.0f / sqrtf(tot / (float)H + 1e-6f);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int n = 0; n < TB; ++n)
+#pragma unroll
+    for (int v = 0; v < kMaxVec; ++v) {
+      const int idx = tid + kThreads * v;
+      if (n < tb && idx < nvec) {
+        const uint32_t w4[4] = {u[n][v].x, u[n][v].y, u[n][v].z, u[n][v].w};
+        float f[8];
+        uint32_t ob[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+          if (a.normalize) {
+            const uint16_t lb = float_to_bf16_bits(lo * s_inv[n]), hb = float_to_bf16_bits(hi * s_inv[n]);
+            ob[q] = (uint32_t)lb | ((uint32_t)hb << 16);
+            lo = bf16_bits_to_float(lb);
+            hi = bf16_bits_to_float(hb);
+          }
+          f[2 * q] = lo;
+          f[2 * q + 1] = hi;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(sx + n * H + 8 * idx);
+        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        if (a.normalize && blockIdx.x == 0) {
+          const size_t o = (size_t)(t0 + n) * H + 8 * idx;
+          *reinterpret_cast<uint4 *>(a.xn + o) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+          if (a.xn_user) *reinterpret_cast<uint4 *>(a.xn_user + o) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        }
+      }
+    }
+  __syncthreads();
+
+  // logits of expert e (one warp) for the tile's tokens: w = q*s + b in
+  // fp32, dotted with x; lane l covers codes 4c..4c+3, c = l + 32m.
+  float acc[TB];
+#pragma unroll
+  for (int n = 0; n < TB; ++n) acc[n] = 0.f;
+  if (e < E) {
+#pragma unroll
+    for (int m = 0; m < kMaxRouterWords; ++m) {
+      const int c = lane + 32 * m;
+      if (c < nwords) {
+        const float s = bf16_bits_to_float(wsb[m] & 0xFFFFu);
+        const float b = bf16_bits_to_float(wsb[m] >> 16);
+        float w4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float q = __uint_as_float(0x4B000000u | ((wq[m] >> (8 * i)) & 0xFFu)) - 8388608.0f;
+          w4[i] = fmaf(q, s, b);
+        }
+#pragma unroll
+        for (int n = 0; n < TB; ++n) {
+          if (n < tb) {
+            const float4 xv = *reinterpret_cast<const float4 *>(sx + n * H + 4 * c);
+            float t = acc[n];
+            t = fmaf(w4[0], xv.x, t);
+            t = fmaf(w4[1], xv.y, t);
+            t = fmaf(w4[2], xv.z, t);
+            t = fmaf(w4[3], xv.w, t);
+            acc[n] = t;
+          }
         }
       }
     }
@@ -342,27 +461,31 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (tid == 0) trace_max(a.trace, kTrLoaded);  // all logits written
+  if (T * k <= 32) {
+    // decode-sized: one warp does everything, no block barriers
+    if (warp == 0) {
+      for (int t = 0; t < T; ++t)
+        topk_token(a.logits + (size_t)t * E, E, k, a.r.ids + t * k, a.r.wts + t * k,
+                   a.ids_user ? a.ids_user + t * k : nullptr, a.wts_user ? a.wts_user + t * k : nullptr, a.err);
+      __syncwarp();
+      group_pairs_warp(a.r.ids, T, k, E, a.r, 1, a.err);
+      if (lane == 0) {
+        *a.counter = 0u;
+        trace_max(a.trace, kTrExit);
+      }
+    }
+    return;
+  }
   for (int t = warp; t < T; t += kWarps)
     topk_token(a.logits + (size_t)t * E, E, k, a.r.ids + t * k, a.r.wts + t * k,
                a.ids_user ? a.ids_user + t * k : nullptr, a.wts_user ? a.wts_user + t * k : nullptr, a.err);
   __syncthreads();
   group_pairs(a.r.ids, T, k, E, a.r, 1, a.err);
-
-  // warm L2 with the selected experts' blobs while the next kernel launches
-  if (a.prefetch_bytes_max > 0) {
-    const int nact = a.r.n_act[0];
-    const size_t blob_bytes = a.w.blob_bytes;
-    if ((size_t)(nact - 1) * blob_bytes <= (size_t)a.prefetch_bytes_max) {
-      const size_t nchunks = (blob_bytes + 32767) / 32768;
-      for (size_t it = tid; it < (size_t)(nact - 1) * nchunks; it += kThreads) {
-        const int slot = 1 + (int)(it / nchunks);
-        const size_t o = (it % nchunks) * 32768;
-        const int ex = a.r.act_e[slot];
-        prefetch_l2(a.w.experts + (size_t)ex * a.w.stride + o, (uint32_t)min((size_t)32768, blob_bytes - o));
-      }
-    }
+  if (tid == 0) {
+    *a.counter = 0u;
+    trace_max(a.trace, kTrExit);
   }
-  if (tid == 0) *a.counter = 0u;
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
@@ -385,6 +508,10 @@ cudaError_t launch_wait_timeout(unsigned *err, unsigned long long limit_ns, cuda
 __global__ void __launch_bounds__(kThreads) sort_kernel(const SortArgs a) {
   pdl_wait();
   pdl_launch_dependents();
+  if (a.T * a.k <= 32) {
+    if (threadIdx.x < 32) group_pairs_warp(a.ids, a.T, a.k, a.E, a.r, a.include_shared, a.err);
+    return;
+  }
   group_pairs(a.ids, a.T, a.k, a.E, a.r, a.include_shared, a.err);
 }
 

@@ -187,6 +187,19 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
                                int32_t *ids_out, float *logits_out, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* Launch tracing (diagnostics).  With a non-null device buffer of
+ * 4 * n_launches u64, each subsequent kernel launch by this handle takes the
+ * next 4 slots (wrapping) and records %globaltimer values, combined with
+ * atomicMax so a zeroed buffer is the reset state:
+ *   [0] bitwise NOT of the first block's entry time
+ *   [1] bitwise NOT of the time that block passed its dependency wait
+ *   [2] latest time a block had its weights in shared memory (0: n/a)
+ *   [3] latest block exit time (the router: its last block's exit).
+ * A call launches 3 (T == 1) or 4 kernels; slot groups are reserved as
+ * router 1, gate/up 1, down (+ combine) 2, sort 1.  Buffer owned by the
+ * caller; NULL turns tracing off.  Tracing adds a few atomics per block. */
+int moe_set_trace(moe_handle *h, unsigned long long *buffer, int n_launches);
+
 /* Self-test of the device-side bounded waits (failure detection without a
  * GPU fault): launches one thread that waits on a barrier nothing ever
  * completes; after limit_ns (1 .. 2e9 ns) of device time it gives up and
