@@ -16,6 +16,9 @@ struct moe_handle {
   unsigned long long *trace;  // caller's trace buffer (nullable)
   int trace_groups;           // 4-slot groups in it
   int trace_next;             // next group handed to a launch
+  int n_sm;                   // multiprocessors: grid of the fused decode kernel
+  bool fused;                 // single-token calls use the fused layer kernel
+  int fused_key[3], fused_ok; // cached shape check (hidden, inter, top_k) -> usable
 };
 
 namespace {
@@ -32,6 +35,10 @@ unsigned long long *take_trace(moe_handle *h, int n) {
 namespace {
 
 constexpr size_t kSmemCap = 227 * 1024;
+// handle-owned device words: [0] error bits, [1] router ticket; from
+// kSyncOffset the fused kernel's grid barrier (epoch, release, per-block flags)
+constexpr size_t kSyncOffset = 256;
+constexpr size_t kDeviceWords = kSyncOffset + 64 + 1024;
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -171,6 +178,40 @@ int run_router(moe_handle *h, const moe_layer_weights *w, int T, const void *x, 
   return cuda_status(moe::launch_router(a, st, h->pdl));
 }
 
+// The fused single-token kernel needs one resident block per SM (grid
+// barriers) and one router row per block.
+bool use_fused(moe_handle *h, const moe_layer_weights *w, int T) {
+  if (!h->fused || T != 1 || w->dims.n_experts > h->n_sm || h->n_sm > 1024) return false;
+  const int key[3] = {w->dims.hidden, w->dims.inter, w->dims.top_k};
+  if (key[0] != h->fused_key[0] || key[1] != h->fused_key[1] || key[2] != h->fused_key[2]) {
+    const moe::Dims d = to_dims(w->dims, 1);
+    h->fused_ok = moe::fused_decode_smem(d) <= kSmemCap && moe::decode_blocks_per_sm(d) >= 1;
+    memcpy(h->fused_key, key, sizeof(key));
+  }
+  return h->fused_ok != 0;
+}
+
+int run_fused(moe_handle *h, const moe_layer_weights *w, const void *x, void *hres, void *y, void *x_out,
+              float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(w->dims, 1);
+  moe::DecodeArgs a;
+  a.w = layer_ptrs(*w);
+  a.d = to_dims(w->dims, 1);
+  a.x = (const uint16_t *)x;
+  a.hres = (uint16_t *)hres;
+  a.xn_user = (uint16_t *)x_out;
+  a.logits = logits ? logits : (float *)(ws + L.logits);
+  a.ids_user = ids;
+  a.wts_user = wts;
+  a.hbuf = (__half *)(ws + L.h);
+  a.y = (uint16_t *)y;
+  a.sync = h->dwords + kSyncOffset;
+  a.err = h->dwords;
+  a.trace = take_trace(h, 1);
+  a.normalize = hres != nullptr;
+  return cuda_status(moe::launch_decode_fused(a, h->n_sm, st, h->pdl));
+}
+
 int run_ffn(moe_handle *h, const moe_layer_weights *w, int T, const void *x, const moe::Routing &r, int include_shared,
             void *y, void *hres, uint8_t *ws, cudaStream_t st) {
   const WsLayout L = ws_layout(w->dims, T);
@@ -220,15 +261,20 @@ int moe_create(moe_handle **out) {
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
-  if (moe::router_set_attributes() != cudaSuccess || moe::ffn_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::router_set_attributes() != cudaSuccess || moe::ffn_set_attributes() != cudaSuccess ||
+      moe::decode_set_attributes() != cudaSuccess)
+    return MOE_ERR_CUDA;
   moe_handle *h = (moe_handle *)calloc(1, sizeof(moe_handle));
   if (!h) return MOE_ERR_CUDA;
   h->device = dev;
-  if (cudaMalloc(&h->dwords, 64 * sizeof(unsigned)) != cudaSuccess) {
+  h->n_sm = prop.multiProcessorCount;
+  const char *fz = getenv("MOE_DECODE_FUSED");
+  h->fused = !(fz && fz[0] == '0');
+  if (cudaMalloc(&h->dwords, kDeviceWords * sizeof(unsigned)) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
   }
-  if (cudaMemset(h->dwords, 0, 64 * sizeof(unsigned)) != cudaSuccess) {
+  if (cudaMemset(h->dwords, 0, kDeviceWords * sizeof(unsigned)) != cudaSuccess) {
     cudaFree(h->dwords);
     free(h);
     return MOE_ERR_CUDA;
@@ -326,6 +372,8 @@ int moe_layer_forward(moe_handle *h, const void *x, int n_tokens, const moe_laye
   if (!aligned(x, 16) || !aligned(y, 16) || (logits_out && !aligned(logits_out, 16))) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
   uint8_t *wsb = (uint8_t *)ws;
+  if (use_fused(h, w, n_tokens))
+    return run_fused(h, w, x, nullptr, y, nullptr, logits_out, ids_out, weights_out, wsb, (cudaStream_t)stream);
   if ((st = run_router(h, w, n_tokens, x, nullptr, nullptr, logits_out, ids_out, weights_out, wsb,
                        (cudaStream_t)stream)))
     return st;
@@ -346,6 +394,8 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens, const 
   if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
   uint8_t *wsb = (uint8_t *)ws;
   const WsLayout L = ws_layout(w->dims, n_tokens);
+  if (use_fused(h, w, n_tokens))
+    return run_fused(h, w, nullptr, hidden, y_out, x_out, logits_out, ids_out, nullptr, wsb, (cudaStream_t)stream);
   if ((st = run_router(h, w, n_tokens, nullptr, hidden, x_out, logits_out, ids_out, nullptr, wsb,
                        (cudaStream_t)stream)))
     return st;

@@ -125,15 +125,7 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// D(16x8, f32) += A(16x16) * B(16x8), bf16 operands.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// Same with f16 operands.
+// D(16x8, f32) += A(16x16) * B(16x8), f16 operands.
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -143,24 +135,34 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
 }
 
 // ------------------------------------------------------------------ codes
-// Two 4-bit codes of word w -> bf16x2 {128 + q_i, 128 + q_{i+4}}, exact.
-// 0x4300 is bf16 128.0, whose unit in the last place is 1, so OR-ing a
-// code 0..15 into the low mantissa bits yields 128 + code.
+// Two 4-bit codes of word w as fp16 subnormals, one AND each: pair i holds
+// codes (i, i+4).  Even i: (q_i, q_{i+4}) * 2^-24.  Odd i: the mask keeps the
+// nibbles in place, i.e. 16 * (q_i, q_{i+4}) * 2^-24; the matching
+// activations are stored divided by 16, so every product is q * x * 2^-24
+// exactly (fp16 subnormal inputs are exact in the tensor cores).  The group
+// correction multiplies the accumulator by scale * 2^24.
 template <int i>
-__device__ __forceinline__ uint32_t codes_bf16_plus128(uint32_t w) {
-  return ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+__device__ __forceinline__ uint32_t codes_sub(uint32_t w) {
+  if (i == 0) return w & 0x000F000Fu;
+  if (i == 1) return w & 0x00F000F0u;
+  if (i == 2) return (w >> 8) & 0x000F000Fu;
+  return (w >> 8) & 0x00F000F0u;
 }
-// Two 4-bit codes -> f16x2 {q_i, q_{i+4}}, exact: 0x6400 is f16 1024.0 with
-// unit last place 1; subtracting 1024 leaves the code.
-template <int i>
-__device__ __forceinline__ uint32_t codes_f16(uint32_t w) {
-  const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64006400u));
-  return r;
-}
+constexpr float kCodeScale = 16777216.0f;  // 2^24
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// bf16 pair -> fp16 pair (exact in fp16's normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+// fp16 pair * 1/16 (exact unless the result is subnormal).
+__device__ __forceinline__ uint32_t f16x2_div16(uint32_t w) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0x2C002C00u));
+  return r;
+}
 
 // float -> bf16 bits, round to nearest even (finite inputs).
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
@@ -169,7 +171,7 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 
 // Operand order inside one 64-wide group.  The tensor-core fragments take
 // the 4-bit codes of a thread's two packed words in the order produced by
-// codes_*<i>: pair i of word w holds codes (i, i+4).  The activation vector
+// codes_sub<i>: pair i of word w holds codes (i, i+4).  The activation vector
 // is stored in shared memory permuted so that each B fragment (4 values) is
 // one 8-byte load.  Slot j = 16c + 4s + m of a group holds element
 // 16c + 8(s>>1) + 2(s&1) + {0,4,1,5}[m].
@@ -186,6 +188,19 @@ __device__ __forceinline__ void permute_quarter(const uint32_t (&in)[8], uint32_
       out[4 * h + 2 * e + 1] = __byte_perm(a, b, 0x7632);  // (8h+2e+1, 8h+2e+5)
     }
   }
+}
+
+// The B-operand form of one 16-element quarter: permuted, converted to fp16
+// (kBf16: the input is bf16), odd words (the slots facing the x16 codes)
+// divided by 16.
+template <bool kBf16>
+__device__ __forceinline__ void operand_quarter(const uint32_t (&in)[8], uint32_t (&out)[8]) {
+  uint32_t h[8];
+#pragma unroll
+  for (int w = 0; w < 8; ++w) h[w] = kBf16 ? bf16x2_to_f16x2(in[w]) : in[w];
+  permute_quarter(h, out);
+#pragma unroll
+  for (int w = 1; w < 8; w += 2) out[w] = f16x2_div16(out[w]);
 }
 
 __device__ __forceinline__ unsigned lanemask_lt() {

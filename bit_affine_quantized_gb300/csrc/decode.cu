@@ -1,0 +1,637 @@
+// Fused single-token MoE layer (decode, T == 1), sm_103a.
+//
+// Page "TurboFieldfare - System design", section "Decode": per layer the
+// router picks 8 of 128 experts, the shared expert runs alongside, the routed
+// outputs are reduced with the router weights and added to the shared one
+// (section "Metal execution" fuses decode, GeGLU and the weighted reduction).
+// There, the expert ids travel GPU -> CPU -> SSD reads -> GPU; here every
+// expert is in HBM and the whole layer is one launch.
+//
+// One persistent block per SM (the grid is the SM count; shared memory use
+// keeps it at one block per SM).  Phases:
+//   0. before the dependency wait: this block's router row goes to
+//      registers, and the producer warp starts the bulk copies of the
+//      shared expert's gate/up tiles (they need no routing);
+//   1. x = input (or rmsnorm of the residual), one logit per block row;
+//   2. grid barrier; every block computes the top-k itself (no second
+//      barrier), then the producer streams the routed gate/up tiles and the
+//      down tiles through a 3-slot ring of shared memory;
+//   3. gate/up + GeGLU per 16-row unit (mma.m16n8k16, exact integer
+//      operands, per-group affine correction), h to global fp16;
+//   4. grid barrier; down for 16 output rows over all k+1 experts, weighted
+//      sum, bf16 out, optional residual add.
+// All waits are bounded (2 s): a timeout records MOE_ERR_TIMEOUT, the block
+// drains its copies in flight and exits.
+#include <math.h>
+
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int kCons = 16;                    // consumer warps
+constexpr int kConsThreads = kCons * 32;     // 256
+constexpr int kThreadsF = kConsThreads + 32; // + producer warp
+constexpr int kSlots = 3;                    // ring slots
+constexpr int kRowsU = 16;                   // rows per unit
+
+__host__ __device__ inline int pw8(int w) { return w + ((8 - (w % 16)) + 16) % 16; }
+__host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
+
+struct FusedLayout {
+  int nrt;          // gate/up units per expert (I / 16)
+  int n_gu, n_dn;   // gate/up units, down units
+  int gu_qp;        // gate/up code row pitch (bytes)
+  int gu_bytes, dn_qp, dn_slot_bytes, dn_bytes, slot_bytes;
+  int ring, xnat, xperm, xsum, qsum, hperm, hsum, red, misc, total;
+};
+
+__host__ __device__ inline FusedLayout fused_layout(int H, int I, int k) {
+  FusedLayout L;
+  const int G = H / kGroup, GI = I / kGroup, S = k + 1;
+  L.nrt = I / kRowsU;
+  L.n_gu = S * L.nrt;
+  L.n_dn = H / kRowsU;
+  L.gu_qp = pw8(H / 8) * 4;
+  L.gu_bytes = 2 * kRowsU * L.gu_qp + 4 * kRowsU * G * 2;
+  L.dn_qp = pw8(I / 8) * 4;
+  L.dn_slot_bytes = kRowsU * L.dn_qp + 2 * kRowsU * GI * 2;
+  L.dn_bytes = S * L.dn_slot_bytes;
+  L.slot_bytes = al16(L.gu_bytes > L.dn_bytes ? L.gu_bytes : L.dn_bytes);
+  int o = 0;
+  L.ring = o;
+  o += kSlots * L.slot_bytes;
+  L.xnat = o;
+  o = al16(o + H * 2);
+  L.xperm = o;
+  o = al16(o + H * 2);
+  L.xsum = o;
+  o = al16(o + G * 4);
+  L.qsum = o;
+  o = al16(o + (H / 16) * 4);
+  L.hperm = o;
+  o = al16(o + S * I * 2);
+  L.hsum = o;
+  o = al16(o + S * GI * 4);
+  L.red = o;
+  o = al16(o + kCons * 32 * 8 * 4);
+  L.misc = o;  // 8 partial logits, k ids, k weights, 2k+1 mbarriers, flags
+  o = al16(o + 256);
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsThreads) : "memory"); }
+
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid barrier on one 64-bit arrival counter, run by the consumer threads of
+// every block: each block adds 1 with a release reduction (no return value,
+// so arrivals pipeline at L2 instead of serialising) and polls until the
+// counter reaches `target`.  The counter only grows; a launch's targets are
+// derived from its value at launch start (see the caller).  Bounded.
+__device__ bool grid_sync(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag) {
+  cons_sync();  // the block's writes happen-before thread 0's release below
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
+    bool ok = true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+      if (ld_acquire64(count) >= target) break;
+      if ((it & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+    }
+    if (!ok) set_error(err, kErrTimeout);
+    *s_flag = ok ? 1 : 0;
+  }
+  cons_sync();
+  return *s_flag != 0;
+}
+
+// Orderable 32-bit key of a float (larger float -> larger key).
+__device__ __forceinline__ unsigned ord_key(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ float gelu_tanh_f(float z) {
+  const float c0 = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * z * (1.0f + tanhf(c0 * fmaf(0.044715f * z, z * z, z)));
+}
+
+// One 64-wide group of a gate/up unit: rows r, r+8 of gate and up, token
+// column 0 (valid in the lanes with cq == 0).  Accumulates the affine-
+// corrected partials s*acc + (b - 128 s)*sum(x).
+__device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xperm, const float *xsum, int g, int r,
+                                         int cq, int G, int qp, float &tg0, float &tg2, float &tu0, float &tu2) {
+  const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 2 * 16 * qp);  // gs, gb, us, ub [16][G]
+  const uint2 g0 = *reinterpret_cast<const uint2 *>(tile + r * qp + g * 32 + cq * 8);
+  const uint2 g1 = *reinterpret_cast<const uint2 *>(tile + (r + 8) * qp + g * 32 + cq * 8);
+  const uint2 u0 = *reinterpret_cast<const uint2 *>(tile + (16 + r) * qp + g * 32 + cq * 8);
+  const uint2 u1 = *reinterpret_cast<const uint2 *>(tile + (16 + r + 8) * qp + g * 32 + cq * 8);
+  float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const uint2 bx = r == 0 ? *reinterpret_cast<const uint2 *>(xperm + g * 128 + cq * 32 + s * 8) : make_uint2(0u, 0u);
+    const uint32_t wg0 = (s >> 1) ? g0.y : g0.x, wg1 = (s >> 1) ? g1.y : g1.x;
+    const uint32_t wu0 = (s >> 1) ? u0.y : u0.x, wu1 = (s >> 1) ? u1.y : u1.x;
+    uint32_t A[4], B[4];
+    if ((s & 1) == 0) {
+      A[0] = codes_sub<0>(wg0); A[1] = codes_sub<0>(wg1); A[2] = codes_sub<1>(wg0); A[3] = codes_sub<1>(wg1);
+      B[0] = codes_sub<0>(wu0); B[1] = codes_sub<0>(wu1); B[2] = codes_sub<1>(wu0); B[3] = codes_sub<1>(wu1);
+    } else {
+      A[0] = codes_sub<2>(wg0); A[1] = codes_sub<2>(wg1); A[2] = codes_sub<3>(wg0); A[3] = codes_sub<3>(wg1);
+      B[0] = codes_sub<2>(wu0); B[1] = codes_sub<2>(wu1); B[2] = codes_sub<3>(wu0); B[3] = codes_sub<3>(wu1);
+    }
+    mma_f16(ag, A, bx.x, bx.y);
+    mma_f16(au, B, bx.x, bx.y);
+  }
+  const float xs = xsum[g];
+  const float sg0 = bf16_bits_to_float(raw[r * G + g]), bg0 = bf16_bits_to_float(raw[16 * G + r * G + g]);
+  const float sg1 = bf16_bits_to_float(raw[(r + 8) * G + g]), bg1 = bf16_bits_to_float(raw[16 * G + (r + 8) * G + g]);
+  const float su0 = bf16_bits_to_float(raw[32 * G + r * G + g]), bu0 = bf16_bits_to_float(raw[48 * G + r * G + g]);
+  const float su1 = bf16_bits_to_float(raw[32 * G + (r + 8) * G + g]), bu1 = bf16_bits_to_float(raw[48 * G + (r + 8) * G + g]);
+  tg0 = fmaf(bg0, xs, fmaf(sg0 * kCodeScale, ag[0], tg0));
+  tg2 = fmaf(bg1, xs, fmaf(sg1 * kCodeScale, ag[2], tg2));
+  tu0 = fmaf(bu0, xs, fmaf(su0 * kCodeScale, au[0], tu0));
+  tu2 = fmaf(bu1, xs, fmaf(su1 * kCodeScale, au[2], tu2));
+}
+
+// One (expert slot, 64-wide group) item of a down unit: rows r, r+8 of the
+// 16-row tile, token column 0.  Returns the weighted partials.
+__device__ __forceinline__ void down_item(const uint8_t *tile, const uint8_t *hperm, const float *hsum,
+                                          const float *s_w, int s, int g, int r, int cq, int I, int GI, int dn_qp,
+                                          int dn_slot_bytes, float &t0, float &t2) {
+  const uint8_t *qb = tile + s * dn_slot_bytes + g * 32 + cq * 8;
+  const uint16_t *sb = reinterpret_cast<const uint16_t *>(tile + s * dn_slot_bytes + 16 * dn_qp);
+  const uint2 w0 = *reinterpret_cast<const uint2 *>(qb + r * dn_qp);
+  const uint2 w1 = *reinterpret_cast<const uint2 *>(qb + (r + 8) * dn_qp);
+  const uint8_t *hrow = hperm + (s * I + g * kGroup) * 2 + cq * 32;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const uint2 bx = r == 0 ? *reinterpret_cast<const uint2 *>(hrow + st * 8) : make_uint2(0u, 0u);
+    const uint32_t x0 = (st >> 1) ? w0.y : w0.x, x1 = (st >> 1) ? w1.y : w1.x;
+    uint32_t A[4];
+    if ((st & 1) == 0) {
+      A[0] = codes_sub<0>(x0); A[1] = codes_sub<0>(x1); A[2] = codes_sub<1>(x0); A[3] = codes_sub<1>(x1);
+    } else {
+      A[0] = codes_sub<2>(x0); A[1] = codes_sub<2>(x1); A[2] = codes_sub<3>(x0); A[3] = codes_sub<3>(x1);
+    }
+    mma_f16(acc, A, bx.x, bx.y);
+  }
+  const float wt = s == 0 ? 1.0f : s_w[s - 1];
+  const float hs = hsum[s * GI + g];
+  const float s0 = bf16_bits_to_float(sb[r * GI + g]) * kCodeScale, b0 = bf16_bits_to_float(sb[16 * GI + r * GI + g]);
+  const float s1 = bf16_bits_to_float(sb[(r + 8) * GI + g]) * kCodeScale, b1 = bf16_bits_to_float(sb[16 * GI + (r + 8) * GI + g]);
+  t0 = fmaf(wt, fmaf(s0, acc[0], b0 * hs), t0);
+  t2 = fmaf(wt, fmaf(s1, acc[2], b1 * hs), t2);
+}
+}  // namespace
+
+size_t fused_decode_smem(const Dims &d) { return (size_t)fused_layout(d.H, d.I, d.k).total; }
+
+__global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int H = a.d.H, I = a.d.I, E = a.d.E, k = a.d.k;
+  const int G = H / kGroup, GI = I / kGroup, S = k + 1;
+  const FusedLayout L = fused_layout(H, I, k);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nb = gridDim.x, c = blockIdx.x;
+  uint8_t *ring = smem + L.ring;
+  uint16_t *xnat = reinterpret_cast<uint16_t *>(smem + L.xnat);
+  uint8_t *xperm = smem + L.xperm;
+  float *xsum = reinterpret_cast<float *>(smem + L.xsum);
+  float *qsum = reinterpret_cast<float *>(smem + L.qsum);
+  uint8_t *hperm = smem + L.hperm;
+  float *hsum = reinterpret_cast<float *>(smem + L.hsum);
+  float *sred = reinterpret_cast<float *>(smem + L.red);
+  float *s_part = reinterpret_cast<float *>(smem + L.misc);        // [8]
+  int *s_sel = reinterpret_cast<int *>(smem + L.misc + 32);        // [8]
+  float *s_w = reinterpret_cast<float *>(smem + L.misc + 64);      // [8]
+  int *s_flag = reinterpret_cast<int *>(smem + L.misc + 96);       // [4]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.misc + 128);  // [3]
+  uint64_t *empty = full + kSlots;                                     // [3]
+  uint64_t *route = empty + kSlots;                                    // [1]
+
+  // this block's unit lists: gate/up u = c + nb*i; down d = (nb-1-c) + nb*i
+  const int n_gu_mine = c < L.n_gu ? (L.n_gu - 1 - c) / nb + 1 : 0;
+  const int c_dn = nb - 1 - c;
+  const int n_dn_mine = c_dn < L.n_dn ? (L.n_dn - 1 - c_dn) / nb + 1 : 0;
+  const int n_units = n_gu_mine + n_dn_mine;
+
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(route, 1);
+    fence_mbar_init();
+    s_flag[2] = 0;  // abort: set by the consumers before releasing `route` on a failure
+  }
+  __syncthreads();
+  if (c == 0 && tid == 0) trace_min(a.trace, kTrEntry);
+
+  // ============================================================ producer warp
+  if (warp == kCons) {
+    bool routed = false, ok = true;
+    int issued = 0;
+    for (int it = 0; it < n_units && ok; ++it) {
+      const int slot = it % kSlots;
+      if (it >= kSlots) ok = mbar_wait(&empty[slot], ((it / kSlots) - 1) & 1);
+      if (!ok) break;
+      uint8_t *dst = ring + slot * L.slot_bytes;
+      const bool is_gu = it < n_gu_mine;
+      const int u = is_gu ? c + nb * it : c_dn + nb * (it - n_gu_mine);
+      const int gslot = is_gu ? u / L.nrt : 0;
+      if ((!is_gu || gslot > 0) && !routed) {
+        ok = mbar_wait(route, 0) && *reinterpret_cast<volatile int *>(&s_flag[2]) == 0;
+        routed = true;
+        if (!ok) break;
+      }
+      if (is_gu) {
+        const int rt = u % L.nrt, r0 = rt * kRowsU;
+        const uint8_t *blob = gslot == 0 ? a.w.shared : a.w.experts + (size_t)s_sel[gslot - 1] * a.w.stride;
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRowsU * (H / 2) + 4 * kRowsU * G * 2));
+        __syncwarp();
+        const int m = lane >> 4, row = lane & 15;
+        bulk_g2s(dst + (m * kRowsU + row) * L.gu_qp,
+                 blob + (m == 0 ? a.w.off.gate_q : a.w.off.up_q) + (size_t)(r0 + row) * (H / 2), (uint32_t)(H / 2),
+                 &full[slot]);
+        if (lane < 4) {
+          const size_t off = lane == 0 ? a.w.off.gate_s : lane == 1 ? a.w.off.gate_b : lane == 2 ? a.w.off.up_s : a.w.off.up_b;
+          bulk_g2s(dst + 2 * kRowsU * L.gu_qp + lane * kRowsU * G * 2, blob + off + (size_t)r0 * G * 2,
+                   (uint32_t)(kRowsU * G * 2), &full[slot]);
+        }
+      } else {
+        const int n0 = u * kRowsU;
+        const bool one = L.dn_qp == I / 2;
+        const int nq = one ? 1 : kRowsU;
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(S * (kRowsU * (I / 2) + 2 * kRowsU * GI * 2)));
+        __syncwarp();
+        for (int ci = lane; ci < S * (nq + 2); ci += 32) {
+          const int s = ci / (nq + 2), j = ci - s * (nq + 2);
+          const uint8_t *blob = s == 0 ? a.w.shared : a.w.experts + (size_t)s_sel[s - 1] * a.w.stride;
+          uint8_t *sd = dst + s * L.dn_slot_bytes;
+          if (j < nq) {
+            const int row = one ? 0 : j;
+            bulk_g2s(sd + row * L.dn_qp, blob + a.w.off.down_q + (size_t)(n0 + row) * (I / 2),
+                     one ? (uint32_t)(kRowsU * (I / 2)) : (uint32_t)(I / 2), &full[slot]);
+          } else {
+            const int f = j - nq;
+            bulk_g2s(sd + kRowsU * L.dn_qp + f * kRowsU * GI * 2,
+                     blob + (f == 0 ? a.w.off.down_s : a.w.off.down_b) + (size_t)n0 * GI * 2,
+                     (uint32_t)(kRowsU * GI * 2), &full[slot]);
+          }
+        }
+      }
+      issued = it + 1;
+    }
+    // Copies still in flight must land before this block's shared memory is
+    // released: wait (bounded) for every issued unit's full barrier phase.
+    if (lane == 0) {
+      if (!ok) set_error(a.err, kErrTimeout);
+      for (int it = issued - kSlots > 0 ? issued - kSlots : 0; it < issued; ++it)
+        mbar_wait(&full[it % kSlots], (it / kSlots) & 1);
+    }
+    return;
+  }
+
+  // ============================================================ consumers
+  // router row of this block (expert e = c; E <= gridDim.x is checked on the host)
+  const int nwords = H / 4;
+  const int wpw = (nwords + kCons - 1) / kCons;  // words per warp
+  uint32_t rq[4], rsb[4];
+  const bool has_row = c < E;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int wi = warp * wpw + lane + 32 * j;
+    if (has_row && lane + 32 * j < wpw && wi < nwords) {
+      rq[j] = __ldg(reinterpret_cast<const uint32_t *>(a.w.router_q + (size_t)c * H) + wi);
+      rsb[j] = (uint32_t)__ldg(a.w.router_s + (size_t)c * G + (wi >> 4)) |
+               ((uint32_t)__ldg(a.w.router_b + (size_t)c * G + (wi >> 4)) << 16);
+    }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (c == 0 && tid == 0) trace_min(a.trace, kTrWaited);
+  // Barrier targets of this launch.  Every launch adds exactly 2*nb to the
+  // counter (two barriers); read after the dependency wait it is
+  // 2*nb*epoch + (arrivals of fast blocks at barrier 1, fewer than nb), so
+  // the epoch follows by division.
+  unsigned long long *bar_count = reinterpret_cast<unsigned long long *>(a.sync);
+  const unsigned long long base = (ld_acquire64(bar_count) / (2ull * nb)) * (2ull * nb);
+
+  // Residual values of this block's down rows, needed only at the very end:
+  // load them now.  Only this block writes these rows, after it read them.
+  uint32_t hres_pre0 = 0, hres_pre1 = 0;
+  if (a.hres && tid < kRowsU) {
+    if (n_dn_mine > 0) hres_pre0 = a.hres[c_dn * kRowsU + tid];
+    if (n_dn_mine > 1) hres_pre1 = a.hres[(c_dn + nb) * kRowsU + tid];
+  }
+
+  // ---- phase 1: x (one 16-element quarter per thread) and the logit
+  const int nquart = H / 16;
+  uint32_t qin[8];
+  float qss = 0.f;
+  const uint16_t *src = a.normalize ? a.hres : a.x;
+  if (tid < nquart) {
+    const uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(src) + 2 * tid);
+    const uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(src) + 2 * tid + 1);
+    qin[0] = v0.x; qin[1] = v0.y; qin[2] = v0.z; qin[3] = v0.w;
+    qin[4] = v1.x; qin[5] = v1.y; qin[6] = v1.z; qin[7] = v1.w;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float lo = __uint_as_float(qin[i] << 16), hi = __uint_as_float(qin[i] & 0xFFFF0000u);
+      qss = fmaf(lo, lo, qss);
+      qss = fmaf(hi, hi, qss);
+    }
+  }
+  if (a.normalize) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) qss += __shfl_xor_sync(0xffffffffu, qss, off);
+    if (lane == 0) s_part[warp] = qss;
+    cons_sync();
+    float tot = 0.f;
+    for (int w = 0; w < kCons; ++w) tot += s_part[w];
+    const float inv = 1.0f / sqrtf(tot / (float)H + 1e-6f);
+    if (tid < nquart) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint16_t lb = float_to_bf16_bits(__uint_as_float(qin[i] << 16) * inv);
+        const uint16_t hb = float_to_bf16_bits(__uint_as_float(qin[i] & 0xFFFF0000u) * inv);
+        qin[i] = (uint32_t)lb | ((uint32_t)hb << 16);
+      }
+    }
+    cons_sync();  // s_part is reused below
+  }
+  if (tid < nquart) {
+    uint4 *xn4 = reinterpret_cast<uint4 *>(xnat) + 2 * tid;
+    xn4[0] = make_uint4(qin[0], qin[1], qin[2], qin[3]);
+    xn4[1] = make_uint4(qin[4], qin[5], qin[6], qin[7]);
+    if (c == 0 && a.xn_user) {
+      uint4 *xu = reinterpret_cast<uint4 *>(a.xn_user) + 2 * tid;
+      xu[0] = xn4[0];
+      xu[1] = xn4[1];
+    }
+    uint32_t out[8];
+    operand_quarter<true>(qin, out);  // bf16 x -> fp16 B operand
+    uint2 *dst = reinterpret_cast<uint2 *>(xperm + tid * 32);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) dst[w] = make_uint2(out[2 * w], out[2 * w + 1]);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s += __uint_as_float(qin[i] << 16);
+      s += __uint_as_float(qin[i] & 0xFFFF0000u);
+    }
+    qsum[tid] = s;
+  }
+  cons_sync();
+  if (tid < G) xsum[tid] = ((qsum[4 * tid] + qsum[4 * tid + 1]) + qsum[4 * tid + 2]) + qsum[4 * tid + 3];
+  float lg = 0.f;
+  if (has_row) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int wi = warp * wpw + lane + 32 * j;
+      if (lane + 32 * j < wpw && wi < nwords) {
+        const float s = bf16_bits_to_float(rsb[j] & 0xFFFFu), b = bf16_bits_to_float(rsb[j] >> 16);
+        const uint2 xv = *reinterpret_cast<const uint2 *>(xnat + 4 * wi);
+        const float xs[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
+                             __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float q = __uint_as_float(0x4B000000u | ((rq[j] >> (8 * i)) & 0xFFu)) - 8388608.0f;
+          lg = fmaf(fmaf(q, s, b), xs[i], lg);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, off);
+  if (lane == 0) s_part[warp] = lg;
+  cons_sync();
+  if (tid == 0 && has_row) {
+    float t = 0.f;
+    for (int w = 0; w < kCons; ++w) t += s_part[w];
+    a.logits[c] = t + (a.w.logit_bias ? a.w.logit_bias[c] : 0.f);
+  }
+
+  // ---- phase 2: grid barrier, then every block selects the top-k itself
+  if (!grid_sync(bar_count, base + nb, a.err, &s_flag[0])) {
+    if (tid == 0) {
+      s_flag[2] = 1;                     // no routing: the producer must not stream routed tiles
+      mbar_arrive_expect_tx(route, 0);   // release it; it drains its copies and exits
+      // still count this block's second arrival: every launch moves the
+      // counter by exactly 2*nb
+      asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar_count) : "memory");
+    }
+    return;
+  }
+  if (warp == 0) {
+    // Top-k with two warp reductions per pick: the largest key, then the
+    // lowest expert id holding it (ties to the lower id).  Keys are the
+    // order-preserving bit patterns of the fp32 logits; non-finite -> -inf.
+    unsigned key[4];
+    bool nonfinite = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = 0u;  // below every real key: never picked while k <= E
+      if (e < E) {
+        float x = __ldcg(a.logits + e);
+        if (!isfinite(x)) {
+          x = -INFINITY;
+          nonfinite = true;
+        }
+        key[i] = ord_key(x);
+      }
+    }
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0 && c == 0) set_error(a.err, kErrNonFinite);
+    float selv[kMaxTopK];
+    int seli[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        // lane-local best: highest key, lowest index on ties
+        unsigned bk = key[0];
+        int bi = lane;
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+          if (key[i] > bk) {
+            bk = key[i];
+            bi = lane + 32 * i;
+          }
+        const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
+        const unsigned idmin = __reduce_min_sync(0xffffffffu, bk == kmax ? (unsigned)bi : 0xffffffffu);
+        selv[j] = key_value(kmax);
+        seli[j] = (int)idmin;
+        if ((int)(idmin & 31u) == lane) key[idmin >> 5] = 0u;  // taken
+      }
+    }
+    float ex[kMaxTopK], den = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k) {
+        ex[j] = expf(selv[j] - selv[0]);
+        den += ex[j];
+      }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < k && lane == j) {
+        const float wj = ex[j] / den;
+        s_sel[j] = seli[j];
+        s_w[j] = wj;
+        if (c == 0) {
+          if (a.ids_user) a.ids_user[j] = seli[j];
+          if (a.wts_user) a.wts_user[j] = wj;
+        }
+      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(route, 0);  // routing known: producer may stream
+  }
+  cons_sync();
+  if (c == 0 && tid == 0) trace_max(a.trace, kTrLoaded);
+
+  // ---- phase 3: gate/up units
+  const int r = lane >> 2, cq = lane & 3;
+  int it = 0;
+  bool ok = true;
+  for (; it < n_gu_mine; ++it) {
+    const int slot = it % kSlots;
+    const int u = c + nb * it;
+    const int gslot = u / L.nrt, rt = u % L.nrt;
+    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) { ok = false; break; }
+    const uint8_t *tile = ring + slot * L.slot_bytes;
+    // groups warp, warp + kCons, ...; two groups in flight per iteration
+    float tg0a = 0.f, tg2a = 0.f, tu0a = 0.f, tu2a = 0.f, tg0b = 0.f, tg2b = 0.f, tu0b = 0.f, tu2b = 0.f;
+    int g = warp;
+    for (; g + kCons < G; g += 2 * kCons) {
+      gu_group(tile, xperm, xsum, g, r, cq, G, L.gu_qp, tg0a, tg2a, tu0a, tu2a);
+      gu_group(tile, xperm, xsum, g + kCons, r, cq, G, L.gu_qp, tg0b, tg2b, tu0b, tu2b);
+    }
+    if (g < G) gu_group(tile, xperm, xsum, g, r, cq, G, L.gu_qp, tg0a, tg2a, tu0a, tu2a);
+    if (cq == 0) {
+      float *red = sred + warp * 64;
+      red[r] = tg0a + tg0b;
+      red[r + 8] = tg2a + tg2b;
+      red[16 + r] = tu0a + tu0b;
+      red[16 + r + 8] = tu2a + tu2b;
+    }
+    cons_sync();
+    if (tid < kRowsU) {
+      float gs = 0.f, us = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCons; ++w) {
+        gs += sred[w * 64 + tid];
+        us += sred[w * 64 + 16 + tid];
+      }
+      const float hv = gelu_tanh_f(gs) * us;
+      if (!(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
+      a.hbuf[(size_t)gslot * I + rt * kRowsU + tid] = __float2half_rn(hv);
+    }
+    cons_sync();
+    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);  // slot free
+  }
+  if (!ok) set_error(a.err, kErrTimeout);
+
+  // ---- phase 4: grid barrier (all of h written), then the down units
+  if (!grid_sync(bar_count, base + 2ull * nb, a.err, &s_flag[1]) || !ok) return;
+  // stage every expert's h row (permuted fp16) one 16-wide quarter per
+  // thread (all loads in one round), then the group sums in quarter order
+  {
+    const int nq = S * (I / 16);
+    float *hq = sred;  // quarter sums (sred is free until the first down unit)
+    for (int q = tid; q < nq; q += kConsThreads) {
+      const uint4 *srch = reinterpret_cast<const uint4 *>(a.hbuf) + 2 * q;
+      const uint4 v0 = __ldcg(srch), v1 = __ldcg(srch + 1);
+      const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t out[8];
+      operand_quarter<false>(in, out);  // fp16 h -> B operand
+      uint2 *dst = reinterpret_cast<uint2 *>(hperm + q * 32);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) dst[w] = make_uint2(out[2 * w], out[2 * w + 1]);
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        sum += __half2float(__ushort_as_half((unsigned short)(in[w] & 0xFFFFu)));
+        sum += __half2float(__ushort_as_half((unsigned short)(in[w] >> 16)));
+      }
+      hq[q] = sum;
+    }
+    cons_sync();
+    for (int q = tid; q < S * GI; q += kConsThreads)
+      hsum[q] = ((hq[4 * q] + hq[4 * q + 1]) + hq[4 * q + 2]) + hq[4 * q + 3];
+  }
+  cons_sync();
+  for (int jd = 0; jd < n_dn_mine; ++jd, ++it) {
+    const int slot = it % kSlots;
+    const int n0 = (c_dn + nb * jd) * kRowsU;
+    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) {
+      set_error(a.err, kErrTimeout);
+      return;
+    }
+    const uint8_t *tile = ring + slot * L.slot_bytes;
+    const int nitems = S * GI;
+    const int per = (nitems + kCons - 1) / kCons;
+    const int ib = warp * per, ie = min(nitems, ib + per);
+    // two independent accumulation chains per warp (items q and q+1)
+    float t0a = 0.f, t2a = 0.f, t0b = 0.f, t2b = 0.f;
+    int q = ib;
+    for (; q + 1 < ie; q += 2) {
+      const int sa = q / GI, ga = q - sa * GI, sb2 = (q + 1) / GI, gb = (q + 1) - sb2 * GI;
+      down_item(tile, hperm, hsum, s_w, sa, ga, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0a, t2a);
+      down_item(tile, hperm, hsum, s_w, sb2, gb, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0b, t2b);
+    }
+    if (q < ie) {
+      const int sa = q / GI, ga = q - sa * GI;
+      down_item(tile, hperm, hsum, s_w, sa, ga, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0a, t2a);
+    }
+    if (cq == 0) {
+      sred[warp * kRowsU + r] = t0a + t0b;
+      sred[warp * kRowsU + r + 8] = t2a + t2b;
+    }
+    cons_sync();
+    if (tid < kRowsU) {
+      float y = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCons; ++w) y += sred[w * kRowsU + tid];
+      const uint16_t yb = float_to_bf16_bits(y);
+      if (a.y) a.y[n0 + tid] = yb;
+      if (a.hres) {
+        const uint32_t hb = jd == 0 ? hres_pre0 : jd == 1 ? hres_pre1 : a.hres[n0 + tid];
+        a.hres[n0 + tid] = float_to_bf16_bits(bf16_bits_to_float(hb) + bf16_bits_to_float(yb));
+      }
+    }
+    cons_sync();
+    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);
+  }
+  if (tid == 0) trace_max(a.trace, kTrExit);
+}
+
+cudaError_t launch_decode_fused(const DecodeArgs &a, int n_blocks, cudaStream_t st, bool pdl) {
+  return launch_k(decode_layer_kernel, dim3(n_blocks), dim3(kThreadsF), fused_decode_smem(a.d), st, pdl, a);
+}
+
+cudaError_t decode_set_attributes() {
+  return cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+int decode_blocks_per_sm(const Dims &d) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel, kThreadsF, fused_decode_smem(d)) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace moe

@@ -132,7 +132,7 @@ __device__ __forceinline__ float stage_group(const uint16_t *__restrict__ src_ro
     const uint4 v0 = v[2 * c], v1 = v[2 * c + 1];
     const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     uint32_t out[8];
-    permute_quarter(in, out);
+    operand_quarter<!kHalf>(in, out);
 #pragma unroll
     for (int w = 0; w < 4; ++w) dst[4 * c + w] = make_uint2(out[2 * w], out[2 * w + 1]);
 #pragma unroll
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(const FfnArgs a) {
         const int m = it / (kRows * G), rem = it - m * kRows * G;
         const float s = bf16_bits_to_float(sraw[(2 * m) * kRows * G + rem]);
         const float b = bf16_bits_to_float(sraw[(2 * m + 1) * kRows * G + rem]);
-        ssb[it] = make_float2(s, fmaf(-128.0f, s, b));  // codes enter the mma as 128 + q
+        ssb[it] = make_float2(s * kCodeScale, b);  // codes enter the mma as q * 2^-24
       }
       __syncthreads();
       ready = true;
@@ -293,18 +293,14 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(const FfnArgs a) {
         const uint32_t wu0 = (s >> 1) ? u0.y : u0.x, wu1 = (s >> 1) ? u1.y : u1.x;
         uint32_t A[4], B[4];
         if ((s & 1) == 0) {
-          A[0] = codes_bf16_plus128<0>(wg0); A[1] = codes_bf16_plus128<0>(wg1);
-          A[2] = codes_bf16_plus128<1>(wg0); A[3] = codes_bf16_plus128<1>(wg1);
-          B[0] = codes_bf16_plus128<0>(wu0); B[1] = codes_bf16_plus128<0>(wu1);
-          B[2] = codes_bf16_plus128<1>(wu0); B[3] = codes_bf16_plus128<1>(wu1);
+          A[0] = codes_sub<0>(wg0); A[1] = codes_sub<0>(wg1); A[2] = codes_sub<1>(wg0); A[3] = codes_sub<1>(wg1);
+          B[0] = codes_sub<0>(wu0); B[1] = codes_sub<0>(wu1); B[2] = codes_sub<1>(wu0); B[3] = codes_sub<1>(wu1);
         } else {
-          A[0] = codes_bf16_plus128<2>(wg0); A[1] = codes_bf16_plus128<2>(wg1);
-          A[2] = codes_bf16_plus128<3>(wg0); A[3] = codes_bf16_plus128<3>(wg1);
-          B[0] = codes_bf16_plus128<2>(wu0); B[1] = codes_bf16_plus128<2>(wu1);
-          B[2] = codes_bf16_plus128<3>(wu0); B[3] = codes_bf16_plus128<3>(wu1);
+          A[0] = codes_sub<2>(wg0); A[1] = codes_sub<2>(wg1); A[2] = codes_sub<3>(wg0); A[3] = codes_sub<3>(wg1);
+          B[0] = codes_sub<2>(wu0); B[1] = codes_sub<2>(wu1); B[2] = codes_sub<3>(wu0); B[3] = codes_sub<3>(wu1);
         }
-        mma_bf16(ag, A, bx.x, bx.y);
-        mma_bf16(au, B, bx.x, bx.y);
+        mma_f16(ag, A, bx.x, bx.y);
+        mma_f16(au, B, bx.x, bx.y);
       }
       const float2 sg0 = ssb[r * G + g], sg1 = ssb[(r + 8) * G + g];
       const float2 su0 = ssb[(kRows + r) * G + g], su1 = ssb[(kRows + r + 8) * G + g];
@@ -436,7 +432,7 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(const FfnArgs a) 
     if (s < n_valid || (s == k && a.include_shared)) {
       const float sc = bf16_bits_to_float(sraw[(s * 2) * kRows * GI + rem]);
       const float bi = bf16_bits_to_float(sraw[(s * 2 + 1) * kRows * GI + rem]);
-      ssb[it] = make_float2(sc, bi);
+      ssb[it] = make_float2(sc * kCodeScale, bi);
     }
   }
   __syncthreads();
@@ -461,9 +457,9 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(const FfnArgs a) 
       const uint32_t x0 = (st >> 1) ? w0.y : w0.x, x1 = (st >> 1) ? w1.y : w1.x;
       uint32_t A[4];
       if ((st & 1) == 0) {
-        A[0] = codes_f16<0>(x0); A[1] = codes_f16<0>(x1); A[2] = codes_f16<1>(x0); A[3] = codes_f16<1>(x1);
+        A[0] = codes_sub<0>(x0); A[1] = codes_sub<0>(x1); A[2] = codes_sub<1>(x0); A[3] = codes_sub<1>(x1);
       } else {
-        A[0] = codes_f16<2>(x0); A[1] = codes_f16<2>(x1); A[2] = codes_f16<3>(x0); A[3] = codes_f16<3>(x1);
+        A[0] = codes_sub<2>(x0); A[1] = codes_sub<2>(x1); A[2] = codes_sub<3>(x0); A[3] = codes_sub<3>(x1);
       }
       mma_f16(acc, A, bx.x, bx.y);
     }
@@ -558,7 +554,7 @@ __global__ void __launch_bounds__(kDgThreads) down_grouped_kernel(const FfnArgs 
       if (!block_wait(bar, 0, a.err)) return;
       if (tid == 0) trace_max(a.trace, kTrLoaded);
       for (int it = tid; it < kDownRows * GI; it += kDgThreads) {
-        ssb[it] = make_float2(bf16_bits_to_float(sraw[it]), bf16_bits_to_float(sraw[kDownRows * GI + it]));
+        ssb[it] = make_float2(bf16_bits_to_float(sraw[it]) * kCodeScale, bf16_bits_to_float(sraw[kDownRows * GI + it]));
       }
       __syncthreads();
       ready = true;
@@ -577,9 +573,9 @@ __global__ void __launch_bounds__(kDgThreads) down_grouped_kernel(const FfnArgs 
         const uint32_t x0 = (st >> 1) ? w0.y : w0.x, x1 = (st >> 1) ? w1.y : w1.x;
         uint32_t A[4];
         if ((st & 1) == 0) {
-          A[0] = codes_f16<0>(x0); A[1] = codes_f16<0>(x1); A[2] = codes_f16<1>(x0); A[3] = codes_f16<1>(x1);
+          A[0] = codes_sub<0>(x0); A[1] = codes_sub<0>(x1); A[2] = codes_sub<1>(x0); A[3] = codes_sub<1>(x1);
         } else {
-          A[0] = codes_f16<2>(x0); A[1] = codes_f16<2>(x1); A[2] = codes_f16<3>(x0); A[3] = codes_f16<3>(x1);
+          A[0] = codes_sub<2>(x0); A[1] = codes_sub<2>(x1); A[2] = codes_sub<3>(x0); A[3] = codes_sub<3>(x1);
         }
         mma_f16(acc, A, bx.x, bx.y);
       }

@@ -51,6 +51,29 @@ struct SortArgs {
   unsigned long long *trace;  // nullable: 4 trace slots of this launch (common.cuh)
 };
 
+// Fused single-token layer (decode.cu): one persistent block per SM.
+struct DecodeArgs {
+  LayerPtrs w;
+  Dims d;                   // T == 1
+  const uint16_t *x;        // bf16 [H] block input (normalize == 0)
+  uint16_t *hres;           // bf16 [H] residual stream (normalize == 1), updated in place
+  uint16_t *xn_user;        // nullable: normalised input out
+  float *logits;            // fp32 [E] (user buffer or workspace)
+  int32_t *ids_user;        // nullable [k]
+  float *wts_user;          // nullable [k]
+  __half *hbuf;             // fp16 [k+1, I]: slot 0 shared, slot j+1 = j-th selected
+  uint16_t *y;              // nullable bf16 [H]
+  unsigned *sync;           // grid barrier area: [0] epoch, [32] release, [64..] per-block flags
+  unsigned *err;
+  unsigned long long *trace;
+  int normalize;
+};
+
+size_t fused_decode_smem(const Dims &d);
+int decode_blocks_per_sm(const Dims &d);
+cudaError_t decode_set_attributes();
+cudaError_t launch_decode_fused(const DecodeArgs &a, int n_blocks, cudaStream_t st, bool pdl);
+
 // smem budgets (bytes) for a given shape; 0 = shape not supported by that kernel
 size_t router_smem(const Dims &d, int tb);
 size_t gateup_smem(const Dims &d, int tt);

@@ -212,6 +212,51 @@ def test_small_shapes(moe, hidden_dim, inter, n_experts, k, n_tokens):
     assert_close(bf16_bits_to_f64(out["y"]), ref["y"], "small-shape y")
 
 
+@pytest.mark.parametrize("residual", [False, True])
+def test_single_token_paths_agree(layer0, residual):
+    """T == 1 runs the fused one-launch layer kernel by default; a handle
+    created with MOE_DECODE_FUSED=0 runs the router/gate-up/down chain.  Both
+    must match the oracle; ids must be identical."""
+    import os
+    outs = {}
+    for fused in ("1", "0"):
+        old = os.environ.get("MOE_DECODE_FUSED")
+        os.environ["MOE_DECODE_FUSED"] = fused
+        try:
+            m = bq.Moe()
+        finally:
+            if old is None:
+                del os.environ["MOE_DECODE_FUSED"]
+            else:
+                os.environ["MOE_DECODE_FUSED"] = old
+        w = weights_of(layer0)
+        x_bits = hidden(2024, 0, 1, rms=not residual)
+        h = to_dev_bf16(x_bits)
+        y = torch.empty_like(h)
+        xo = torch.empty_like(h)
+        ids = torch.empty((1, K), dtype=torch.int32, device="cuda")
+        logits = torch.empty((1, E), dtype=torch.float32, device="cuda")
+        ws = workspace(m, w, 1)
+        if residual:
+            m.layer_forward_residual(h, 1, w, ws, y_out=y, x_out=xo, ids_out=ids, logits_out=logits)
+        else:
+            m.layer_forward(h, 1, w, y, ws, ids_out=ids, logits_out=logits)
+        torch.cuda.synchronize()
+        assert m.get_error() == bq.MOE_OK
+        x_used = from_dev_bf16(xo) if residual else x_bits
+        out = {"ids": ids.cpu().numpy(), "logits": logits.cpu().numpy(), "y": from_dev_bf16(y), "x": x_used,
+               "h": from_dev_bf16(h)}
+        assert np.array_equal(out["ids"], O.select_top_k(out["logits"], K))
+        ref = oracle_layer(layer0, x_used, K, out["ids"])
+        assert_close(bf16_bits_to_f64(out["y"]), ref["y"], f"y fused={fused}")
+        if residual:
+            assert np.array_equal(out["h"], O.residual_add(x_bits, out["y"]))
+        outs[fused] = out
+        m.close()
+    assert np.array_equal(outs["1"]["ids"], outs["0"]["ids"])
+    assert np.array_equal(outs["1"]["x"], outs["0"]["x"])
+
+
 def test_argument_errors(moe, layer0):
     w = weights_of(layer0)
     x = to_dev_bf16(hidden(0, 0, 2))
