@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH):
         "moe_layer_forward_residual": (I, [V, V, I, P(LayerWeights), V, V, V, V, V, Z, V]),
         "moe_selftest_wait_timeout": (I, [V, ctypes.c_ulonglong, V]),
         "moe_set_trace": (I, [V, V, I]),
+        "moe_layer_forward_static": (I, [V, P(LayerWeights), V, V, V, V, V]),
         "moe_get_error": (I, [V, P(I)]),
     }
     for name, (res, args) in proto.items():
@@ -134,6 +135,17 @@ def make_layer_weights(dims: Dims, router_q: int, router_s: int, router_b: int, 
     """LayerWeights from device addresses; `layout` maps gate_q .. down_b to byte offsets."""
     return LayerWeights(dims, QMat(router_q, router_s, router_b), experts, expert_stride,
                         BlobLayout(*[layout[n] for n in _BLOB_FIELDS]), shared, _ptr(logit_bias))
+
+
+def layer_forward_static(x, w: LayerWeights, y, ids_out=None, logits_out=None, weights_out=None, stream=None):
+    """moe_layer_forward_static: one token, no handle, no workspace.
+
+    For hosts that cannot allocate device memory; the library's scratch for
+    this call is a fixed static device array (see include/moe.h)."""
+    st = load_library().moe_layer_forward_static(_ptr(x), ctypes.byref(w), _ptr(y), _ptr(ids_out), _ptr(logits_out),
+                                                 _ptr(weights_out), _stream(stream))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_layer_forward_static")
 
 
 class Moe:

@@ -187,6 +187,30 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
                                int32_t *ids_out, float *logits_out, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* Single-token layer call that allocates nothing (the pages have no
+ * counterpart: it exists for hosts that cannot allocate device memory,
+ * e.g. a program whose own pool owns the whole device, or a per-token loop
+ * where an allocation would stall the device and cannot be captured).
+ * Same computation as moe_layer_forward with n_tokens = 1 on the fused
+ * single-token kernel, but with no handle and no workspace: its scratch
+ * (h, logits when logits_out is NULL, the grid-barrier counter and the
+ * device error word) is one 16 KiB static device array that every GPU
+ * loading this library holds until the process exits.
+ *   x    bf16 [H] in;  y bf16 [H] out;  ids_out int32 [k], logits_out
+ *        fp32 [E], weights_out fp32 [k] nullable.
+ * Limits: (top_k + 1) * inter * 2 <= 15 KiB (top-8 of inter 704 uses
+ * 12,672 B) and the fused kernel's
+ * conditions (n_experts <= SM count, its shared memory fits); otherwise
+ * MOE_ERR_UNSUPPORTED and nothing is launched.  The first call on a device
+ * looks up the array's device address and sets kernel attributes, so make
+ * it before any stream capture.  Every call clears the counter and error
+ * word, then launches; the array keeps the last call's contents.  Calls
+ * that overlap on the GPU (different streams, or the same array from two
+ * threads) race on the shared scratch.  Device-side error flags of this
+ * call (bounded-wait timeouts, non-finite logits) are not reported. */
+int moe_layer_forward_static(const void *x, const moe_layer_weights *w, void *y, int32_t *ids_out,
+                             float *logits_out, float *weights_out, moe_stream_t stream);
+
 /* Launch tracing (diagnostics).  With a non-null device buffer of
  * 4 * n_launches u64, each subsequent kernel launch by this handle takes the
  * next 4 slots (wrapping) and records %globaltimer values, combined with
