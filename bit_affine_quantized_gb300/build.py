@@ -16,8 +16,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "moe")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300.so")
-SOURCES = ["abi.cu", "router.cu", "ffn.cu", "decode.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "kernels.h"]
+SOURCES = ["abi.cu", "router.cu", "ffn.cu", "decode.cu", "prefill.cu", "noalloc.cu"]
+HEADERS = ["common.cuh", "fused.cuh", "kernels.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

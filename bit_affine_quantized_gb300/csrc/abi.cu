@@ -19,6 +19,8 @@ struct moe_handle {
   int n_sm;                   // multiprocessors: grid of the fused decode kernel
   bool fused;                 // single-token calls use the fused layer kernel
   int fused_key[3], fused_ok; // cached shape check (hidden, inter, top_k) -> usable
+  bool prefill;               // multi-token layer calls use the fused prefill kernel
+  int prefill_key[4], prefill_ok;  // cached check (hidden, inter, n_experts, top_k) -> usable
 };
 
 namespace {
@@ -35,9 +37,12 @@ unsigned long long *take_trace(moe_handle *h, int n) {
 namespace {
 
 constexpr size_t kSmemCap = 227 * 1024;
-// handle-owned device words: [0] error bits, [1] router ticket; from
-// kSyncOffset the fused kernel's grid barrier (epoch, release, per-block flags)
+// handle-owned device words: [0] error bits, [1] router ticket; at
+// kSyncOffset the single-token kernel's 64-bit grid barrier counter, at
+// kPrefillSyncOffset the prefill kernel's (each launch of a kernel adds a
+// fixed multiple of its grid size to its own counter, so they stay apart)
 constexpr size_t kSyncOffset = 256;
+constexpr size_t kPrefillSyncOffset = kSyncOffset + 16;
 constexpr size_t kDeviceWords = kSyncOffset + 64 + 1024;
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -72,7 +77,7 @@ size_t blob_extent(const moe_layer_weights &w) {
 }
 
 struct WsLayout {
-  size_t logits, ids, wts, counts, offsets, perm, pos, act_e, act_beg, act_cnt, n_act, xn, h, o, total;
+  size_t logits, ids, wts, counts, offsets, perm, pos, act_e, act_beg, act_cnt, n_act, xn, h, o, xq, hq, total;
 };
 
 WsLayout ws_layout(const moe_dims &d, int T) {
@@ -98,6 +103,9 @@ WsLayout ws_layout(const moe_dims &d, int T) {
   L.xn = take((size_t)T * H * 2);
   L.h = take(((size_t)T * k + T) * I * 2);
   L.o = moe::use_down_decode(to_dims(d, T)) ? off : take(((size_t)T * k + T) * H * 4);
+  // quarter sums of the fused prefill kernel (its operand rows reuse xn and h)
+  L.xq = T > 1 ? take((size_t)T * (H / 16) * 4) : off;
+  L.hq = T > 1 ? take(((size_t)T * k + T) * (I / 16) * 4) : off;
   L.total = off;
   return L;
 }
@@ -212,6 +220,44 @@ int run_fused(moe_handle *h, const moe_layer_weights *w, const void *x, void *hr
   return cuda_status(moe::launch_decode_fused(a, h->n_sm, st, h->pdl));
 }
 
+// The fused prefill kernel: one resident block per SM (grid barriers).
+bool use_prefill(moe_handle *h, const moe_layer_weights *w, int T) {
+  if (!h->prefill || T < 2 || h->n_sm > 1024) return false;
+  const int key[4] = {w->dims.hidden, w->dims.inter, w->dims.n_experts, w->dims.top_k};
+  if (memcmp(key, h->prefill_key, sizeof(key)) != 0) {
+    const moe::Dims d = to_dims(w->dims, moe::kMaxTokens);
+    h->prefill_ok = moe::prefill_fused_smem(d) != 0 && moe::prefill_blocks_per_sm(d) >= 1;
+    memcpy(h->prefill_key, key, sizeof(key));
+  }
+  return h->prefill_ok != 0;
+}
+
+int run_prefill(moe_handle *h, const moe_layer_weights *w, int T, const void *x, void *hres, void *y, void *x_out,
+                float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(w->dims, T);
+  moe::PrefillArgs a;
+  a.w = layer_ptrs(*w);
+  a.d = to_dims(w->dims, T);
+  a.x = (const uint16_t *)x;
+  a.hres = (uint16_t *)hres;
+  a.xn_user = (uint16_t *)x_out;
+  a.logits = logits ? logits : (float *)(ws + L.logits);
+  a.ids_user = ids;
+  a.wts_user = wts;
+  a.r = routing_in(ws, L);
+  a.xperm = (__half *)(ws + L.xn);
+  a.xq = (float *)(ws + L.xq);
+  a.hperm = (__half *)(ws + L.h);
+  a.hq = (float *)(ws + L.hq);
+  a.obuf = (float *)(ws + L.o);
+  a.y = (uint16_t *)y;
+  a.sync = h->dwords + kPrefillSyncOffset;
+  a.err = h->dwords;
+  a.trace = take_trace(h, 1);
+  a.normalize = hres != nullptr;
+  return cuda_status(moe::launch_prefill_fused(a, h->n_sm, st, h->pdl));
+}
+
 int run_ffn(moe_handle *h, const moe_layer_weights *w, int T, const void *x, const moe::Routing &r, int include_shared,
             void *y, void *hres, uint8_t *ws, cudaStream_t st) {
   const WsLayout L = ws_layout(w->dims, T);
@@ -262,7 +308,7 @@ int moe_create(moe_handle **out) {
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
   if (moe::router_set_attributes() != cudaSuccess || moe::ffn_set_attributes() != cudaSuccess ||
-      moe::decode_set_attributes() != cudaSuccess)
+      moe::decode_set_attributes() != cudaSuccess || moe::prefill_set_attributes() != cudaSuccess)
     return MOE_ERR_CUDA;
   moe_handle *h = (moe_handle *)calloc(1, sizeof(moe_handle));
   if (!h) return MOE_ERR_CUDA;
@@ -270,6 +316,8 @@ int moe_create(moe_handle **out) {
   h->n_sm = prop.multiProcessorCount;
   const char *fz = getenv("MOE_DECODE_FUSED");
   h->fused = !(fz && fz[0] == '0');
+  const char *pz = getenv("MOE_PREFILL_FUSED");
+  h->prefill = !(pz && pz[0] == '0');
   if (cudaMalloc(&h->dwords, kDeviceWords * sizeof(unsigned)) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
@@ -374,6 +422,9 @@ int moe_layer_forward(moe_handle *h, const void *x, int n_tokens, const moe_laye
   uint8_t *wsb = (uint8_t *)ws;
   if (use_fused(h, w, n_tokens))
     return run_fused(h, w, x, nullptr, y, nullptr, logits_out, ids_out, weights_out, wsb, (cudaStream_t)stream);
+  if (use_prefill(h, w, n_tokens))
+    return run_prefill(h, w, n_tokens, x, nullptr, y, nullptr, logits_out, ids_out, weights_out, wsb,
+                       (cudaStream_t)stream);
   if ((st = run_router(h, w, n_tokens, x, nullptr, nullptr, logits_out, ids_out, weights_out, wsb,
                        (cudaStream_t)stream)))
     return st;
@@ -396,6 +447,9 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens, const 
   const WsLayout L = ws_layout(w->dims, n_tokens);
   if (use_fused(h, w, n_tokens))
     return run_fused(h, w, nullptr, hidden, y_out, x_out, logits_out, ids_out, nullptr, wsb, (cudaStream_t)stream);
+  if (use_prefill(h, w, n_tokens))
+    return run_prefill(h, w, n_tokens, nullptr, hidden, y_out, x_out, logits_out, ids_out, nullptr, wsb,
+                       (cudaStream_t)stream);
   if ((st = run_router(h, w, n_tokens, nullptr, hidden, x_out, logits_out, ids_out, nullptr, wsb,
                        (cudaStream_t)stream)))
     return st;

@@ -69,6 +69,34 @@ struct DecodeArgs {
   int normalize;
 };
 
+// Fused multi-token layer (prefill.cu): one persistent block per SM, 2 <= T <= 128.
+struct PrefillArgs {
+  LayerPtrs w;
+  Dims d;
+  const uint16_t *x;        // bf16 [T, H] block input (normalize == 0)
+  uint16_t *hres;           // bf16 [T, H] residual stream (normalize == 1), updated in place
+  uint16_t *xn_user;        // nullable: normalised input out
+  float *logits;            // fp32 [T, E] (user buffer or workspace)
+  int32_t *ids_user;        // nullable [T, k]
+  float *wts_user;          // nullable [T, k]
+  Routing r;                // ids, wts used
+  __half *xperm;            // fp16 [T, H] permuted operand rows
+  float *xq;                // fp32 [T, H/16] quarter sums of x
+  __half *hperm;            // fp16 [T*k + T, I] permuted h rows per sorted position
+  float *hq;                // fp32 [T*k + T, I/16] quarter sums of h
+  float *obuf;              // fp32 [T*k + T, H] weighted expert outputs
+  uint16_t *y;              // nullable bf16 [T, H]
+  unsigned *sync;           // 64-bit grid barrier counter (this kernel's own)
+  unsigned *err;
+  unsigned long long *trace;
+  int normalize;
+};
+
+size_t prefill_fused_smem(const Dims &d);  // 0: shape not supported
+int prefill_blocks_per_sm(const Dims &d);
+cudaError_t prefill_set_attributes();
+cudaError_t launch_prefill_fused(const PrefillArgs &a, int n_blocks, cudaStream_t st, bool pdl);
+
 size_t fused_decode_smem(const Dims &d);
 int decode_blocks_per_sm(const Dims &d);
 cudaError_t decode_set_attributes();

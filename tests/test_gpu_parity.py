@@ -213,48 +213,54 @@ def test_small_shapes(moe, hidden_dim, inter, n_experts, k, n_tokens):
 
 
 @pytest.mark.parametrize("residual", [False, True])
-def test_single_token_paths_agree(layer0, residual):
-    """T == 1 runs the fused one-launch layer kernel by default; a handle
-    created with MOE_DECODE_FUSED=0 runs the router/gate-up/down chain.  Both
-    must match the oracle; ids must be identical."""
+@pytest.mark.parametrize("n_tokens", [1, 2, 37, 128])
+def test_fused_and_chained_paths_agree(layer0, layer0_zipf, residual, n_tokens):
+    """Layer calls run a fused one-launch kernel by default (the single-token
+    kernel for T == 1, the prefill kernel for 2 <= T <= 128); a handle created
+    with MOE_DECODE_FUSED=0 / MOE_PREFILL_FUSED=0 runs the router, gate/up and
+    down launches instead.  Both must match the oracle; ids must be identical."""
     import os
+    var = "MOE_DECODE_FUSED" if n_tokens == 1 else "MOE_PREFILL_FUSED"
+    layer = layer0_zipf if n_tokens == 128 else layer0
     outs = {}
     for fused in ("1", "0"):
-        old = os.environ.get("MOE_DECODE_FUSED")
-        os.environ["MOE_DECODE_FUSED"] = fused
+        old = os.environ.get(var)
+        os.environ[var] = fused
         try:
             m = bq.Moe()
         finally:
             if old is None:
-                del os.environ["MOE_DECODE_FUSED"]
+                del os.environ[var]
             else:
-                os.environ["MOE_DECODE_FUSED"] = old
-        w = weights_of(layer0)
-        x_bits = hidden(2024, 0, 1, rms=not residual)
+                os.environ[var] = old
+        w = weights_of(layer)
+        x_bits = hidden(2024, 0, n_tokens, rms=not residual)
         h = to_dev_bf16(x_bits)
         y = torch.empty_like(h)
         xo = torch.empty_like(h)
-        ids = torch.empty((1, K), dtype=torch.int32, device="cuda")
-        logits = torch.empty((1, E), dtype=torch.float32, device="cuda")
-        ws = workspace(m, w, 1)
+        ids = torch.empty((n_tokens, K), dtype=torch.int32, device="cuda")
+        logits = torch.empty((n_tokens, E), dtype=torch.float32, device="cuda")
+        ws = workspace(m, w, n_tokens)
         if residual:
-            m.layer_forward_residual(h, 1, w, ws, y_out=y, x_out=xo, ids_out=ids, logits_out=logits)
+            m.layer_forward_residual(h, n_tokens, w, ws, y_out=y, x_out=xo, ids_out=ids, logits_out=logits)
         else:
-            m.layer_forward(h, 1, w, y, ws, ids_out=ids, logits_out=logits)
+            m.layer_forward(h, n_tokens, w, y, ws, ids_out=ids, logits_out=logits)
         torch.cuda.synchronize()
         assert m.get_error() == bq.MOE_OK
         x_used = from_dev_bf16(xo) if residual else x_bits
         out = {"ids": ids.cpu().numpy(), "logits": logits.cpu().numpy(), "y": from_dev_bf16(y), "x": x_used,
                "h": from_dev_bf16(h)}
         assert np.array_equal(out["ids"], O.select_top_k(out["logits"], K))
-        ref = oracle_layer(layer0, x_used, K, out["ids"])
+        ref = oracle_layer(layer, x_used, K, out["ids"])
         assert_close(bf16_bits_to_f64(out["y"]), ref["y"], f"y fused={fused}")
         if residual:
             assert np.array_equal(out["h"], O.residual_add(x_bits, out["y"]))
+            xr = bf16_bits_to_f64(O.rmsnorm_no_scale(x_bits))
+            # fp32 on the device against fp64: at most one bf16 rounding step apart
+            assert np.all(np.abs(bf16_bits_to_f64(out["x"]) - xr) <= 2.0 ** -7 * np.abs(xr))
         outs[fused] = out
         m.close()
     assert np.array_equal(outs["1"]["ids"], outs["0"]["ids"])
-    assert np.array_equal(outs["1"]["x"], outs["0"]["x"])
 
 
 def test_argument_errors(moe, layer0):
