@@ -71,7 +71,8 @@ __device__ __forceinline__ float key_value(unsigned k) {
 
 // Top-k of E <= 128 fp32 logits by one warp: ids by descending logit, ties to
 // the lower id (two warp reductions per pick), softmax weights over the k.
-// Non-finite logits count as -inf and set *nonfinite.
+// Non-finite logits count as -inf and set *nonfinite.  `logits` is read with
+// plain loads: shared memory, or global memory this block wrote itself.
 __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int32_t *ids_out, float *wts_out,
                                           bool *nonfinite) {
   const int lane = threadIdx.x & 31;
@@ -82,7 +83,7 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
     const int e = lane + 32 * i;
     key[i] = 0u;  // below every real key: never picked while k <= E
     if (e < E) {
-      float x = __ldcg(logits + e);
+      float x = logits[e];
       if (!isfinite(x)) {
         x = -INFINITY;
         bad = true;

@@ -5,29 +5,27 @@
 // token/expert pairs are grouped per expert, the routed experts run on their
 // groups and the shared branch on every row, and the branches are combined.
 //
-// One persistent block per SM; 16 consumer warps and 1 producer warp.
-//   A  tokens t = block, block + grid, ...: x = input (or rmsnorm of the
-//      residual) -> bf16 copy, permuted fp16 operand rows and quarter sums
-//      in the workspace;
-//   B  router tasks (8 experts x 8 tokens): each task normalises its own 8
-//      rows from the input, so no barrier separates it from A;
-//   == barrier 1 ==  top-k of tokens t = block, ... (one warp each)
-//   == barrier 2 ==  every block groups all pairs in shared memory (stable
+// One persistent block per SM; 16 consumer warps and 1 producer warp.  The
+// producer streams weight tiles through a 3-slot ring (W) and operand rows
+// into one buffer (X) that stays put while consecutive units share a chunk.
+//   R  tokens t = block, block + grid, ...: x = input (or rmsnorm of the
+//      residual); permuted fp16 operand rows and quarter sums go to the
+//      workspace for the experts; the block scores its own token against
+//      the router streamed through W in 16-expert tiles (tensor cores, 8-bit
+//      codes as exact fp16 subnormals), then selects the top-k;
+//   == barrier 1 ==  every block groups all pairs in shared memory (stable
 //      counting sort) and derives the unit lists;
-//   C  gate/up units (active slot, 8-token chunk, 16 rows of I): the
-//      producer streams the 16-row gate/up tile and the chunk's operand rows
-//      into a 2-slot ring; consumers compute GeGLU and write h as permuted
-//      fp16 quarters with their sums;
+//   G  gate/up units (slot, 8-token chunk, 16 rows of I), a contiguous
+//      range per block: GeGLU, h written as permuted fp16 quarters + sums;
+//   == barrier 2 ==
+//   D  down units (slot, chunk, 128 rows of H): weighted outputs w * o in
+//      fp32 per sorted position; their weight tiles stream during barrier 2;
 //   == barrier 3 ==
-//   D  down units (slot, chunk, 64 rows of H): weighted outputs w * o (fp32)
-//      per sorted position; the weight tiles of the first units are already
-//      in flight during the barrier;
-//   == barrier 4 ==
-//   E  combine of tokens t = block, ...: y = sum_j o[pos(t, j)] + o[shared t]
+//   C  combine of tokens t = block, ...: y = sum_j o[pos(t, j)] + o[shared t]
 //      in selection order, bf16 out, optional residual add.
-// The gate/up and down math is the tensor-core scheme of the other kernels:
-// codes as exact fp16 subnormals, activations permuted and /16 on the odd
-// slots, per-group correction (scale * 2^24) * acc + bias * sum.
+// Expert math: 4-bit codes as exact fp16 subnormals (code * 2^-24; odd
+// nibbles come out * 16 and meet activations stored / 16), per-group
+// correction (scale * 2^24) * acc + bias * sum(x).
 #include <math.h>
 
 #include "fused.cuh"
@@ -39,57 +37,72 @@ namespace {
 using fused::cons_sync;
 using fused::kCons;
 using fused::kConsThreads;
-constexpr int kSlots = 2;
-constexpr int kTC = 8;        // tokens per unit (one mma N tile)
-constexpr int kGuRows = 16;   // gate/up rows per unit
-constexpr int kDnRows = 64;   // down rows per unit (4 x m16)
-constexpr int kNBar = 4;      // grid barriers per launch
+constexpr int kWSlots = 3;   // weight ring
+constexpr int kTC = 8;       // tokens per unit (one mma N tile)
+constexpr int kGuRows = 16;  // gate/up rows per unit (each of gate and up)
+constexpr int kDnRows = 128; // down rows per unit (8 x m16)
+constexpr int kRtRows = 16;  // router experts per tile
+constexpr int kNBar = 3;     // grid barriers per launch
+constexpr int kRedBytes = kCons * 256 * 4;
 
 __host__ __device__ inline int pw8(int w) { return w + ((8 - (w % 16)) + 16) % 16; }
 __host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
+__host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
 
 struct PL {
-  int G, GI, nrt, nrt_dn;
-  int gu_qp, gu_w, gu_x, gu_xq, gu_bytes;
-  int dn_qp, dn_w, dn_h, dn_hq, dn_bytes;
-  int slot, ring, grp, misc, total;
+  int G, GI, nrt, nrt_dn, n_mt;
+  int gu_qp, rt_qp, dn_qp, wslot;   // W slot: code row pitches, slot bytes
+  int xp, xqp, x_xq;                // X as gate/up operand: row pitch (B), quarter-sum pitch (floats), offset
+  int hp, hqp, x_hq;                // X as down operand
+  int rx_q, rx_sb;                  // X as router operand: quarter sums after the fp16 row, then the
+                                    // router's scales and biases (bf16 [16 n_mt][G] each)
+  int xbuf;
+  int ring, xb, red, grp, misc, total;
 };
 
+// Row pitches: 8-byte fragment loads of 8 rows hit disjoint banks when the
+// pitch is 8 mod 16 words (gate/up, down codes); 16-byte loads of 2 rows
+// when it is 64 mod 128 bytes (router codes) or 4 mod 8 words (operands).
 __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) {
   PL L;
   L.G = H / kGroup;
   L.GI = I / kGroup;
   L.nrt = I / kGuRows;
-  L.nrt_dn = H / kDnRows;
+  L.nrt_dn = (H + kDnRows - 1) / kDnRows;
+  L.n_mt = (E + kRtRows - 1) / kRtRows;
   L.gu_qp = pw8(H / 8) * 4;
-  L.gu_w = 2 * kGuRows * L.gu_qp + 4 * kGuRows * L.G * 2;  // gate, up codes + 4 scale/bias tiles
-  L.gu_x = al16(L.gu_w);                                   // kTC operand rows (fp16, H)
-  L.gu_xq = L.gu_x + kTC * H * 2;                          // kTC rows of quarter sums (H/16 fp32)
-  L.gu_bytes = al16(L.gu_xq + kTC * (H / 16) * 4);
-  // the cross-warp reduction (8 floats per consumer lane) reuses the operand rows
-  L.gu_bytes = max(L.gu_bytes, L.gu_x + kConsThreads * 8 * 4);
+  L.rt_qp = H + ((64 - H % 128) + 128) % 128;
   L.dn_qp = pw8(I / 8) * 4;
-  L.dn_w = kDnRows * L.dn_qp + 2 * kDnRows * L.GI * 2;
-  L.dn_h = al16(L.dn_w);                                   // kTC h rows (fp16, I)
-  L.dn_hq = L.dn_h + kTC * I * 2;
-  L.dn_bytes = al16(L.dn_hq + kTC * (I / 16) * 4);
-  L.dn_bytes = max(L.dn_bytes, L.dn_h + kConsThreads * 4 * 4);  // reduction: 4 floats per lane over the h rows
-  L.slot = al16(L.gu_bytes > L.dn_bytes ? L.gu_bytes : L.dn_bytes);
-  L.ring = 0;
-  int o = kSlots * L.slot;
-  L.grp = o;  // chunk0 int32 [E+2], perm int16 [T*k], pos int16 [T*k], act_e/beg/cnt int16 [E+1] each
+  const int gu = 2 * kGuRows * L.gu_qp + 4 * kGuRows * L.G * 2;
+  const int rt = kRtRows * L.rt_qp;
+  const int dn = kDnRows * L.dn_qp + 2 * kDnRows * L.GI * 2;
+  L.wslot = al16(imax(gu, imax(rt, dn)));
+  L.xp = 2 * H + 16;
+  L.xqp = H / 16 + 4;
+  L.x_xq = kTC * L.xp;
+  L.hp = 2 * I + 16;
+  L.hqp = I / 16 + 4;
+  L.x_hq = kTC * L.hp;
+  L.rx_q = 2 * H;
+  L.rx_sb = al16(L.rx_q + (H / 16) * 4);
+  L.xbuf = al16(imax(L.x_xq + kTC * L.xqp * 4, imax(L.x_hq + kTC * L.hqp * 4, L.rx_sb + 2 * kRtRows * L.n_mt * L.G * 2)));
+  int o = 0;
+  L.ring = o;
+  o += kWSlots * L.wslot;
+  L.xb = o;
+  o += L.xbuf;
+  L.red = o;  // cross-warp reductions, grouping temporaries
+  o += imax(kRedBytes, (1 + kCons) * E * 4);
+  L.grp = o;  // chunk0 int32 [E+2], perm/pos int16 [T*k], act_e/beg/cnt int16 [E+1]
   o = al16(o + (E + 2) * 4 + 2 * T * k * 2 + 3 * (E + 1) * 2);
-  L.misc = o;  // flags, h staging [kTC][16] fp16, mbarriers
+  L.misc = o;
   o = al16(o + 1024);
   L.total = o;
   return L;
 }
 
-// Router scratch (8 rows of x as fp32) and the sort's temporaries alias the
-// ring: neither is live once the producer starts.
-__host__ __device__ inline bool prefill_fits(const PL &L, int H, int E) {
-  return L.total <= 227 * 1024 && kSlots * L.slot >= kTC * H * 4 && kSlots * L.slot >= (1 + kCons) * E * 4;
-}
+// misc: s_flag int[16] | s_hst fp16[8][16] | s_logit float[128] | s_part float[16] | mbarriers [10] | s_wt float[8]
+constexpr int kMiscHst = 64, kMiscLogit = 320, kMiscPart = 832, kMiscBar = 896, kMiscWt = 976;
 
 // First index i in [0, n) with v[i + 1] > x (v ascending, v[0] == 0).
 __device__ __forceinline__ int find_slot(const int *v, int n, int x) {
@@ -101,20 +114,54 @@ __device__ __forceinline__ int find_slot(const int *v, int n, int x) {
   return lo;
 }
 
-// One 64-wide group of a gate/up unit for an 8-token tile: rows r, r+8 of
-// gate and up, token columns 2cq, 2cq+1.
-__device__ __forceinline__ void gu_group8(const uint8_t *tile, const uint8_t *xrows, const float *xq, int H, int G,
-                                          int qp, int g, int r, int cq, float (&tg)[4], float (&tu)[4]) {
-  const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 2 * 16 * qp);
+// Two 8-bit codes as exact fp16 subnormals: bytes 0 and 2, or 1 and 3.
+__device__ __forceinline__ uint32_t bytes02(uint32_t w) { return __byte_perm(w, 0u, 0x4240); }
+__device__ __forceinline__ uint32_t bytes13(uint32_t w) { return __byte_perm(w, 0u, 0x4341); }
+
+// Router: one 64-wide group of a 16-expert tile against one token (column 0,
+// supplied by the lanes with r == 0).  rx holds, per quarter, the pairs
+// (x0,x2)(x1,x3)(x4,x6)... so that k-step s meets code word s of the lane.
+// rs/rb: the tile's scales and biases ([row][G] bf16).
+__device__ __forceinline__ void rt_group(const uint8_t *tile, const uint8_t *rx, const float *rq, const uint16_t *rs,
+                                         const uint16_t *rb, int qp, int G, int g, int r, int cq, float &t0,
+                                         float &t1) {
+  const uint4 w0 = *reinterpret_cast<const uint4 *>(tile + r * qp + g * 64 + cq * 16);
+  const uint4 w1 = *reinterpret_cast<const uint4 *>(tile + (r + 8) * qp + g * 64 + cq * 16);
+  uint4 b0 = make_uint4(0u, 0u, 0u, 0u), b1 = b0;
+  if (r == 0) {
+    b0 = *reinterpret_cast<const uint4 *>(rx + g * 128 + cq * 32);
+    b1 = *reinterpret_cast<const uint4 *>(rx + g * 128 + cq * 32 + 16);
+  }
+  const uint32_t a0[4] = {w0.x, w0.y, w0.z, w0.w}, a1[4] = {w1.x, w1.y, w1.z, w1.w};
+  const uint32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const uint32_t A[4] = {bytes02(a0[s]), bytes02(a1[s]), bytes13(a0[s]), bytes13(a1[s])};
+    mma_f16(acc, A, bb[2 * s], bb[2 * s + 1]);
+  }
+  const float4 q = *reinterpret_cast<const float4 *>(rq + 4 * g);
+  const float xs = ((q.x + q.y) + q.z) + q.w;
+  t0 = fmaf(bf16_bits_to_float(rb[r * G + g]), xs, fmaf(bf16_bits_to_float(rs[r * G + g]) * kCodeScale, acc[0], t0));
+  t1 = fmaf(bf16_bits_to_float(rb[(r + 8) * G + g]), xs,
+            fmaf(bf16_bits_to_float(rs[(r + 8) * G + g]) * kCodeScale, acc[2], t1));
+}
+
+// Gate/up: one 64-wide group for an 8-token tile: rows r, r+8 of gate and
+// up, token columns 2cq, 2cq+1.
+__device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xrows, const float *xq, int qp, int xp,
+                                         int xqp, int G, int g, int r, int cq, float (&tg)[4], float (&tu)[4]) {
+  const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 2 * kGuRows * qp);  // gs, gb, us, ub [16][G]
   const uint2 g0 = *reinterpret_cast<const uint2 *>(tile + r * qp + g * 32 + cq * 8);
   const uint2 g1 = *reinterpret_cast<const uint2 *>(tile + (r + 8) * qp + g * 32 + cq * 8);
   const uint2 u0 = *reinterpret_cast<const uint2 *>(tile + (16 + r) * qp + g * 32 + cq * 8);
   const uint2 u1 = *reinterpret_cast<const uint2 *>(tile + (16 + r + 8) * qp + g * 32 + cq * 8);
-  const uint8_t *xb = xrows + r * H * 2 + g * 128 + cq * 32;  // token row n = r
+  const uint4 bA = *reinterpret_cast<const uint4 *>(xrows + r * xp + g * 128 + cq * 32);
+  const uint4 bB = *reinterpret_cast<const uint4 *>(xrows + r * xp + g * 128 + cq * 32 + 16);
+  const uint32_t bb[8] = {bA.x, bA.y, bA.z, bA.w, bB.x, bB.y, bB.z, bB.w};
   float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    const uint2 bx = *reinterpret_cast<const uint2 *>(xb + s * 8);
     const uint32_t wg0 = (s >> 1) ? g0.y : g0.x, wg1 = (s >> 1) ? g1.y : g1.x;
     const uint32_t wu0 = (s >> 1) ? u0.y : u0.x, wu1 = (s >> 1) ? u1.y : u1.x;
     uint32_t A[4], B[4];
@@ -125,12 +172,12 @@ __device__ __forceinline__ void gu_group8(const uint8_t *tile, const uint8_t *xr
       A[0] = codes_sub<2>(wg0); A[1] = codes_sub<2>(wg1); A[2] = codes_sub<3>(wg0); A[3] = codes_sub<3>(wg1);
       B[0] = codes_sub<2>(wu0); B[1] = codes_sub<2>(wu1); B[2] = codes_sub<3>(wu0); B[3] = codes_sub<3>(wu1);
     }
-    mma_f16(ag, A, bx.x, bx.y);
-    mma_f16(au, B, bx.x, bx.y);
+    mma_f16(ag, A, bb[2 * s], bb[2 * s + 1]);
+    mma_f16(au, B, bb[2 * s], bb[2 * s + 1]);
   }
-  const int nq = H / 16;
-  const float *q0 = xq + (2 * cq) * nq + 4 * g, *q1 = xq + (2 * cq + 1) * nq + 4 * g;
-  const float xs0 = ((q0[0] + q0[1]) + q0[2]) + q0[3], xs1 = ((q1[0] + q1[1]) + q1[2]) + q1[3];
+  const float4 q0 = *reinterpret_cast<const float4 *>(xq + (2 * cq) * xqp + 4 * g);
+  const float4 q1 = *reinterpret_cast<const float4 *>(xq + (2 * cq + 1) * xqp + 4 * g);
+  const float xs0 = ((q0.x + q0.y) + q0.z) + q0.w, xs1 = ((q1.x + q1.y) + q1.z) + q1.w;
   const float sg0 = bf16_bits_to_float(raw[r * G + g]) * kCodeScale, bg0 = bf16_bits_to_float(raw[16 * G + r * G + g]);
   const float sg1 = bf16_bits_to_float(raw[(r + 8) * G + g]) * kCodeScale, bg1 = bf16_bits_to_float(raw[16 * G + (r + 8) * G + g]);
   const float su0 = bf16_bits_to_float(raw[32 * G + r * G + g]) * kCodeScale, bu0 = bf16_bits_to_float(raw[48 * G + r * G + g]);
@@ -145,18 +192,19 @@ __device__ __forceinline__ void gu_group8(const uint8_t *tile, const uint8_t *xr
   tu[3] = fmaf(bu1, xs1, fmaf(su1, au[3], tu[3]));
 }
 
-// One 64-wide group of a down unit: rows m16 + r, +8 of the 64-row tile,
-// token columns 2cq, 2cq+1.
-__device__ __forceinline__ void dn_group8(const uint8_t *tile, const uint8_t *hrows, const float *hq, int I, int GI,
-                                          int qp, int row0, int g, int r, int cq, float (&t)[4]) {
-  const uint16_t *sb = reinterpret_cast<const uint16_t *>(tile + kDnRows * qp);  // scales [64][GI], biases [64][GI]
+// Down: one 64-wide group; rows row0 + r, +8 of the 128-row tile, token
+// columns 2cq, 2cq+1.
+__device__ __forceinline__ void dn_group(const uint8_t *tile, const uint8_t *hrows, const float *hq, int qp, int hp,
+                                         int hqp, int GI, int row0, int g, int r, int cq, float (&t)[4]) {
+  const uint16_t *sb = reinterpret_cast<const uint16_t *>(tile + kDnRows * qp);  // scales [128][GI], biases [128][GI]
   const uint2 w0 = *reinterpret_cast<const uint2 *>(tile + (row0 + r) * qp + g * 32 + cq * 8);
   const uint2 w1 = *reinterpret_cast<const uint2 *>(tile + (row0 + r + 8) * qp + g * 32 + cq * 8);
-  const uint8_t *hb = hrows + r * I * 2 + g * 128 + cq * 32;
+  const uint4 bA = *reinterpret_cast<const uint4 *>(hrows + r * hp + g * 128 + cq * 32);
+  const uint4 bB = *reinterpret_cast<const uint4 *>(hrows + r * hp + g * 128 + cq * 32 + 16);
+  const uint32_t bb[8] = {bA.x, bA.y, bA.z, bA.w, bB.x, bB.y, bB.z, bB.w};
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int st = 0; st < 4; ++st) {
-    const uint2 bx = *reinterpret_cast<const uint2 *>(hb + st * 8);
     const uint32_t x0 = (st >> 1) ? w0.y : w0.x, x1 = (st >> 1) ? w1.y : w1.x;
     uint32_t A[4];
     if ((st & 1) == 0) {
@@ -164,11 +212,11 @@ __device__ __forceinline__ void dn_group8(const uint8_t *tile, const uint8_t *hr
     } else {
       A[0] = codes_sub<2>(x0); A[1] = codes_sub<2>(x1); A[2] = codes_sub<3>(x0); A[3] = codes_sub<3>(x1);
     }
-    mma_f16(acc, A, bx.x, bx.y);
+    mma_f16(acc, A, bb[2 * st], bb[2 * st + 1]);
   }
-  const int nq = I / 16;
-  const float *q0 = hq + (2 * cq) * nq + 4 * g, *q1 = hq + (2 * cq + 1) * nq + 4 * g;
-  const float hs0 = ((q0[0] + q0[1]) + q0[2]) + q0[3], hs1 = ((q1[0] + q1[1]) + q1[2]) + q1[3];
+  const float4 q0 = *reinterpret_cast<const float4 *>(hq + (2 * cq) * hqp + 4 * g);
+  const float4 q1 = *reinterpret_cast<const float4 *>(hq + (2 * cq + 1) * hqp + 4 * g);
+  const float hs0 = ((q0.x + q0.y) + q0.z) + q0.w, hs1 = ((q1.x + q1.y) + q1.z) + q1.w;
   const float s0 = bf16_bits_to_float(sb[(row0 + r) * GI + g]) * kCodeScale;
   const float b0 = bf16_bits_to_float(sb[kDnRows * GI + (row0 + r) * GI + g]);
   const float s1 = bf16_bits_to_float(sb[(row0 + r + 8) * GI + g]) * kCodeScale;
@@ -178,40 +226,80 @@ __device__ __forceinline__ void dn_group8(const uint8_t *tile, const uint8_t *hr
   t[2] = fmaf(b1, hs0, fmaf(s1, acc[2], t[2]));
   t[3] = fmaf(b1, hs1, fmaf(s1, acc[3], t[3]));
 }
+
+// Decoded work unit: active slot, chunk within it, tile within the chunk.
+struct Unit {
+  int sa, ch, tile, e, beg, nt;
+};
+__device__ __forceinline__ Unit decode_unit(int u, int per, const int *chunk0, int nact, const int16_t *act_e,
+                                            const int16_t *act_beg, const int16_t *act_cnt) {
+  Unit x;
+  const int chg = u / per;
+  x.tile = u - chg * per;
+  x.sa = find_slot(chunk0, nact + 1, chg);
+  x.ch = chg - chunk0[x.sa];
+  x.e = act_e[x.sa];
+  x.beg = act_beg[x.sa];
+  x.nt = min(kTC, (int)act_cnt[x.sa] - kTC * x.ch);
+  return x;
+}
 }  // namespace
 
 size_t prefill_fused_smem(const Dims &d) {
   const PL L = prefill_layout(d.H, d.I, d.E, d.k, d.T);
-  return prefill_fits(L, d.H, d.E) ? (size_t)L.total : 0;
+  return L.total <= 227 * 1024 ? (size_t)L.total : 0;
 }
 
-__global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const PrefillArgs a) {
+namespace {
+// Kernel parameters: the arguments and the shared-memory layout (computed on
+// the host, so its fields are read from the parameter bank, not registers).
+struct PrefillParams {
+  PrefillArgs a;
+  PL L;
+};
+}  // namespace
+
+__global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const PrefillParams prm) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const PrefillArgs &a = prm.a;
+  const PL &L = prm.L;
   const int H = a.d.H, I = a.d.I, E = a.d.E, k = a.d.k, T = a.d.T;
-  const PL L = prefill_layout(H, I, E, k, T);
   const int G = L.G, GI = L.GI;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nb = gridDim.x, c = blockIdx.x;
   const int npairs = T * k;
   uint8_t *ring = smem + L.ring;
+  uint8_t *xbuf = smem + L.xb;
+  float *red = reinterpret_cast<float *>(smem + L.red);
   int *chunk0 = reinterpret_cast<int *>(smem + L.grp);                  // [E+2]
   int16_t *g_perm = reinterpret_cast<int16_t *>(chunk0 + E + 2);        // [T*k]
   int16_t *g_pos = g_perm + npairs;                                     // [T*k]
   int16_t *g_act_e = g_pos + npairs;                                    // [E+1]
   int16_t *g_act_beg = g_act_e + (E + 1);                               // [E+1]
   int16_t *g_act_cnt = g_act_beg + (E + 1);                             // [E+1]
-  int *s_flag = reinterpret_cast<int *>(smem + L.misc);                 // [16]
-  __half *s_hst = reinterpret_cast<__half *>(smem + L.misc + 64);       // [kTC][16]
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.misc + 64 + kTC * 16 * 2);
-  uint64_t *empty = full + kSlots;
-  uint64_t *route = empty + kSlots;   // grouping ready
-  uint64_t *hready = route + 1;       // all h written (barrier 3 passed)
+  int *s_flag = reinterpret_cast<int *>(smem + L.misc);
+  __half *s_hst = reinterpret_cast<__half *>(smem + L.misc + kMiscHst);
+  float *s_logit = reinterpret_cast<float *>(smem + L.misc + kMiscLogit);
+  float *s_part = reinterpret_cast<float *>(smem + L.misc + kMiscPart);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.misc + kMiscBar);  // [kWSlots]
+  uint64_t *empty = full + kWSlots;                                         // [kWSlots], one arrival per warp
+  uint64_t *xfull = empty + kWSlots;
+  uint64_t *xempty = xfull + 1;
+  uint64_t *route = xempty + 1;   // grouping ready
+  uint64_t *hready = route + 1;   // all h written (barrier 2 passed)
+  float *s_wt = reinterpret_cast<float *>(smem + L.misc + kMiscWt);  // routing weights of the current down chunk
+
+  // this block's router tiles: every 16-expert tile once per own token
+  const int n_tok = c < T ? (T - 1 - c) / nb + 1 : 0;
+  const int n_ru = n_tok * L.n_mt;
 
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
+    for (int i = 0; i < kWSlots; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], kCons);
     }
+    mbar_init(xfull, 1);
+    mbar_init(xempty, 1);
     mbar_init(route, 1);
     mbar_init(hready, 1);
     fence_mbar_init();
@@ -222,105 +310,151 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
 
   // ============================================================ producer warp
   if (warp == kCons) {
-    bool ok = mbar_wait(route, 0) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
+    bool ok = true;
+    int it = 0, xk = 0;
+    // next W slot in ring order (waits for the consumers to release it)
+    auto acquire = [&]() -> uint8_t * {
+      const int slot = it % kWSlots;
+      if (it >= kWSlots) ok = mbar_wait(&empty[slot], ((it / kWSlots) - 1) & 1);
+      return ring + slot * L.wslot;
+    };
+    // router tiles: weights only, so they are fetched before the dependency wait
+    for (int i = 0; i < n_ru && ok; ++i) {
+      uint8_t *dst = acquire();
+      if (!ok) break;
+      const int m = i % L.n_mt, e0 = m * kRtRows, rows = min(kRtRows, E - e0);
+      uint64_t *bar = &full[it % kWSlots];
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows * H));
+      __syncwarp();
+      for (int j = lane; j < rows; j += 32)
+        bulk_g2s(dst + j * L.rt_qp, a.w.router_q + (size_t)(e0 + j) * H, (uint32_t)H, bar);
+      ++it;
+    }
+    if (ok) ok = mbar_wait(route, 0) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
     fused::fence_proxy_async_global();  // operand rows written by other blocks before barrier 1
-    int issued = 0;
     if (ok) {
       const int nact = s_flag[9];
       const int nchunks = chunk0[nact];
       const int n_gu = nchunks * L.nrt, n_dn = nchunks * L.nrt_dn;
-      const int my_gu = c < n_gu ? (n_gu - 1 - c) / nb + 1 : 0;
-      const int my_dn = c < n_dn ? (n_dn - 1 - c) / nb + 1 : 0;
-      bool hr = false;
-      for (int it = 0; it < my_gu + my_dn && ok; ++it) {
-        const int slot = it % kSlots;
-        if (it >= kSlots) ok = mbar_wait(&empty[slot], ((it / kSlots) - 1) & 1);
+      int cur = -1;
+      // gate/up: weight tile, then the chunk's operand rows when the chunk changes
+      const uint8_t *blob = nullptr;  // weights of the current chunk's slot
+      for (int u = c * n_gu / nb; u < (c + 1) * n_gu / nb && ok; ++u) {
+        const int chg = u / L.nrt, tile = u - chg * L.nrt;
+        Unit x;
+        if (chg != cur) {
+          x = decode_unit(u, L.nrt, chunk0, nact, g_act_e, g_act_beg, g_act_cnt);
+          blob = x.e < 0 ? a.w.shared : a.w.experts + (size_t)x.e * a.w.stride;
+        }
+        uint8_t *dst = acquire();
         if (!ok) break;
-        uint8_t *dst = ring + slot * L.slot;
-        const bool is_gu = it < my_gu;
-        const int u = c + nb * (is_gu ? it : it - my_gu);
-        const int per = is_gu ? L.nrt : L.nrt_dn;
-        const int chg = u / per, tile = u - chg * per;
-        const int sa = find_slot(chunk0, nact + 1, chg);
-        const int ch = chg - chunk0[sa];
-        const int e = g_act_e[sa], beg = g_act_beg[sa];
-        const int nt = min(kTC, (int)g_act_cnt[sa] - kTC * ch);
-        const uint8_t *blob = e < 0 ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
-        if (is_gu) {
-          const int r0 = tile * kGuRows;
-          const uint32_t tx = (uint32_t)(2 * kGuRows * (H / 2) + 4 * kGuRows * G * 2 + nt * (H * 2 + (H / 16) * 4));
-          if (lane == 0) mbar_arrive_expect_tx(&full[slot], tx);
-          __syncwarp();
+        uint64_t *bar = &full[it % kWSlots];
+        const int r0 = tile * kGuRows;
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * kGuRows * (H / 2) + 4 * kGuRows * G * 2));
+        __syncwarp();
+        {
           const int m = lane >> 4, row = lane & 15;
           bulk_g2s(dst + (m * kGuRows + row) * L.gu_qp,
                    blob + (m == 0 ? a.w.off.gate_q : a.w.off.up_q) + (size_t)(r0 + row) * (H / 2), (uint32_t)(H / 2),
-                   &full[slot]);
+                   bar);
           if (lane < 4) {
             const size_t off = lane == 0 ? a.w.off.gate_s : lane == 1 ? a.w.off.gate_b : lane == 2 ? a.w.off.up_s : a.w.off.up_b;
             bulk_g2s(dst + 2 * kGuRows * L.gu_qp + lane * kGuRows * G * 2, blob + off + (size_t)r0 * G * 2,
-                     (uint32_t)(kGuRows * G * 2), &full[slot]);
+                     (uint32_t)(kGuRows * G * 2), bar);
           }
-          if (lane < 2 * nt) {
-            const int j = lane >> 1;
-            const int tok = e < 0 ? kTC * ch + j : g_perm[beg + kTC * ch + j] / k;
-            if ((lane & 1) == 0)
-              bulk_g2s(dst + L.gu_x + j * H * 2, a.xperm + (size_t)tok * H, (uint32_t)(H * 2), &full[slot]);
-            else
-              bulk_g2s(dst + L.gu_xq + j * (H / 16) * 4, a.xq + (size_t)tok * (H / 16), (uint32_t)((H / 16) * 4),
-                       &full[slot]);
-          }
-        } else {
-          const int n0 = tile * kDnRows;
-          // weights first (they do not depend on h): bytes expected without
-          // the arrival, so the phase cannot complete before the h rows land
-          if (lane == 0) fused::mbar_expect_tx(&full[slot], (uint32_t)(kDnRows * (I / 2) + 2 * kDnRows * GI * 2));
+        }
+        ++it;
+        if (chg != cur) {
+          if (xk >= 1) ok = mbar_wait(xempty, (xk - 1) & 1);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(x.nt * (H * 2 + (H / 16) * 4)));
           __syncwarp();
-          const bool one = L.dn_qp == I / 2;
-          const int nq = one ? 1 : kDnRows;
-          for (int ci = lane; ci < nq + 2; ci += 32) {
-            if (ci < nq) {
-              const int row = one ? 0 : ci;
-              bulk_g2s(dst + row * L.dn_qp, blob + a.w.off.down_q + (size_t)(n0 + row) * (I / 2),
-                       one ? (uint32_t)(kDnRows * (I / 2)) : (uint32_t)(I / 2), &full[slot]);
-            } else {
-              const int f = ci - nq;
-              bulk_g2s(dst + kDnRows * L.dn_qp + f * kDnRows * GI * 2,
-                       blob + (f == 0 ? a.w.off.down_s : a.w.off.down_b) + (size_t)n0 * GI * 2,
-                       (uint32_t)(kDnRows * GI * 2), &full[slot]);
-            }
+          if (lane < 2 * x.nt) {
+            const int j = lane >> 1;
+            const int tok = x.e < 0 ? kTC * x.ch + j : g_perm[x.beg + kTC * x.ch + j] / k;
+            if ((lane & 1) == 0)
+              bulk_g2s(xbuf + j * L.xp, a.xperm + (size_t)tok * H, (uint32_t)(H * 2), xfull);
+            else
+              bulk_g2s(xbuf + L.x_xq + j * L.xqp * 4, a.xq + (size_t)tok * (H / 16), (uint32_t)((H / 16) * 4), xfull);
           }
-          // ... then the h rows, once every block has written them
+          ++xk;
+          cur = chg;
+        }
+      }
+      // down: weight tiles go out at once (they stream during barrier 2); the
+      // h rows of a chunk once every block has written them
+      bool hr = false;
+      cur = -1;
+      for (int u = c * n_dn / nb; u < (c + 1) * n_dn / nb && ok; ++u) {
+        const int chg = u / L.nrt_dn, tile = u - chg * L.nrt_dn;
+        Unit x;
+        if (chg != cur) {
+          x = decode_unit(u, L.nrt_dn, chunk0, nact, g_act_e, g_act_beg, g_act_cnt);
+          blob = x.e < 0 ? a.w.shared : a.w.experts + (size_t)x.e * a.w.stride;
+        }
+        uint8_t *dst = acquire();
+        if (!ok) break;
+        uint64_t *bar = &full[it % kWSlots];
+        const int n0 = tile * kDnRows, rows = min(kDnRows, H - n0);
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows * (I / 2) + 2 * rows * GI * 2));
+        __syncwarp();
+        const bool one = L.dn_qp == I / 2;
+        const int nq = one ? 1 : rows;
+        for (int ci = lane; ci < nq + 2; ci += 32) {
+          if (ci < nq) {
+            const int row = one ? 0 : ci;
+            bulk_g2s(dst + row * L.dn_qp, blob + a.w.off.down_q + (size_t)(n0 + row) * (I / 2),
+                     one ? (uint32_t)(rows * (I / 2)) : (uint32_t)(I / 2), bar);
+          } else {
+            const int f = ci - nq;
+            bulk_g2s(dst + kDnRows * L.dn_qp + f * kDnRows * GI * 2,
+                     blob + (f == 0 ? a.w.off.down_s : a.w.off.down_b) + (size_t)n0 * GI * 2,
+                     (uint32_t)(rows * GI * 2), bar);
+          }
+        }
+        ++it;
+        if (chg != cur) {
           if (!hr) {
             ok = mbar_wait(hready, 0) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
             fused::fence_proxy_async_global();
             hr = true;
           }
-          // on a failure the arrival alone ends the phase once the weights land
-          if (lane == 0) mbar_arrive_expect_tx(&full[slot], ok ? (uint32_t)(nt * (I * 2 + (I / 16) * 4)) : 0u);
+          if (ok && xk >= 1) ok = mbar_wait(xempty, (xk - 1) & 1);
+          if (!ok) break;
+          if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(x.nt * (I * 2 + (I / 16) * 4)));
           __syncwarp();
-          if (ok && lane < 2 * nt) {
+          if (lane < 2 * x.nt) {
             const int j = lane >> 1;
-            const int pos = beg + kTC * ch + j;
+            const int pos = x.beg + kTC * x.ch + j;
             if ((lane & 1) == 0)
-              bulk_g2s(dst + L.dn_h + j * I * 2, a.hperm + (size_t)pos * I, (uint32_t)(I * 2), &full[slot]);
+              bulk_g2s(xbuf + j * L.hp, a.hperm + (size_t)pos * I, (uint32_t)(I * 2), xfull);
             else
-              bulk_g2s(dst + L.dn_hq + j * (I / 16) * 4, a.hq + (size_t)pos * (I / 16), (uint32_t)((I / 16) * 4),
-                       &full[slot]);
+              bulk_g2s(xbuf + L.x_hq + j * L.hqp * 4, a.hq + (size_t)pos * (I / 16), (uint32_t)((I / 16) * 4), xfull);
           }
+          ++xk;
+          cur = chg;
         }
-        issued = it + 1;
       }
     }
     // copies in flight must land before the block's shared memory is released
     if (lane == 0) {
       if (!ok) set_error(a.err, kErrTimeout);
-      for (int it = issued - kSlots > 0 ? issued - kSlots : 0; it < issued; ++it)
-        mbar_wait(&full[it % kSlots], (it / kSlots) & 1);
+      for (int j = it - kWSlots > 0 ? it - kWSlots : 0; j < it; ++j) mbar_wait(&full[j % kWSlots], (j / kWSlots) & 1);
+      if (xk >= 1) mbar_wait(xfull, (xk - 1) & 1);
     }
     return;
   }
 
   // ============================================================ consumers
+  // the router's scales and biases (weights: read before the dependency wait)
+  uint16_t *rsb = reinterpret_cast<uint16_t *>(xbuf + L.rx_sb);  // scales [16 n_mt][G], then biases
+  const int rsb_n = kRtRows * L.n_mt * G;
+  if (n_tok > 0) {
+    for (int i = tid; i < E * G; i += kConsThreads) {
+      rsb[i] = __ldg(a.w.router_s + i);
+      rsb[rsb_n + i] = __ldg(a.w.router_b + i);
+    }
+  }
   pdl_wait();
   pdl_launch_dependents();
   if (c == 0 && tid == 0) trace_min(a.trace, kTrWaited);
@@ -340,11 +474,18 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       cons_sync();
     }
   };
+  // one arrival per consumer warp releases a W slot
+  auto release = [&](int slot) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(&empty[slot], 0);
+  };
   const uint16_t *src = a.normalize ? a.hres : a.x;
   const int nquart = H / 16;
+  const int r = lane >> 2, cq = lane & 3;
+  int it = 0, xk = 0;
 
-  // ---- A: operand rows of tokens t = c, c + nb, ...
-  for (int t = c; t < T; t += nb) {
+  // ---- R: operand rows, router scores and top-k of tokens t = c, c + nb, ...
+  for (int t = c; t < T && !aborted; t += nb) {
     uint32_t qin[8];
     float qss = 0.f;
     if (tid < nquart) {
@@ -360,7 +501,6 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       }
     }
     if (a.normalize) {
-      float *s_part = reinterpret_cast<float *>(ring);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) qss += __shfl_xor_sync(0xffffffffu, qss, off);
       if (lane == 0) s_part[warp] = qss;
@@ -376,7 +516,6 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
           qin[i] = (uint32_t)lb | ((uint32_t)hb << 16);
         }
       }
-      cons_sync();
     }
     if (tid < nquart) {
       if (a.xn_user) {
@@ -396,108 +535,67 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         s += __uint_as_float(qin[i] & 0xFFFF0000u);
       }
       a.xq[(size_t)t * nquart + tid] = s;
+      // router operand: fp16 pairs (x0,x2)(x1,x3)(x4,x6)(x5,x7)... of this quarter
+      uint32_t h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = bf16x2_to_f16x2(qin[i]);
+      uint32_t rp[8];
+#pragma unroll
+      for (int s2 = 0; s2 < 4; ++s2) {
+        rp[2 * s2] = __byte_perm(h[2 * s2], h[2 * s2 + 1], 0x5410);      // x[4s], x[4s+2]
+        rp[2 * s2 + 1] = __byte_perm(h[2 * s2], h[2 * s2 + 1], 0x7632);  // x[4s+1], x[4s+3]
+      }
+      uint4 *rx = reinterpret_cast<uint4 *>(xbuf + tid * 32);
+      rx[0] = make_uint4(rp[0], rp[1], rp[2], rp[3]);
+      rx[1] = make_uint4(rp[4], rp[5], rp[6], rp[7]);
+      reinterpret_cast<float *>(xbuf + L.rx_q)[tid] = s;
     }
-  }
-
-  // ---- B: router tasks (8 experts x 8 tokens), logits[t][e]
-  {
-    const int n_eb = (E + 7) / 8, n_tb = (T + 7) / 8;
-    float *xs = reinterpret_cast<float *>(ring);  // [8][H] fp32
-    for (int task = c; task < n_eb * n_tb; task += nb) {
-      const int eb = task % n_eb, tb = task / n_eb;
-      const int t0 = tb * 8, tn = min(8, T - t0);
-      const int e = eb * 8 + (warp & 7);
-      const int half = warp >> 3;  // tokens t0 + 4*half .. +3
-      cons_sync();                 // xs free (previous task, phase A's s_part)
-      // stage the 8 rows (normalised like phase A) as fp32
-      for (int n = 0; n < tn; ++n) {
-        uint32_t qin[8];
-        float qss = 0.f;
-        if (tid < nquart) {
-          const uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(src + (size_t)(t0 + n) * H) + 2 * tid);
-          const uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(src + (size_t)(t0 + n) * H) + 2 * tid + 1);
-          qin[0] = v0.x; qin[1] = v0.y; qin[2] = v0.z; qin[3] = v0.w;
-          qin[4] = v1.x; qin[5] = v1.y; qin[6] = v1.z; qin[7] = v1.w;
+    cons_sync();  // rx complete
+    float rt0[8], rt1[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float lo = __uint_as_float(qin[i] << 16), hi = __uint_as_float(qin[i] & 0xFFFF0000u);
-            qss = fmaf(lo, lo, qss);
-            qss = fmaf(hi, hi, qss);
-          }
+    for (int m = 0; m < 8; ++m) {
+      rt0[m] = 0.f;
+      rt1[m] = 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (m < L.n_mt && !aborted) {
+        const int slot = it % kWSlots;
+        if (!mbar_wait(&full[slot], (it / kWSlots) & 1)) {
+          aborted = true;
+          set_error(a.err, kErrTimeout);
+        } else {
+          const uint8_t *tile = ring + slot * L.wslot;
+          const uint16_t *rs = rsb + m * kRtRows * G, *rb = rsb + rsb_n + m * kRtRows * G;
+          for (int g = warp; g < G; g += kCons)
+            rt_group(tile, xbuf, reinterpret_cast<const float *>(xbuf + L.rx_q), rs, rb, L.rt_qp, G, g, r, cq, rt0[m],
+                     rt1[m]);
+          release(slot);
+          ++it;
         }
-        float inv = 1.0f;
-        if (a.normalize) {
-          float *s_part = reinterpret_cast<float *>(smem + L.misc + 512);
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) qss += __shfl_xor_sync(0xffffffffu, qss, off);
-          if (lane == 0) s_part[warp] = qss;
-          cons_sync();
-          float tot = 0.f;
-          for (int w = 0; w < kCons; ++w) tot += s_part[w];
-          inv = 1.0f / sqrtf(tot / (float)H + 1e-6f);
-          cons_sync();
-        }
-        if (tid < nquart) {
-          float4 *dst = reinterpret_cast<float4 *>(xs + n * H + 16 * tid);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float f[4];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              float lo = __uint_as_float(qin[2 * i + j] << 16), hi = __uint_as_float(qin[2 * i + j] & 0xFFFF0000u);
-              if (a.normalize) {
-                lo = bf16_bits_to_float(float_to_bf16_bits(lo * inv));
-                hi = bf16_bits_to_float(float_to_bf16_bits(hi * inv));
-              }
-              f[2 * j] = lo;
-              f[2 * j + 1] = hi;
-            }
-            dst[i] = make_float4(f[0], f[1], f[2], f[3]);
-          }
-        }
-      }
-      cons_sync();
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (e < E) {
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.w.router_q + (size_t)e * H);
-        const uint16_t *srow = a.w.router_s + (size_t)e * G, *brow = a.w.router_b + (size_t)e * G;
-        for (int cw = lane; cw < H / 4; cw += 32) {
-          const uint32_t wd = __ldg(qrow + cw);
-          const float s = bf16_bits_to_float(__ldg(srow + (cw >> 4))), b = bf16_bits_to_float(__ldg(brow + (cw >> 4)));
-          float w4[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            w4[i] = fmaf(__uint_as_float(0x4B000000u | ((wd >> (8 * i)) & 0xFFu)) - 8388608.0f, s, b);
-#pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            const int tt = 4 * half + n;
-            if (tt < tn) {
-              const float4 xv = *reinterpret_cast<const float4 *>(xs + tt * H + 4 * cw);
-              acc[n] = fmaf(w4[3], xv.w, fmaf(w4[2], xv.z, fmaf(w4[1], xv.y, fmaf(w4[0], xv.x, acc[n]))));
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc[n] += __shfl_xor_sync(0xffffffffu, acc[n], off);
-      if (e < E && lane == 0) {
-        const float bias = a.w.logit_bias ? a.w.logit_bias[e] : 0.f;
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-          if (4 * half + n < tn) a.logits[(size_t)(t0 + 4 * half + n) * E + e] = acc[n] + bias;
       }
     }
-  }
-
-  fused::fence_proxy_async_global();  // operand rows are read back by bulk copies
-  barrier();  // 1: logits, operand rows, quarter sums
-  // ---- top-k of tokens t = c, c + nb, ...
-  if (!aborted && warp == 0) {
-    for (int t = c; t < T; t += nb) {
+    if (cq == 0) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        if (m < L.n_mt) {
+          red[warp * 128 + m * 16 + r] = rt0[m];
+          red[warp * 128 + m * 16 + r + 8] = rt1[m];
+        }
+    }
+    cons_sync();
+    if (tid < E) {
+      float v = a.w.logit_bias ? a.w.logit_bias[tid] : 0.f;
+      float sum = 0.f;
+      for (int w = 0; w < kCons; ++w) sum += red[w * 128 + tid];
+      v += sum;
+      s_logit[tid] = v;
+      a.logits[(size_t)t * E + tid] = v;
+    }
+    cons_sync();
+    if (warp == 0) {
       bool bad = false;
-      fused::warp_topk(a.logits + (size_t)t * E, E, k, a.r.ids + t * k, a.r.wts + t * k, &bad);
+      fused::warp_topk(s_logit, E, k, a.r.ids + t * k, a.r.wts + t * k, &bad);
       if (bad && lane == 0) set_error(a.err, kErrNonFinite);
       __syncwarp();
       if (lane < k) {
@@ -505,19 +603,22 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         if (a.wts_user) a.wts_user[t * k + lane] = a.r.wts[t * k + lane];
       }
     }
+    cons_sync();  // rx, red and s_logit are reused by the next token
   }
-  barrier();  // 2: ids, weights
+
+  fused::fence_proxy_async_global();  // operand rows are read back by bulk copies
+  barrier();  // 1: operand rows, quarter sums, routing
 
   // ---- every block groups all pairs (stable counting sort by expert id)
   if (!aborted) {
-    int *cnt = reinterpret_cast<int *>(ring);  // [E]
-    int *wc = cnt + E;                         // [kCons][E]
+    int *cnt = reinterpret_cast<int *>(red);  // [E]
+    int *wc = cnt + E;                        // [kCons][E]
     for (int i = tid; i < (1 + kCons) * E; i += kConsThreads) cnt[i] = 0;
     cons_sync();
     for (int p = tid; p < npairs; p += kConsThreads) atomicAdd(&cnt[__ldcg(a.r.ids + p)], 1);
     cons_sync();
     if (warp == 0) {
-      // exclusive scan of counts -> offsets; active slots (shared first); chunk prefix
+      // exclusive scan of counts -> fill positions; active slots (shared first); chunk prefix
       int run = 0, nact = 1, chunks = (T + kTC - 1) / kTC;
       if (lane == 0) {
         g_act_e[0] = -1;
@@ -550,7 +651,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
           chunk0[sa] = chunks + incl_ch - nch;
         }
         if (e < E) cnt[e] = run + incl - ce;  // from here on: next free position of expert e
-        run +=__shfl_sync(0xffffffffu, incl, 31);
+        run += __shfl_sync(0xffffffffu, incl, 31);
         chunks += __shfl_sync(0xffffffffu, incl_ch, 31);
         nact += __popc(act);
       }
@@ -593,136 +694,161 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   }
   if (c == 0 && tid == 0) trace_max(a.trace, kTrLoaded);
 
-  // ---- C: gate/up units
-  const int nact = s_flag[9];
+  const int nact = aborted ? 0 : s_flag[9];
   const int nchunks = aborted ? 0 : chunk0[nact];
-  const int n_gu = nchunks * L.nrt, n_dn = nchunks * L.nrt_dn;
-  const int my_gu = c < n_gu ? (n_gu - 1 - c) / nb + 1 : 0;
-  const int my_dn = c < n_dn ? (n_dn - 1 - c) / nb + 1 : 0;
-  const int r = lane >> 2, cq = lane & 3;
-  int it = 0;
-  for (; it < my_gu && !aborted; ++it) {
-    const int slot = it % kSlots;
-    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) {
-      aborted = true;
-      set_error(a.err, kErrTimeout);
-      break;
-    }
-    const uint8_t *tile = ring + slot * L.slot;
-    const int u = c + nb * it;
-    const int chg = u / L.nrt, rt = u - chg * L.nrt;
-    const int sa = find_slot(chunk0, nact + 1, chg);
-    const int ch = chg - chunk0[sa];
-    const int beg = g_act_beg[sa];
-    const int nt = min(kTC, (int)g_act_cnt[sa] - kTC * ch);
-    float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
-    float tg2[4] = {0.f, 0.f, 0.f, 0.f}, tu2[4] = {0.f, 0.f, 0.f, 0.f};
-    int g = warp;
-    for (; g + kCons < G; g += 2 * kCons) {
-      gu_group8(tile, tile + L.gu_x, reinterpret_cast<const float *>(tile + L.gu_xq), H, G, L.gu_qp, g, r, cq, tg, tu);
-      gu_group8(tile, tile + L.gu_x, reinterpret_cast<const float *>(tile + L.gu_xq), H, G, L.gu_qp, g + kCons, r, cq,
-                tg2, tu2);
-    }
-    if (g < G)
-      gu_group8(tile, tile + L.gu_x, reinterpret_cast<const float *>(tile + L.gu_xq), H, G, L.gu_qp, g, r, cq, tg, tu);
-    cons_sync();  // the slot's operand rows become the reduction buffer
-    float *red = reinterpret_cast<float *>(const_cast<uint8_t *>(tile) + L.gu_x);
-    float4 *rw = reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 8);
-    rw[0] = make_float4(tg[0] + tg2[0], tg[1] + tg2[1], tg[2] + tg2[2], tg[3] + tg2[3]);
-    rw[1] = make_float4(tu[0] + tu2[0], tu[1] + tu2[1], tu[2] + tu2[2], tu[3] + tu2[3]);
-    cons_sync();
-    if (tid < kGuRows * kTC) {
-      const int row = tid & 15, n = tid >> 4;
-      const int ln = (row & 7) * 4 + (n >> 1), idx = ((row >> 3) << 1) + (n & 1);
-      float gs = 0.f, us = 0.f;
-#pragma unroll
-      for (int w = 0; w < kCons; ++w) {
-        gs += red[(w * 32 + ln) * 8 + idx];
-        us += red[(w * 32 + ln) * 8 + 4 + idx];
+
+  // ---- G: gate/up units [c * n_gu / nb, (c + 1) * n_gu / nb)
+  {
+    const int n_gu = nchunks * L.nrt;
+    int cur = -1, p0 = 0, nt = 0;  // current chunk: first sorted position, tokens
+    for (int u = c * n_gu / nb; u < (c + 1) * n_gu / nb && !aborted; ++u) {
+      const int chg = u / L.nrt, tile = u - chg * L.nrt;
+      if (chg != cur) {
+        const Unit x = decode_unit(u, L.nrt, chunk0, nact, g_act_e, g_act_beg, g_act_cnt);
+        p0 = x.beg + kTC * x.ch;
+        nt = x.nt;
+        if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
+        if (!mbar_wait(xfull, xk & 1)) {
+          aborted = true;
+          set_error(a.err, kErrTimeout);
+          break;
+        }
+        ++xk;
+        cur = chg;
       }
-      const float hv = fused::gelu_tanh(gs) * us;
-      if (n < nt && !(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
-      s_hst[n * 16 + row] = __float2half_rn(hv);
-    }
-    cons_sync();
-    if (tid < nt) {  // one thread per token writes its 16-row quarter of h
-      const int pos = beg + kTC * ch + tid;
-      const uint4 *hv = reinterpret_cast<const uint4 *>(s_hst + tid * 16);
-      const uint4 v0 = hv[0], v1 = hv[1];
-      const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      uint32_t out[8];
-      operand_quarter<false>(in, out);
-      uint4 *dst = reinterpret_cast<uint4 *>(a.hperm + (size_t)pos * I + rt * kGuRows);
-      dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-      dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
-      float s = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        s += __half2float(__ushort_as_half((unsigned short)(in[w] & 0xFFFFu)));
-        s += __half2float(__ushort_as_half((unsigned short)(in[w] >> 16)));
+      const int slot = it % kWSlots;
+      if (!mbar_wait(&full[slot], (it / kWSlots) & 1)) {
+        aborted = true;
+        set_error(a.err, kErrTimeout);
+        break;
       }
-      a.hq[(size_t)pos * (I / 16) + rt] = s;
+      const uint8_t *wt = ring + slot * L.wslot;
+      const float *xq = reinterpret_cast<const float *>(xbuf + L.x_xq);
+      float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
+      float tg2[4] = {0.f, 0.f, 0.f, 0.f}, tu2[4] = {0.f, 0.f, 0.f, 0.f};
+      int g = warp;
+      for (; g + kCons < G; g += 2 * kCons) {
+        gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
+        gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g + kCons, r, cq, tg2, tu2);
+      }
+      if (g < G) gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
+      release(slot);
+      ++it;
+      // cross-warp reduction, transposed so both sides are conflict-free: red[w][i][lane]
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        red[warp * 256 + i * 32 + lane] = tg[i] + tg2[i];
+        red[warp * 256 + (i + 4) * 32 + lane] = tu[i] + tu2[i];
+      }
+      cons_sync();
+      if (tid < kGuRows * kTC) {
+        const int idx = tid >> 5, ln = tid & 31;
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) {
+          gs += red[w * 256 + idx * 32 + ln];
+          us += red[w * 256 + (idx + 4) * 32 + ln];
+        }
+        const int row = (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);
+        const float hv = fused::gelu_tanh(gs) * us;
+        if (n < nt && !(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
+        s_hst[n * 16 + row] = __float2half_rn(hv);
+      }
+      cons_sync();
+      if (tid < nt) {  // one thread per token writes its 16-row quarter of h
+        const int pos = p0 + tid;
+        const uint4 *hv = reinterpret_cast<const uint4 *>(s_hst + tid * 16);
+        const uint4 v0 = hv[0], v1 = hv[1];
+        const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t out[8];
+        operand_quarter<false>(in, out);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.hperm + (size_t)pos * I + tile * kGuRows);
+        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          s += __half2float(__ushort_as_half((unsigned short)(in[w] & 0xFFFFu)));
+          s += __half2float(__ushort_as_half((unsigned short)(in[w] >> 16)));
+        }
+        a.hq[(size_t)pos * (I / 16) + tile] = s;
+      }
+      // red is rewritten after the next unit's compute and s_hst after its
+      // first consumer barrier, which every thread reaches after this point
     }
-    cons_sync();
-    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);
+    if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
   }
 
   fused::fence_proxy_async_global();  // h rows are read back by bulk copies
-  barrier();  // 3: all of h
+  barrier();  // 2: all of h
   if (tid == 0) {
     if (aborted) s_flag[8] = 1;
     mbar_arrive_expect_tx(hready, 0);
   }
 
-  // ---- D: down units -> weighted outputs per sorted position
-  for (int jd = 0; jd < my_dn && !aborted; ++jd, ++it) {
-    const int slot = it % kSlots;
-    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) {
-      aborted = true;
-      set_error(a.err, kErrTimeout);
-      break;
-    }
-    const uint8_t *tile = ring + slot * L.slot;
-    const int u = c + nb * jd;
-    const int chg = u / L.nrt_dn, nt64 = u - chg * L.nrt_dn;
-    const int sa = find_slot(chunk0, nact + 1, chg);
-    const int ch = chg - chunk0[sa];
-    const int beg = g_act_beg[sa];
-    const int nt = min(kTC, (int)g_act_cnt[sa] - kTC * ch);
-    const int m = warp & 3, kq = warp >> 2;  // 16-row tile, K quarter
-    float t4[4] = {0.f, 0.f, 0.f, 0.f}, t4b[4] = {0.f, 0.f, 0.f, 0.f};
-    int g = kq;
-    for (; g + 4 < GI; g += 8) {
-      dn_group8(tile, tile + L.dn_h, reinterpret_cast<const float *>(tile + L.dn_hq), I, GI, L.dn_qp, 16 * m, g, r, cq, t4);
-      dn_group8(tile, tile + L.dn_h, reinterpret_cast<const float *>(tile + L.dn_hq), I, GI, L.dn_qp, 16 * m, g + 4, r,
-                cq, t4b);
-    }
-    if (g < GI)
-      dn_group8(tile, tile + L.dn_h, reinterpret_cast<const float *>(tile + L.dn_hq), I, GI, L.dn_qp, 16 * m, g, r, cq, t4);
-    cons_sync();  // the slot's h rows become the reduction buffer
-    float *red = reinterpret_cast<float *>(const_cast<uint8_t *>(tile) + L.dn_h);
-    *reinterpret_cast<float4 *>(red + (warp * 32 + lane) * 4) =
-        make_float4(t4[0] + t4b[0], t4[1] + t4b[1], t4[2] + t4b[2], t4[3] + t4b[3]);
-    cons_sync();
-    for (int o = tid; o < kDnRows * kTC; o += kConsThreads) {
-      const int row = o & 63, n = o >> 6;
-      if (n < nt) {
-        const int mm = row >> 4, rr = row & 15;
-        const int ln = (rr & 7) * 4 + (n >> 1), idx = ((rr >> 3) << 1) + (n & 1);
-        float v = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v += red[(((q << 2) | mm) * 32 + ln) * 4 + idx];
-        const int pos = beg + kTC * ch + n;
-        const float wt = pos >= npairs ? 1.0f : __ldcg(a.r.wts + g_perm[pos]);
-        a.obuf[(size_t)pos * H + nt64 * kDnRows + row] = wt * v;
+  // ---- D: down units [c * n_dn / nb, (c + 1) * n_dn / nb) -> weighted outputs
+  {
+    const int n_dn = nchunks * L.nrt_dn;
+    const int mt = warp & 7, kh = warp >> 3;  // 16-row tile, K half
+    int cur = -1, p0 = 0, nt = 0;
+    for (int u = c * n_dn / nb; u < (c + 1) * n_dn / nb && !aborted; ++u) {
+      const int chg = u / L.nrt_dn, tile = u - chg * L.nrt_dn;
+      if (chg != cur) {
+        const Unit x = decode_unit(u, L.nrt_dn, chunk0, nact, g_act_e, g_act_beg, g_act_cnt);
+        p0 = x.beg + kTC * x.ch;
+        nt = x.nt;
+        // the chunk's routing weights, read once (the previous unit's readers
+        // are past its last consumer barrier)
+        if (tid < nt) {
+          const int pos = p0 + tid;
+          s_wt[tid] = pos >= npairs ? 1.0f : __ldcg(a.r.wts + g_perm[pos]);
+        }
+        if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
+        if (!mbar_wait(xfull, xk & 1)) {
+          aborted = true;
+          set_error(a.err, kErrTimeout);
+          break;
+        }
+        ++xk;
+        cur = chg;
       }
+      const int slot = it % kWSlots;
+      if (!mbar_wait(&full[slot], (it / kWSlots) & 1)) {
+        aborted = true;
+        set_error(a.err, kErrTimeout);
+        break;
+      }
+      const uint8_t *wt = ring + slot * L.wslot;
+      const float *hq = reinterpret_cast<const float *>(xbuf + L.x_hq);
+      float t4[4] = {0.f, 0.f, 0.f, 0.f}, t4b[4] = {0.f, 0.f, 0.f, 0.f};
+      int g = kh;
+      for (; g + 2 < GI; g += 4) {
+        dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * mt, g, r, cq, t4);
+        dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * mt, g + 2, r, cq, t4b);
+      }
+      if (g < GI) dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * mt, g, r, cq, t4);
+      release(slot);
+      ++it;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) red[warp * 128 + i * 32 + lane] = t4[i] + t4b[i];
+      cons_sync();
+      const int n0 = tile * kDnRows, rows = min(kDnRows, H - n0);
+      for (int o = tid; o < kDnRows * kTC; o += kConsThreads) {
+        const int m = o >> 7, idx = (o >> 5) & 3, ln = o & 31;
+        const int row = 16 * m + (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);
+        if (n < nt && row < rows) {
+          const float v = red[m * 128 + idx * 32 + ln] + red[(m + 8) * 128 + idx * 32 + ln];
+          const int pos = p0 + n;
+          a.obuf[(size_t)pos * H + n0 + row] = s_wt[n] * v;
+        }
+      }
+      cons_sync();  // red is rewritten by the next unit
     }
-    cons_sync();
-    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);
+    if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
   }
 
-  barrier();  // 4: all weighted outputs
-  // ---- E: combine tokens t = c, c + nb, ...
+  barrier();  // 3: all weighted outputs
+  // ---- C: combine tokens t = c, c + nb, ...
   if (!aborted) {
     for (int t = c; t < T; t += nb) {
       int pos[kMaxTopK];
@@ -764,7 +890,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
 }
 
 cudaError_t launch_prefill_fused(const PrefillArgs &a, int n_blocks, cudaStream_t st, bool pdl) {
-  return launch_k(prefill_layer_kernel, dim3(n_blocks), dim3(fused::kThreads), prefill_fused_smem(a.d), st, pdl, a);
+  const PrefillParams prm{a, prefill_layout(a.d.H, a.d.I, a.d.E, a.d.k, a.d.T)};
+  return launch_k(prefill_layer_kernel, dim3(n_blocks), dim3(fused::kThreads), prefill_fused_smem(a.d), st, pdl, prm);
 }
 
 cudaError_t prefill_set_attributes() {

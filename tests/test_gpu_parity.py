@@ -241,12 +241,18 @@ def test_fused_and_chained_paths_agree(layer0, layer0_zipf, residual, n_tokens):
         ids = torch.empty((n_tokens, K), dtype=torch.int32, device="cuda")
         logits = torch.empty((n_tokens, E), dtype=torch.float32, device="cuda")
         ws = workspace(m, w, n_tokens)
+        trace = torch.zeros(4 * 4, dtype=torch.int64, device="cuda")
+        m.set_trace(trace, 4)
         if residual:
             m.layer_forward_residual(h, n_tokens, w, ws, y_out=y, x_out=xo, ids_out=ids, logits_out=logits)
         else:
             m.layer_forward(h, n_tokens, w, y, ws, ids_out=ids, logits_out=logits)
         torch.cuda.synchronize()
+        m.set_trace(None, 0)
         assert m.get_error() == bq.MOE_OK
+        # which path ran: the fused kernel traces one launch, the chain one per launch
+        launches = int((trace.view(4, 4) != 0).any(dim=1).sum())
+        assert launches == (1 if fused == "1" else (3 if n_tokens == 1 else 4)), f"fused={fused}: {launches} launches"
         x_used = from_dev_bf16(xo) if residual else x_bits
         out = {"ids": ids.cpu().numpy(), "logits": logits.cpu().numpy(), "y": from_dev_bf16(y), "x": x_used,
                "h": from_dev_bf16(h)}
