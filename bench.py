@@ -4,10 +4,10 @@
 Default workload (one "step" = one decode token through the whole hot path):
 a 30-layer stack of independent MoE layers (hidden 2816, inter 704, 128
 experts, top-8, 4-bit experts, 8-bit router, group 64; layer l generated with
-seed l, all 30 x 128 experts resident in HBM), each step one fresh N(0,1)
-hidden state, x_l = rmsnorm_no_scale(h_l), h_{l+1} = h_l + MoE_l(x_l).  The
-30 layer calls of a step are captured in one CUDA graph; the kernels chain
-with programmatic dependent launch.
+seed l, all 30 x 128 experts resident in HBM), 256 steps, each step one fresh
+N(0,1) hidden state, x_l = rmsnorm_no_scale(h_l), h_{l+1} = h_l + MoE_l(x_l).
+The 30 layer calls of a step are captured in one CUDA graph; each call is one
+launch of the fused layer kernel, chained with programmatic dependent launch.
 
 Prints one JSON line (see the keys below).  `--impl reference` times the
 float64 CPU oracle instead, on a bounded sample of the same workload.
@@ -38,6 +38,13 @@ ROUTER_BYTES = E * H + 2 * E * (H // 64) * 2                                   #
 EXPERT_BYTES = 3 * (I * H // 2 + 2 * I * (H // 64) * 2)                          # 3,345,408
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "bit_affine_quantized_gb300", "csrc")
+# per-launch DRAM traffic of the fused kernels, from committed ncu summaries:
+# (summary file, sources that define the kernel)
+TRAFFIC = {
+    1: ("decode_layer_kernel_T1.md", ("decode.cu", "common.cuh", "kernels.h")),
+    128: ("prefill_layer_kernel_T128.md", ("prefill.cu", "fused.cuh", "common.cuh", "kernels.h")),
+}
 
 
 def layer_bytes(n_tokens: int, distinct_routed: int) -> int:
@@ -61,6 +68,37 @@ WORKLOADS = {
 
 
 # ---------------------------------------------------------------- helpers
+def sources_sha256(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def traffic_per_launch(T: int):
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)
+    from the committed summary for this token count, or None when there is
+    none or the kernel's sources changed since it was taken."""
+    if T not in TRAFFIC:
+        return None, "no capture for this token count"
+    name, files = TRAFFIC[T]
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if "=" in line and line.strip().startswith("- "):
+                    k, v = line.strip()[2:].split("=", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("kernel_sources_sha256") != sources_sha256(files):
+            return None, f"profiles/{name}: kernel changed since the capture"
+        return int(fields["traffic_bytes_per_launch"]), f"profiles/{name}"
+    except Exception as exc:
+        return None, f"profiles/{name}: {type(exc).__name__}"
+
+
 def peaks():
     try:
         with open(MEASURED_PEAKS) as f:
@@ -203,9 +241,27 @@ def run_ours(args, spec, rank, world, device):
 
     out_src = h if spec["residual"] else y
 
+    # launches per layer call, read from the trace slots the kernels stamp
+    trace = torch.zeros(4 * 8, dtype=torch.int64, device=device)
+    moe.set_trace(trace, 8)
+    with torch.cuda.stream(stream):
+        if spec["residual"]:
+            moe.layer_forward_residual(h, T, weights[0], ws, stream=stream)
+        else:
+            moe.layer_forward(h, T, weights[0], y, ws, stream=stream)
+    torch.cuda.synchronize(device)
+    moe.set_trace(None, 0)
+    launches_per_call = int((trace.view(8, 4) != 0).any(dim=1).sum())
+    calls_per_step = spec["layers"] if spec["residual"] else 1
+
+    # the kernels' own time: events around each graph replay, on its stream
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps_total)]
+
     def one_step(s):
         h.copy_(inputs[s], non_blocking=True)
+        kev[s][0].record(stream)
         graphs[s % len(graphs)].replay()
+        kev[s][1].record(stream)
         outputs[s].copy_(out_src, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -226,6 +282,7 @@ def run_ours(args, spec, rank, world, device):
         ev1.record(stream)
     torch.cuda.synchronize(device)
     elapsed_ms = ev0.elapsed_time(ev1)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in kev[args.warmup:steps_total])
     clocks = sampler.stop()
     barrier(world)
     st = moe.get_error()
@@ -246,14 +303,20 @@ def run_ours(args, spec, rank, world, device):
         n_calls = 1
         distinct = [len(np.unique(ids_np[(steps_total - 1) % len(graphs)]))]
     bytes_per_step = sum(layer_bytes(T, d) for d in distinct)
+    bytes_per_call = bytes_per_step / n_calls
     hbm, peak_kind = peaks()
-    achieved = bytes_per_step / (ms_per_step / 1e3) / 1e9
+    # one layer call is one launch of the fused kernel (the dominant and only
+    # kernel of the step); its average duration over the timed region
+    call_us = max_over_ranks(kernel_ms, world, device) * 1e3 / (args.steps * calls_per_step)
+    achieved = bytes_per_call / (call_us / 1e6) / 1e9
+    fused = launches_per_call == 1
+    traffic, traffic_src = traffic_per_launch(T) if fused else (None, "chained launches")
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's input, the layer calls, D2H of the result, every step
     pin_in = torch.from_numpy(host_in.view(np.int16)).pin_memory()
     pin_out = torch.empty_like(pin_in).pin_memory()
-    e2e_steps = min(args.steps, 64)
+    e2e_steps = args.steps
     torch.cuda.synchronize(device)
     barrier(world)
     t0 = time.perf_counter()
@@ -266,7 +329,8 @@ def run_ours(args, spec, rank, world, device):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
     e2e_value = world * units_per_step * e2e_steps / e2e_s
 
-    launches_per_call = 3 if T == 1 else 4
+    kernel_name = ("decode_layer_kernel" if T == 1 else "prefill_layer_kernel") if fused else \
+        "router + gate/up + down launches (MOE_*_FUSED=0)"
     line = {
         "metric": args.metric, "value": round(value, 3), "unit": args.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -277,13 +341,14 @@ def run_ours(args, spec, rank, world, device):
                        bytes_per_step / 1e6, "" if spec["residual"] else "; 8 layer copies rotated"),
                    "cuda_graph": True, "pdl": os.environ.get("MOE_PDL", "1") != "0",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "one MoE layer call (router + gate/up + down launches, PDL-chained)",
+        "roofline": {"bound": "hbm", "kernel": kernel_name,
                      "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
-                     "algorithmic_bytes_per_step": bytes_per_step},
+                     "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": traffic_src,
+                     "algorithmic_bytes_per_launch": round(bytes_per_call), "launch_us": round(call_us, 3),
+                     "launches_timed": args.steps * calls_per_step},
         "e2e": {"value": round(e2e_value, 3), "unit": args.unit, "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
-        "gpu_launches": launches_per_call * n_calls * args.steps,
+        "gpu_launches": launches_per_call * calls_per_step * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -396,7 +461,7 @@ def run_reference(args, spec, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode30")
