@@ -109,6 +109,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
   }
   return false;
 }
+// The same for a warp that waits while other warps of its block compute (a
+// producer): between polls it sleeps, so its polling does not take issue
+// slots from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t *bar, uint32_t parity, unsigned sleep_ns = 64,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 7u) == 7u && global_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
 
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.

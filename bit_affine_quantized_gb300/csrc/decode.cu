@@ -94,10 +94,13 @@ __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long l
 // so arrivals pipeline at L2 instead of serialising) and polls until the
 // counter reaches `target`.  The counter only grows; a launch's targets are
 // derived from its value at launch start (see the caller).  Bounded.
-__device__ bool grid_sync(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag) {
+// grid_arrive + grid_wait split the barrier so a block can work in between.
+__device__ __forceinline__ void grid_arrive(unsigned long long *count) {
   cons_sync();  // the block's writes happen-before thread 0's release below
+  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
+}
+__device__ bool grid_wait(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag) {
   if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
     bool ok = true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 0;; ++it) {
@@ -112,6 +115,10 @@ __device__ bool grid_sync(unsigned long long *count, unsigned long long target, 
   }
   cons_sync();
   return *s_flag != 0;
+}
+__device__ bool grid_sync(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag) {
+  grid_arrive(count);
+  return grid_wait(count, target, err, s_flag);
 }
 
 // Orderable 32-bit key of a float (larger float -> larger key).
@@ -223,8 +230,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   uint64_t *empty = full + kSlots;                                     // [3]
   uint64_t *route = empty + kSlots;                                    // [1]
 
-  // this block's unit lists: gate/up u = c + nb*i; down d = (nb-1-c) + nb*i
-  const int n_gu_mine = c < L.n_gu ? (L.n_gu - 1 - c) / nb + 1 : 0;
+  // This block's unit lists.  Shared gate/up units s = c + nb*i (computed
+  // while the routing completes); routed gate/up units r = p + nb*i with
+  // p = (c - nrt) mod nb, so the round-robin starts after the blocks that own
+  // a shared unit and those get the fewer routed ones; down d = (nb-1-c) + nb*i.
+  const int n_sh_mine = c < L.nrt ? (L.nrt - 1 - c) / nb + 1 : 0;
+  const int n_rt_all = k * L.nrt;
+  const int p_rt = ((c - L.nrt) % nb + nb) % nb;
+  const int n_rt_mine = p_rt < n_rt_all ? (n_rt_all - 1 - p_rt) / nb + 1 : 0;
+  const int n_gu_mine = n_sh_mine + n_rt_mine;
   const int c_dn = nb - 1 - c;
   const int n_dn_mine = c_dn < L.n_dn ? (L.n_dn - 1 - c_dn) / nb + 1 : 0;
   const int n_units = n_gu_mine + n_dn_mine;
@@ -247,19 +261,31 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     int issued = 0;
     for (int it = 0; it < n_units && ok; ++it) {
       const int slot = it % kSlots;
-      if (it >= kSlots) ok = mbar_wait(&empty[slot], ((it / kSlots) - 1) & 1);
+      if (it >= kSlots) ok = mbar_wait_idle(&empty[slot], ((it / kSlots) - 1) & 1);
       if (!ok) break;
       uint8_t *dst = ring + slot * L.slot_bytes;
       const bool is_gu = it < n_gu_mine;
-      const int u = is_gu ? c + nb * it : c_dn + nb * (it - n_gu_mine);
-      const int gslot = is_gu ? u / L.nrt : 0;
+      int u, gslot, rt = 0;
+      if (it < n_sh_mine) {
+        u = c + nb * it;
+        gslot = 0;
+        rt = u;
+      } else if (is_gu) {
+        const int r = p_rt + nb * (it - n_sh_mine);
+        gslot = 1 + r / L.nrt;
+        rt = r - (gslot - 1) * L.nrt;
+        u = r;
+      } else {
+        u = c_dn + nb * (it - n_gu_mine);
+        gslot = 0;
+      }
       if ((!is_gu || gslot > 0) && !routed) {
-        ok = mbar_wait(route, 0) && *reinterpret_cast<volatile int *>(&s_flag[2]) == 0;
+        ok = mbar_wait_idle(route, 0, 32) && *reinterpret_cast<volatile int *>(&s_flag[2]) == 0;
         routed = true;
         if (!ok) break;
       }
       if (is_gu) {
-        const int rt = u % L.nrt, r0 = rt * kRowsU;
+        const int r0 = rt * kRowsU;
         const uint8_t *blob = gslot == 0 ? a.w.shared : a.w.experts + (size_t)s_sel[gslot - 1] * a.w.stride;
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRowsU * (H / 2) + 4 * kRowsU * G * 2));
         __syncwarp();
@@ -301,7 +327,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     if (lane == 0) {
       if (!ok) set_error(a.err, kErrTimeout);
       for (int it = issued - kSlots > 0 ? issued - kSlots : 0; it < issued; ++it)
-        mbar_wait(&full[it % kSlots], (it / kSlots) & 1);
+        mbar_wait_idle(&full[it % kSlots], (it / kSlots) & 1);
     }
     return;
   }
@@ -426,91 +452,24 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     a.logits[c] = t + (a.w.logit_bias ? a.w.logit_bias[c] : 0.f);
   }
 
-  // ---- phase 2: grid barrier, then every block selects the top-k itself
-  if (!grid_sync(bar_count, base + nb, a.err, &s_flag[0])) {
-    if (tid == 0) {
-      s_flag[2] = 1;                     // no routing: the producer must not stream routed tiles
-      mbar_arrive_expect_tx(route, 0);   // release it; it drains its copies and exits
-      // still count this block's second arrival: every launch moves the
-      // counter by exactly 2*nb
-      asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar_count) : "memory");
-    }
-    return;
-  }
-  if (warp == 0) {
-    // Top-k with two warp reductions per pick: the largest key, then the
-    // lowest expert id holding it (ties to the lower id).  Keys are the
-    // order-preserving bit patterns of the fp32 logits; non-finite -> -inf.
-    unsigned key[4];
-    bool nonfinite = false;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = lane + 32 * i;
-      key[i] = 0u;  // below every real key: never picked while k <= E
-      if (e < E) {
-        float x = __ldcg(a.logits + e);
-        if (!isfinite(x)) {
-          x = -INFINITY;
-          nonfinite = true;
-        }
-        key[i] = ord_key(x);
-      }
-    }
-    if (__any_sync(0xffffffffu, nonfinite) && lane == 0 && c == 0) set_error(a.err, kErrNonFinite);
-    float selv[kMaxTopK];
-    int seli[kMaxTopK];
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j < k) {
-        // lane-local best: highest key, lowest index on ties
-        unsigned bk = key[0];
-        int bi = lane;
-#pragma unroll
-        for (int i = 1; i < 4; ++i)
-          if (key[i] > bk) {
-            bk = key[i];
-            bi = lane + 32 * i;
-          }
-        const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
-        const unsigned idmin = __reduce_min_sync(0xffffffffu, bk == kmax ? (unsigned)bi : 0xffffffffu);
-        selv[j] = key_value(kmax);
-        seli[j] = (int)idmin;
-        if ((int)(idmin & 31u) == lane) key[idmin >> 5] = 0u;  // taken
-      }
-    }
-    float ex[kMaxTopK], den = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k) {
-        ex[j] = expf(selv[j] - selv[0]);
-        den += ex[j];
-      }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
-      if (j < k && lane == j) {
-        const float wj = ex[j] / den;
-        s_sel[j] = seli[j];
-        s_w[j] = wj;
-        if (c == 0) {
-          if (a.ids_user) a.ids_user[j] = seli[j];
-          if (a.wts_user) a.wts_user[j] = wj;
-        }
-      }
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(route, 0);  // routing known: producer may stream
-  }
-  cons_sync();
-  if (c == 0 && tid == 0) trace_max(a.trace, kTrLoaded);
-
-  // ---- phase 3: gate/up units
+  // ---- phase 2: arrive at the grid barrier; compute this block's shared
+  // gate/up units (their tiles and x are here) while the routing completes
   const int r = lane >> 2, cq = lane & 3;
   int it = 0;
   bool ok = true;
-  for (; it < n_gu_mine; ++it) {
+  // one gate/up unit: 16 rows of gate and up of one slot, GeGLU, h to global
+  auto gu_unit = [&](int it) -> bool {
     const int slot = it % kSlots;
-    const int u = c + nb * it;
-    const int gslot = u / L.nrt, rt = u % L.nrt;
-    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) { ok = false; break; }
+    int gslot, rt;
+    if (it < n_sh_mine) {
+      gslot = 0;
+      rt = c + nb * it;
+    } else {
+      const int r = p_rt + nb * (it - n_sh_mine);
+      gslot = 1 + r / L.nrt;
+      rt = r - (gslot - 1) * L.nrt;
+    }
+    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) return false;
     const uint8_t *tile = ring + slot * L.slot_bytes;
     // groups warp, warp + kCons, ...; two groups in flight per iteration
     float tg0a = 0.f, tg2a = 0.f, tu0a = 0.f, tu2a = 0.f, tg0b = 0.f, tg2b = 0.f, tu0b = 0.f, tu2b = 0.f;
@@ -541,7 +500,89 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     }
     cons_sync();
     if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);  // slot free
+    return true;
+  };
+
+  grid_arrive(bar_count);
+  for (; it < n_sh_mine && ok; ++it) ok = gu_unit(it);
+  if (!grid_wait(bar_count, base + nb, a.err, &s_flag[0]) || !ok) {
+    if (tid == 0) {
+      if (!ok) set_error(a.err, kErrTimeout);
+      s_flag[2] = 1;                     // no routing: the producer must not stream routed tiles
+      mbar_arrive_expect_tx(route, 0);   // release it; it drains its copies and exits
+      // still count this block's second arrival: every launch moves the
+      // counter by exactly 2*nb
+      asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar_count) : "memory");
+    }
+    return;
   }
+  // ---- top-k, in every block: rank of logit i = number of logits above it
+  // (ties: lower id first); ranks below k are the selection, in order
+  {
+    unsigned *s_key = reinterpret_cast<unsigned *>(sred);  // [kMaxExperts]; 0 past E (below every key)
+    float *s_val = sred + kMaxExperts;                      // [k]
+    if (tid < kMaxExperts) {
+      unsigned key = 0u;
+      if (tid < E) {
+        float x = __ldcg(a.logits + tid);
+        if (!isfinite(x)) {
+          x = -INFINITY;
+          if (c == 0) set_error(a.err, kErrNonFinite);
+        }
+        key = ord_key(x);
+      }
+      s_key[tid] = key;
+    }
+    cons_sync();
+    const int i = tid >> 2, part = tid & 3;  // 4 threads per logit, 32 candidates each
+    int rank = 0;
+    const unsigned ki = s_key[i];
+    {
+      // the 32 candidates in registers first (eight 16-byte loads), then compared
+      uint4 kv[8];
+      const uint4 *src4 = reinterpret_cast<const uint4 *>(s_key + 32 * part);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) kv[v] = src4[v];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const unsigned kk[4] = {kv[v].x, kv[v].y, kv[v].z, kv[v].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int j = 32 * part + 4 * v + w;
+          rank += (kk[w] > ki || (kk[w] == ki && j < i)) ? 1 : 0;
+        }
+      }
+    }
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+    if (i < E && part == 0 && rank < k) {
+      s_sel[rank] = i;
+      s_val[rank] = key_value(ki);
+    }
+    cons_sync();
+    if (warp == 0) {
+      float ex = 0.f;
+      if (lane < k) ex = __expf(s_val[lane] - s_val[0]);
+      float den = ex;
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      if (lane < k) {
+        const float wj = ex / den;
+        s_w[lane] = wj;
+        if (c == 0) {
+          if (a.ids_user) a.ids_user[lane] = s_sel[lane];
+          if (a.wts_user) a.wts_user[lane] = wj;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(route, 0);  // routing known: producer may stream
+    }
+  }
+  cons_sync();
+  if (c == 0 && tid == 0) trace_max(a.trace, kTrLoaded);
+
+  // ---- phase 3: routed gate/up units
+  for (; it < n_gu_mine && ok; ++it) ok = gu_unit(it);
   if (!ok) set_error(a.err, kErrTimeout);
 
   // ---- phase 4: grid barrier (all of h written), then the down units
@@ -584,18 +625,26 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     const int nitems = S * GI;
     const int per = (nitems + kCons - 1) / kCons;
     const int ib = warp * per, ie = min(nitems, ib + per);
-    // two independent accumulation chains per warp (items q and q+1)
+    // two independent accumulation chains per warp (items q and q+1); item
+    // q = (slot sa, group ga), advanced without divisions
     float t0a = 0.f, t2a = 0.f, t0b = 0.f, t2b = 0.f;
-    int q = ib;
+    int q = ib, sa = ib / GI, ga = ib - (ib / GI) * GI;
     for (; q + 1 < ie; q += 2) {
-      const int sa = q / GI, ga = q - sa * GI, sb2 = (q + 1) / GI, gb = (q + 1) - sb2 * GI;
+      int sb2 = sa, gb = ga + 1;
+      if (gb == GI) {
+        gb = 0;
+        ++sb2;
+      }
       down_item(tile, hperm, hsum, s_w, sa, ga, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0a, t2a);
       down_item(tile, hperm, hsum, s_w, sb2, gb, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0b, t2b);
+      sa = sb2;
+      ga = gb + 1;
+      if (ga == GI) {
+        ga = 0;
+        ++sa;
+      }
     }
-    if (q < ie) {
-      const int sa = q / GI, ga = q - sa * GI;
-      down_item(tile, hperm, hsum, s_w, sa, ga, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0a, t2a);
-    }
+    if (q < ie) down_item(tile, hperm, hsum, s_w, sa, ga, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0a, t2a);
     if (cq == 0) {
       sred[warp * kRowsU + r] = t0a + t0b;
       sred[warp * kRowsU + r + 8] = t2a + t2b;

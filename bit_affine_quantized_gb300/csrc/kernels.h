@@ -63,7 +63,7 @@ struct DecodeArgs {
   float *wts_user;          // nullable [k]
   __half *hbuf;             // fp16 [k+1, I]: slot 0 shared, slot j+1 = j-th selected
   uint16_t *y;              // nullable bf16 [H]
-  unsigned *sync;           // grid barrier area: [0] epoch, [32] release, [64..] per-block flags
+  unsigned *sync;           // 64-bit grid barrier counter (this kernel's own)
   unsigned *err;
   unsigned long long *trace;
   int normalize;

@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     // next W slot in ring order (waits for the consumers to release it)
     auto acquire = [&]() -> uint8_t * {
       const int slot = it % kWSlots;
-      if (it >= kWSlots) ok = mbar_wait(&empty[slot], ((it / kWSlots) - 1) & 1);
+      if (it >= kWSlots) ok = mbar_wait_idle(&empty[slot], ((it / kWSlots) - 1) & 1);
       return ring + slot * L.wslot;
     };
     // router tiles: weights only, so they are fetched before the dependency wait
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         bulk_g2s(dst + j * L.rt_qp, a.w.router_q + (size_t)(e0 + j) * H, (uint32_t)H, bar);
       ++it;
     }
-    if (ok) ok = mbar_wait(route, 0) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
+    if (ok) ok = mbar_wait_idle(route, 0, 32) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
     fused::fence_proxy_async_global();  // operand rows written by other blocks before barrier 1
     if (ok) {
       const int nact = s_flag[9];
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         }
         ++it;
         if (chg != cur) {
-          if (xk >= 1) ok = mbar_wait(xempty, (xk - 1) & 1);
+          if (xk >= 1) ok = mbar_wait_idle(xempty, (xk - 1) & 1, 32);
           if (!ok) break;
           if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(x.nt * (H * 2 + (H / 16) * 4)));
           __syncwarp();
@@ -415,11 +415,11 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         ++it;
         if (chg != cur) {
           if (!hr) {
-            ok = mbar_wait(hready, 0) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
+            ok = mbar_wait_idle(hready, 0, 32) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
             fused::fence_proxy_async_global();
             hr = true;
           }
-          if (ok && xk >= 1) ok = mbar_wait(xempty, (xk - 1) & 1);
+          if (ok && xk >= 1) ok = mbar_wait_idle(xempty, (xk - 1) & 1, 32);
           if (!ok) break;
           if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(x.nt * (I * 2 + (I / 16) * 4)));
           __syncwarp();
@@ -439,8 +439,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     // copies in flight must land before the block's shared memory is released
     if (lane == 0) {
       if (!ok) set_error(a.err, kErrTimeout);
-      for (int j = it - kWSlots > 0 ? it - kWSlots : 0; j < it; ++j) mbar_wait(&full[j % kWSlots], (j / kWSlots) & 1);
-      if (xk >= 1) mbar_wait(xfull, (xk - 1) & 1);
+      for (int j = it - kWSlots > 0 ? it - kWSlots : 0; j < it; ++j) mbar_wait_idle(&full[j % kWSlots], (j / kWSlots) & 1);
+      if (xk >= 1) mbar_wait_idle(xfull, (xk - 1) & 1);
     }
     return;
   }
