@@ -539,16 +539,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     const unsigned ki = s_key[i];
     {
       // the 32 candidates in registers first (eight 16-byte loads), then compared
+      // (the four parts start at different 16-byte chunks: no bank conflicts)
       uint4 kv[8];
       const uint4 *src4 = reinterpret_cast<const uint4 *>(s_key + 32 * part);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) kv[v] = src4[v];
+      for (int v = 0; v < 8; ++v) kv[v] = src4[(v + 2 * part) & 7];
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         const unsigned kk[4] = {kv[v].x, kv[v].y, kv[v].z, kv[v].w};
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const int j = 32 * part + 4 * v + w;
+          const int j = 32 * part + 4 * ((v + 2 * part) & 7) + w;
           rank += (kk[w] > ki || (kk[w] == ki && j < i)) ? 1 : 0;
         }
       }
