@@ -8,6 +8,9 @@
 // One persistent block per SM; 16 consumer warps and 1 producer warp.  The
 // producer streams weight tiles through a 3-slot ring (W) and operand rows
 // into one buffer (X) that stays put while consecutive units share a chunk.
+// In the unit phases the consumers work as two groups of 8 warps, each on
+// every other unit with a named barrier of its own, so one group's
+// reduction and epilogue overlap the other group's tensor-core loop.
 //   R  tokens t = block, block + grid, ...: x = input (or rmsnorm of the
 //      residual); permuted fp16 operand rows and quarter sums go to the
 //      workspace for the experts; the block scores its own token against
@@ -44,6 +47,11 @@ constexpr int kDnRows = 128; // down rows per unit (8 x m16)
 constexpr int kRtRows = 16;  // router experts per tile
 constexpr int kNBar = 3;     // grid barriers per launch
 constexpr int kRedBytes = kCons * 256 * 4;
+
+// misc: s_flag int[16] | s_hst fp16[8][16] (group 0) | s_logit float[128] | s_part float[16] |
+// mbarriers [10] | s_wt float[8] (group 0) | s_hst (group 1) | s_wt (group 1)
+constexpr int kMiscHst = 64, kMiscLogit = 320, kMiscPart = 832, kMiscBar = 896, kMiscWt = 976, kMiscHst1 = 1024,
+              kMiscWt1 = 1280, kMiscBytes = 1536;
 
 __host__ __device__ inline int pw8(int w) { return w + ((8 - (w % 16)) + 16) % 16; }
 __host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
@@ -96,13 +104,11 @@ __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) 
   L.grp = o;  // chunk0 int32 [E+2], perm/pos int16 [T*k], act_e/beg/cnt int16 [E+1]
   o = al16(o + (E + 2) * 4 + 2 * T * k * 2 + 3 * (E + 1) * 2);
   L.misc = o;
-  o = al16(o + 1024);
+  o = al16(o + kMiscBytes);
   L.total = o;
   return L;
 }
 
-// misc: s_flag int[16] | s_hst fp16[8][16] | s_logit float[128] | s_part float[16] | mbarriers [10] | s_wt float[8]
-constexpr int kMiscHst = 64, kMiscLogit = 320, kMiscPart = 832, kMiscBar = 896, kMiscWt = 976;
 
 // First index i in [0, n) with v[i + 1] > x (v ascending, v[0] == 0).
 __device__ __forceinline__ int find_slot(const int *v, int n, int x) {
@@ -278,7 +284,6 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   int16_t *g_act_beg = g_act_e + (E + 1);                               // [E+1]
   int16_t *g_act_cnt = g_act_beg + (E + 1);                             // [E+1]
   int *s_flag = reinterpret_cast<int *>(smem + L.misc);
-  __half *s_hst = reinterpret_cast<__half *>(smem + L.misc + kMiscHst);
   float *s_logit = reinterpret_cast<float *>(smem + L.misc + kMiscLogit);
   float *s_part = reinterpret_cast<float *>(smem + L.misc + kMiscPart);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.misc + kMiscBar);  // [kWSlots]
@@ -287,7 +292,10 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   uint64_t *xempty = xfull + 1;
   uint64_t *route = xempty + 1;   // grouping ready
   uint64_t *hready = route + 1;   // all h written (barrier 2 passed)
-  float *s_wt = reinterpret_cast<float *>(smem + L.misc + kMiscWt);  // routing weights of the current down chunk
+  // per consumer group: h staging of a gate/up unit, routing weights of the current down chunk
+  const int gi = (warp >> 3) & 1, wl = warp & 7, gt = tid & 255;
+  __half *s_hst_g = reinterpret_cast<__half *>(smem + L.misc + (gi ? kMiscHst1 : kMiscHst));
+  float *s_wt_g = reinterpret_cast<float *>(smem + L.misc + (gi ? kMiscWt1 : kMiscWt));
 
   // this block's router tiles: every 16-expert tile once per own token
   const int n_tok = c < T ? (T - 1 - c) / nb + 1 : 0;
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       mbar_init(&empty[i], kCons);
     }
     mbar_init(xfull, 1);
-    mbar_init(xempty, 1);
+    mbar_init(xempty, 2);  // one arrival per consumer group
     mbar_init(route, 1);
     mbar_init(hready, 1);
     fence_mbar_init();
@@ -466,6 +474,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   // every launch arrives at all kNBar barriers, even after a failure
   auto barrier = [&]() {
     ++nbar;
+    if (aborted) s_flag[8] = 1;  // make a failure of either group the block's
+    cons_sync();
+    aborted = s_flag[8] != 0;
     if (!aborted) {
       aborted = !fused::grid_sync(bar_count, base + (unsigned long long)nbar * nb, a.err, &s_flag[nbar]);
     } else {
@@ -474,11 +485,17 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       cons_sync();
     }
   };
-  // one arrival per consumer warp releases a W slot
+  // a W slot is released by 16 arrivals: one per consumer warp (router
+  // tiles, used by all warps) or two per warp of the group that used it
   auto release = [&](int slot) {
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(&empty[slot], 0);
   };
+  auto release_g = [&](int slot) {
+    __syncwarp();
+    if (lane == 0) fused::mbar_arrive_cnt(&empty[slot], 2);
+  };
+  auto gsync = [&]() { asm volatile("bar.sync %0, 256;" ::"r"(2 + gi) : "memory"); };
   const uint16_t *src = a.normalize ? a.hres : a.x;
   const int nquart = H / 16;
   const int r = lane >> 2, cq = lane & 3;
@@ -697,86 +714,101 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   const int nact = aborted ? 0 : s_flag[9];
   const int nchunks = aborted ? 0 : chunk0[nact];
 
-  // ---- G: gate/up units [c * n_gu / nb, (c + 1) * n_gu / nb)
+  // ---- G: gate/up units [c * n_gu / nb, (c + 1) * n_gu / nb).  Steps of two
+  // consecutive units of one chunk (group 0 takes the first, group 1 the
+  // second) or one unit at a chunk's end; both groups walk every step so they
+  // leave each X phase (chunk) together.
   {
     const int n_gu = nchunks * L.nrt;
-    int cur = -1, p0 = 0, nt = 0;  // current chunk: first sorted position, tokens
-    for (int u = c * n_gu / nb; u < (c + 1) * n_gu / nb && !aborted; ++u) {
-      const int chg = u / L.nrt, tile = u - chg * L.nrt;
-      if (chg != cur) {
+    const int lo = c * n_gu / nb, hi = (c + 1) * n_gu / nb;
+    int u = lo, itu = it, ph = -1, xp = xk - 1, p0 = 0, nt = 0;
+    while (u < hi && !aborted) {
+      const int chg = u / L.nrt;
+      const bool pair = u + 1 < hi && (u + 1) / L.nrt == chg;
+      if (chg != ph) {
+        // leave the old chunk, then wait for the new one's rows even without a
+        // unit in it: a group never runs a phase ahead, so the release barrier
+        // (two arrivals, one per group) completes phase by phase
+        if (ph >= 0 && gt == 0) fused::mbar_arrive_cnt(xempty, 1);
+        ph = chg;
+        ++xp;
         const Unit x = decode_unit(u, L.nrt, chunk0, nact, g_act_e, g_act_beg, g_act_cnt);
         p0 = x.beg + kTC * x.ch;
         nt = x.nt;
-        if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
-        if (!mbar_wait(xfull, xk & 1)) {
+        if (!mbar_wait(xfull, xp & 1)) {
           aborted = true;
           set_error(a.err, kErrTimeout);
           break;
         }
-        ++xk;
-        cur = chg;
       }
-      const int slot = it % kWSlots;
-      if (!mbar_wait(&full[slot], (it / kWSlots) & 1)) {
-        aborted = true;
-        set_error(a.err, kErrTimeout);
-        break;
-      }
-      const uint8_t *wt = ring + slot * L.wslot;
-      const float *xq = reinterpret_cast<const float *>(xbuf + L.x_xq);
-      float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
-      float tg2[4] = {0.f, 0.f, 0.f, 0.f}, tu2[4] = {0.f, 0.f, 0.f, 0.f};
-      int g = warp;
-      for (; g + kCons < G; g += 2 * kCons) {
-        gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
-        gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g + kCons, r, cq, tg2, tu2);
-      }
-      if (g < G) gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
-      release(slot);
-      ++it;
-      // cross-warp reduction, transposed so both sides are conflict-free: red[w][i][lane]
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        red[warp * 256 + i * 32 + lane] = tg[i] + tg2[i];
-        red[warp * 256 + (i + 4) * 32 + lane] = tu[i] + tu2[i];
-      }
-      cons_sync();
-      if (tid < kGuRows * kTC) {
-        const int idx = tid >> 5, ln = tid & 31;
-        float gs = 0.f, us = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCons; ++w) {
-          gs += red[w * 256 + idx * 32 + ln];
-          us += red[w * 256 + (idx + 4) * 32 + ln];
+      const int mine = gi == 0 ? u : (pair ? u + 1 : -1);
+      if (mine >= 0) {
+        const int myit = itu + gi, slot = myit % kWSlots, tile = mine - chg * L.nrt;
+        if (!mbar_wait(&full[slot], (myit / kWSlots) & 1)) {
+          aborted = true;
+          set_error(a.err, kErrTimeout);
+          break;
         }
-        const int row = (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);
-        const float hv = fused::gelu_tanh(gs) * us;
-        if (n < nt && !(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
-        s_hst[n * 16 + row] = __float2half_rn(hv);
-      }
-      cons_sync();
-      if (tid < nt) {  // one thread per token writes its 16-row quarter of h
-        const int pos = p0 + tid;
-        const uint4 *hv = reinterpret_cast<const uint4 *>(s_hst + tid * 16);
-        const uint4 v0 = hv[0], v1 = hv[1];
-        const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint32_t out[8];
-        operand_quarter<false>(in, out);
-        uint4 *dst = reinterpret_cast<uint4 *>(a.hperm + (size_t)pos * I + tile * kGuRows);
-        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          s += __half2float(__ushort_as_half((unsigned short)(in[w] & 0xFFFFu)));
-          s += __half2float(__ushort_as_half((unsigned short)(in[w] >> 16)));
+        const uint8_t *wt = ring + slot * L.wslot;
+        const float *xq = reinterpret_cast<const float *>(xbuf + L.x_xq);
+        float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
+        float tg2[4] = {0.f, 0.f, 0.f, 0.f}, tu2[4] = {0.f, 0.f, 0.f, 0.f};
+        int g = wl;
+        for (; g + 8 < G; g += 16) {
+          gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
+          gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g + 8, r, cq, tg2, tu2);
         }
-        a.hq[(size_t)pos * (I / 16) + tile] = s;
+        if (g < G) gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
+        release_g(slot);
+        // reduction over the group's 8 warps, transposed (conflict-free): red[w][i][lane]
+        float *red_g = red + gi * 8 * 256;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          red_g[wl * 256 + i * 32 + lane] = tg[i] + tg2[i];
+          red_g[wl * 256 + (i + 4) * 32 + lane] = tu[i] + tu2[i];
+        }
+        gsync();
+        if (gt < kGuRows * kTC) {
+          const int idx = gt >> 5, ln = gt & 31;
+          float gs = 0.f, us = 0.f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            gs += red_g[w * 256 + idx * 32 + ln];
+            us += red_g[w * 256 + (idx + 4) * 32 + ln];
+          }
+          const int row = (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);
+          const float hv = fused::gelu_tanh(gs) * us;
+          if (n < nt && !(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
+          s_hst_g[n * 16 + row] = __float2half_rn(hv);
+        }
+        gsync();
+        if (gt < nt) {  // one thread per token writes its 16-row quarter of h
+          const int pos = p0 + gt;
+          const uint4 *hv = reinterpret_cast<const uint4 *>(s_hst_g + gt * 16);
+          const uint4 v0 = hv[0], v1 = hv[1];
+          const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          uint32_t out[8];
+          operand_quarter<false>(in, out);
+          uint4 *dst = reinterpret_cast<uint4 *>(a.hperm + (size_t)pos * I + tile * kGuRows);
+          dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+          dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+          float sm = 0.f;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            sm += __half2float(__ushort_as_half((unsigned short)(in[w] & 0xFFFFu)));
+            sm += __half2float(__ushort_as_half((unsigned short)(in[w] >> 16)));
+          }
+          a.hq[(size_t)pos * (I / 16) + tile] = sm;
+        }
+        // red_g is rewritten after the group's next tensor-core loop, s_hst_g
+        // after its next barrier: both after every thread's reads here
       }
-      // red is rewritten after the next unit's compute and s_hst after its
-      // first consumer barrier, which every thread reaches after this point
+      u += pair ? 2 : 1;
+      itu += pair ? 2 : 1;
     }
-    if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
+    if (ph >= 0 && gt == 0) fused::mbar_arrive_cnt(xempty, 1);
+    it += hi - lo;
+    xk = xp + 1;
   }
 
   fused::fence_proxy_async_global();  // h rows are read back by bulk copies
@@ -786,65 +818,67 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     mbar_arrive_expect_tx(hready, 0);
   }
 
-  // ---- D: down units [c * n_dn / nb, (c + 1) * n_dn / nb) -> weighted outputs
+  // ---- D: down units [c * n_dn / nb, (c + 1) * n_dn / nb) -> weighted outputs,
+  // in the same two-group steps.  A group's warp w owns rows 16w..16w+15 of its
+  // 128-row unit over the whole K, so its results leave straight from registers.
   {
     const int n_dn = nchunks * L.nrt_dn;
-    const int mt = warp & 7, kh = warp >> 3;  // 16-row tile, K half
-    int cur = -1, p0 = 0, nt = 0;
-    for (int u = c * n_dn / nb; u < (c + 1) * n_dn / nb && !aborted; ++u) {
-      const int chg = u / L.nrt_dn, tile = u - chg * L.nrt_dn;
-      if (chg != cur) {
+    const int lo = c * n_dn / nb, hi = (c + 1) * n_dn / nb;
+    int u = lo, itu = it, ph = -1, xp = xk - 1, p0 = 0, nt = 0;
+    while (u < hi && !aborted) {
+      const int chg = u / L.nrt_dn;
+      const bool pair = u + 1 < hi && (u + 1) / L.nrt_dn == chg;
+      if (chg != ph) {
+        if (ph >= 0 && gt == 0) fused::mbar_arrive_cnt(xempty, 1);
+        ph = chg;
+        ++xp;
         const Unit x = decode_unit(u, L.nrt_dn, chunk0, nact, g_act_e, g_act_beg, g_act_cnt);
         p0 = x.beg + kTC * x.ch;
         nt = x.nt;
-        // the chunk's routing weights, read once (the previous unit's readers
-        // are past its last consumer barrier)
-        if (tid < nt) {
-          const int pos = p0 + tid;
-          s_wt[tid] = pos >= npairs ? 1.0f : __ldcg(a.r.wts + g_perm[pos]);
+        // the chunk's routing weights for this group (after its last readers)
+        gsync();
+        if (gt < nt) {
+          const int pos = p0 + gt;
+          s_wt_g[gt] = pos >= npairs ? 1.0f : __ldcg(a.r.wts + g_perm[pos]);
         }
-        if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
-        if (!mbar_wait(xfull, xk & 1)) {
+        gsync();
+        if (!mbar_wait(xfull, xp & 1)) {  // as for gate/up: never a phase ahead
           aborted = true;
           set_error(a.err, kErrTimeout);
           break;
         }
-        ++xk;
-        cur = chg;
       }
-      const int slot = it % kWSlots;
-      if (!mbar_wait(&full[slot], (it / kWSlots) & 1)) {
-        aborted = true;
-        set_error(a.err, kErrTimeout);
-        break;
-      }
-      const uint8_t *wt = ring + slot * L.wslot;
-      const float *hq = reinterpret_cast<const float *>(xbuf + L.x_hq);
-      float t4[4] = {0.f, 0.f, 0.f, 0.f}, t4b[4] = {0.f, 0.f, 0.f, 0.f};
-      int g = kh;
-      for (; g + 2 < GI; g += 4) {
-        dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * mt, g, r, cq, t4);
-        dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * mt, g + 2, r, cq, t4b);
-      }
-      if (g < GI) dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * mt, g, r, cq, t4);
-      release(slot);
-      ++it;
+      const int mine = gi == 0 ? u : (pair ? u + 1 : -1);
+      if (mine >= 0) {
+        const int myit = itu + gi, slot = myit % kWSlots, tile = mine - chg * L.nrt_dn;
+        if (!mbar_wait(&full[slot], (myit / kWSlots) & 1)) {
+          aborted = true;
+          set_error(a.err, kErrTimeout);
+          break;
+        }
+        const uint8_t *wt = ring + slot * L.wslot;
+        const float *hq = reinterpret_cast<const float *>(xbuf + L.x_hq);
+        float t4[4] = {0.f, 0.f, 0.f, 0.f}, t4b[4] = {0.f, 0.f, 0.f, 0.f};
+        int g = 0;
+        for (; g + 1 < GI; g += 2) {
+          dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * wl, g, r, cq, t4);
+          dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * wl, g + 1, r, cq, t4b);
+        }
+        if (g < GI) dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * wl, g, r, cq, t4);
+        release_g(slot);
+        const int n0 = tile * kDnRows, rows = min(kDnRows, H - n0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) red[warp * 128 + i * 32 + lane] = t4[i] + t4b[i];
-      cons_sync();
-      const int n0 = tile * kDnRows, rows = min(kDnRows, H - n0);
-      for (int o = tid; o < kDnRows * kTC; o += kConsThreads) {
-        const int m = o >> 7, idx = (o >> 5) & 3, ln = o & 31;
-        const int row = 16 * m + (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);
-        if (n < nt && row < rows) {
-          const float v = red[m * 128 + idx * 32 + ln] + red[(m + 8) * 128 + idx * 32 + ln];
-          const int pos = p0 + n;
-          a.obuf[(size_t)pos * H + n0 + row] = s_wt[n] * v;
+        for (int i = 0; i < 4; ++i) {
+          const int row = 16 * wl + r + 8 * (i >> 1), n = 2 * cq + (i & 1);
+          if (n < nt && row < rows) a.obuf[(size_t)(p0 + n) * H + n0 + row] = s_wt_g[n] * (t4[i] + t4b[i]);
         }
       }
-      cons_sync();  // red is rewritten by the next unit
+      u += pair ? 2 : 1;
+      itu += pair ? 2 : 1;
     }
-    if (cur >= 0 && tid == 0) mbar_arrive_expect_tx(xempty, 0);
+    if (ph >= 0 && gt == 0) fused::mbar_arrive_cnt(xempty, 1);
+    it += hi - lo;
+    xk = xp + 1;
   }
 
   barrier();  // 3: all weighted outputs

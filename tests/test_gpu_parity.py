@@ -213,7 +213,7 @@ def test_small_shapes(moe, hidden_dim, inter, n_experts, k, n_tokens):
 
 
 @pytest.mark.parametrize("residual", [False, True])
-@pytest.mark.parametrize("n_tokens", [1, 2, 37, 128])
+@pytest.mark.parametrize("n_tokens", [1, 2, 4, 37, 128])
 def test_fused_and_chained_paths_agree(layer0, layer0_zipf, residual, n_tokens):
     """Layer calls run a fused one-launch kernel by default (the single-token
     kernel for T == 1, the prefill kernel for 2 <= T <= 128); a handle created
