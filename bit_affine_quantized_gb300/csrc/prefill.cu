@@ -56,6 +56,9 @@ constexpr int kMiscHst = 64, kMiscLogit = 320, kMiscPart = 832, kMiscBar = 896, 
 __host__ __device__ inline int pw8(int w) { return w + ((8 - (w % 16)) + 16) % 16; }
 __host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
 __host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
+// Quarter-sum row pitch (floats): the lanes of a fragment read rows 0, 2, 4
+// and 6 as float4s; a pitch of 4 mod 16 puts them in disjoint banks.
+__host__ __device__ inline int qsum_pitch(int n) { return n + ((4 - n % 16) + 16) % 16; }
 
 struct PL {
   int G, GI, nrt, nrt_dn, n_mt;
@@ -70,7 +73,8 @@ struct PL {
 
 // Row pitches: 8-byte fragment loads of 8 rows hit disjoint banks when the
 // pitch is 8 mod 16 words (gate/up, down codes); 16-byte loads of 2 rows
-// when it is 64 mod 128 bytes (router codes) or 4 mod 8 words (operands).
+// when it is 64 mod 128 bytes (router codes) or 4 mod 8 words (operands);
+// quarter sums: see qsum_pitch.
 __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) {
   PL L;
   L.G = H / kGroup;
@@ -86,10 +90,10 @@ __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) 
   const int dn = kDnRows * L.dn_qp + 2 * kDnRows * L.GI * 2;
   L.wslot = al16(imax(gu, imax(rt, dn)));
   L.xp = 2 * H + 16;
-  L.xqp = H / 16 + 4;
+  L.xqp = qsum_pitch(H / 16);
   L.x_xq = kTC * L.xp;
   L.hp = 2 * I + 16;
-  L.hqp = I / 16 + 4;
+  L.hqp = qsum_pitch(I / 16);
   L.x_hq = kTC * L.hp;
   L.rx_q = 2 * H;
   L.rx_sb = al16(L.rx_q + (H / 16) * 4);
