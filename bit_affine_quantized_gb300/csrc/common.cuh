@@ -164,6 +164,16 @@ __device__ __forceinline__ uint32_t codes_sub(uint32_t w) {
 }
 constexpr float kCodeScale = 16777216.0f;  // 2^24
 
+// Gate/up weight tiles (16 rows of gate, then 16 of up) arrive as 4-row
+// blocks of consecutive rows, one bulk copy each, at quad_pitch bytes: 8 mod
+// 32 words, so the rows 4q + i of blocks q = 0..3 fall in disjoint banks.
+// mma row m of a tile holds tile row quad_row(m): each half-warp's four rows
+// come from four different blocks, so the fragment loads are conflict free.
+__host__ __device__ inline int quad_pitch(int H) { return 2 * H + 32; }  // 4 rows of H/2 bytes + 32
+__host__ __device__ inline int quad_row(int m) { return 4 * (m & 3) + (m >> 2); }
+// bytes of a gate/up tile: 8 blocks, then gate scale/bias and up scale/bias [16][H/64] bf16
+__host__ __device__ inline int quad_tile_bytes(int H) { return 8 * quad_pitch(H) + 4 * 16 * (H / 64) * 2; }
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
 // bf16 pair -> fp16 pair (exact in fp16's normal range).

@@ -41,7 +41,7 @@ __host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
 struct FusedLayout {
   int nrt;          // gate/up units per expert (I / 16)
   int n_gu, n_dn;   // gate/up units, down units
-  int gu_qp;        // gate/up code row pitch (bytes)
+  int gu_qp;        // gate/up 4-row block pitch (bytes)
   int gu_bytes, dn_qp, dn_slot_bytes, dn_bytes, slot_bytes;
   int ring, xnat, xperm, xsum, qsum, hperm, hsum, red, misc, total;
 };
@@ -52,8 +52,8 @@ __host__ __device__ inline FusedLayout fused_layout(int H, int I, int k) {
   L.nrt = I / kRowsU;
   L.n_gu = S * L.nrt;
   L.n_dn = H / kRowsU;
-  L.gu_qp = pw8(H / 8) * 4;
-  L.gu_bytes = 2 * kRowsU * L.gu_qp + 4 * kRowsU * G * 2;
+  L.gu_qp = quad_pitch(H);
+  L.gu_bytes = quad_tile_bytes(H);
   L.dn_qp = pw8(I / 8) * 4;
   L.dn_slot_bytes = kRowsU * L.dn_qp + 2 * kRowsU * GI * 2;
   L.dn_bytes = S * L.dn_slot_bytes;
@@ -135,16 +135,19 @@ __device__ __forceinline__ float gelu_tanh_f(float z) {
   return 0.5f * z * (1.0f + tanhf(c0 * fmaf(0.044715f * z, z * z, z)));
 }
 
-// One 64-wide group of a gate/up unit: rows r, r+8 of gate and up, token
-// column 0 (valid in the lanes with cq == 0).  Accumulates the affine-
-// corrected partials s*acc + (b - 128 s)*sum(x).
+// One 64-wide group of a gate/up unit: mma rows r, r+8 (tile rows quad_row(r),
+// quad_row(r + 8)) of gate and up, token column 0 (valid in the lanes with
+// cq == 0).  Accumulates the affine-corrected partials s*acc + b*sum(x).
 __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xperm, const float *xsum, int g, int r,
                                          int cq, int G, int qp, float &tg0, float &tg2, float &tu0, float &tu2) {
-  const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 2 * 16 * qp);  // gs, gb, us, ub [16][G]
-  const uint2 g0 = *reinterpret_cast<const uint2 *>(tile + r * qp + g * 32 + cq * 8);
-  const uint2 g1 = *reinterpret_cast<const uint2 *>(tile + (r + 8) * qp + g * 32 + cq * 8);
-  const uint2 u0 = *reinterpret_cast<const uint2 *>(tile + (16 + r) * qp + g * 32 + cq * 8);
-  const uint2 u1 = *reinterpret_cast<const uint2 *>(tile + (16 + r + 8) * qp + g * 32 + cq * 8);
+  const int rowb = G * 32;                    // bytes of one row of codes (H / 2)
+  const int sr0 = quad_row(r), sr1 = sr0 + 2;  // tile rows of mma rows r and r + 8
+  const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 8 * qp);  // gs, gb, us, ub [16][G]
+  const uint8_t *ga = tile + (r & 3) * qp + (r >> 2) * rowb + g * 32 + cq * 8;
+  const uint2 g0 = *reinterpret_cast<const uint2 *>(ga);
+  const uint2 g1 = *reinterpret_cast<const uint2 *>(ga + 2 * rowb);
+  const uint2 u0 = *reinterpret_cast<const uint2 *>(ga + 4 * qp);
+  const uint2 u1 = *reinterpret_cast<const uint2 *>(ga + 4 * qp + 2 * rowb);
   float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
@@ -163,10 +166,10 @@ __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xpe
     mma_f16(au, B, bx.x, bx.y);
   }
   const float xs = xsum[g];
-  const float sg0 = bf16_bits_to_float(raw[r * G + g]), bg0 = bf16_bits_to_float(raw[16 * G + r * G + g]);
-  const float sg1 = bf16_bits_to_float(raw[(r + 8) * G + g]), bg1 = bf16_bits_to_float(raw[16 * G + (r + 8) * G + g]);
-  const float su0 = bf16_bits_to_float(raw[32 * G + r * G + g]), bu0 = bf16_bits_to_float(raw[48 * G + r * G + g]);
-  const float su1 = bf16_bits_to_float(raw[32 * G + (r + 8) * G + g]), bu1 = bf16_bits_to_float(raw[48 * G + (r + 8) * G + g]);
+  const float sg0 = bf16_bits_to_float(raw[sr0 * G + g]), bg0 = bf16_bits_to_float(raw[16 * G + sr0 * G + g]);
+  const float sg1 = bf16_bits_to_float(raw[sr1 * G + g]), bg1 = bf16_bits_to_float(raw[16 * G + sr1 * G + g]);
+  const float su0 = bf16_bits_to_float(raw[32 * G + sr0 * G + g]), bu0 = bf16_bits_to_float(raw[48 * G + sr0 * G + g]);
+  const float su1 = bf16_bits_to_float(raw[32 * G + sr1 * G + g]), bu1 = bf16_bits_to_float(raw[48 * G + sr1 * G + g]);
   tg0 = fmaf(bg0, xs, fmaf(sg0 * kCodeScale, ag[0], tg0));
   tg2 = fmaf(bg1, xs, fmaf(sg1 * kCodeScale, ag[2], tg2));
   tu0 = fmaf(bu0, xs, fmaf(su0 * kCodeScale, au[0], tu0));
@@ -289,14 +292,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         const uint8_t *blob = gslot == 0 ? a.w.shared : a.w.experts + (size_t)s_sel[gslot - 1] * a.w.stride;
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * kRowsU * (H / 2) + 4 * kRowsU * G * 2));
         __syncwarp();
-        const int m = lane >> 4, row = lane & 15;
-        bulk_g2s(dst + (m * kRowsU + row) * L.gu_qp,
-                 blob + (m == 0 ? a.w.off.gate_q : a.w.off.up_q) + (size_t)(r0 + row) * (H / 2), (uint32_t)(H / 2),
-                 &full[slot]);
-        if (lane < 4) {
-          const size_t off = lane == 0 ? a.w.off.gate_s : lane == 1 ? a.w.off.gate_b : lane == 2 ? a.w.off.up_s : a.w.off.up_b;
-          bulk_g2s(dst + 2 * kRowsU * L.gu_qp + lane * kRowsU * G * 2, blob + off + (size_t)r0 * G * 2,
-                   (uint32_t)(kRowsU * G * 2), &full[slot]);
+        if (lane < 8) {  // 4-row blocks: lanes 0-3 gate, 4-7 up
+          const int m = lane >> 2, q = lane & 3;
+          bulk_g2s(dst + lane * L.gu_qp, blob + (m == 0 ? a.w.off.gate_q : a.w.off.up_q) + (size_t)(r0 + 4 * q) * (H / 2),
+                   (uint32_t)(2 * H), &full[slot]);
+        } else if (lane < 12) {
+          const int f = lane - 8;
+          const size_t off = f == 0 ? a.w.off.gate_s : f == 1 ? a.w.off.gate_b : f == 2 ? a.w.off.up_s : a.w.off.up_b;
+          bulk_g2s(dst + 8 * L.gu_qp + f * kRowsU * G * 2, blob + off + (size_t)r0 * G * 2, (uint32_t)(kRowsU * G * 2),
+                   &full[slot]);
         }
       } else {
         const int n0 = u * kRowsU;
@@ -496,7 +500,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
       }
       const float hv = gelu_tanh_f(gs) * us;
       if (!(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
-      a.hbuf[(size_t)gslot * I + rt * kRowsU + tid] = __float2half_rn(hv);
+      a.hbuf[(size_t)gslot * I + rt * kRowsU + quad_row(tid)] = __float2half_rn(hv);  // tid: mma row
     }
     cons_sync();
     if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);  // slot free

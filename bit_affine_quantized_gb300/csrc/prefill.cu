@@ -62,7 +62,7 @@ __host__ __device__ inline int qsum_pitch(int n) { return n + ((4 - n % 16) + 16
 
 struct PL {
   int G, GI, nrt, nrt_dn, n_mt;
-  int gu_qp, rt_qp, dn_qp, wslot;   // W slot: code row pitches, slot bytes
+  int gu_qp, rt_qp, dn_qp, wslot;   // W slot: gate/up 4-row block pitch, code row pitches, slot bytes
   int xp, xqp, x_xq;                // X as gate/up operand: row pitch (B), quarter-sum pitch (floats), offset
   int hp, hqp, x_hq;                // X as down operand
   int rx_q, rx_sb;                  // X as router operand: quarter sums after the fp16 row, then the
@@ -82,10 +82,10 @@ __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) 
   L.nrt = I / kGuRows;
   L.nrt_dn = (H + kDnRows - 1) / kDnRows;
   L.n_mt = (E + kRtRows - 1) / kRtRows;
-  L.gu_qp = pw8(H / 8) * 4;
+  L.gu_qp = quad_pitch(H);
   L.rt_qp = H + ((64 - H % 128) + 128) % 128;
   L.dn_qp = pw8(I / 8) * 4;
-  const int gu = 2 * kGuRows * L.gu_qp + 4 * kGuRows * L.G * 2;
+  const int gu = quad_tile_bytes(H);
   const int rt = kRtRows * L.rt_qp;
   const int dn = kDnRows * L.dn_qp + 2 * kDnRows * L.GI * 2;
   L.wslot = al16(imax(gu, imax(rt, dn)));
@@ -157,15 +157,18 @@ __device__ __forceinline__ void rt_group(const uint8_t *tile, const uint8_t *rx,
             fmaf(bf16_bits_to_float(rs[(r + 8) * G + g]) * kCodeScale, acc[2], t1));
 }
 
-// Gate/up: one 64-wide group for an 8-token tile: rows r, r+8 of gate and
-// up, token columns 2cq, 2cq+1.
+// Gate/up: one 64-wide group for an 8-token tile: mma rows r, r+8 (tile rows
+// quad_row(r), quad_row(r + 8)) of gate and up, token columns 2cq, 2cq+1.
 __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xrows, const float *xq, int qp, int xp,
                                          int xqp, int G, int g, int r, int cq, float (&tg)[4], float (&tu)[4]) {
-  const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 2 * kGuRows * qp);  // gs, gb, us, ub [16][G]
-  const uint2 g0 = *reinterpret_cast<const uint2 *>(tile + r * qp + g * 32 + cq * 8);
-  const uint2 g1 = *reinterpret_cast<const uint2 *>(tile + (r + 8) * qp + g * 32 + cq * 8);
-  const uint2 u0 = *reinterpret_cast<const uint2 *>(tile + (16 + r) * qp + g * 32 + cq * 8);
-  const uint2 u1 = *reinterpret_cast<const uint2 *>(tile + (16 + r + 8) * qp + g * 32 + cq * 8);
+  const int rowb = G * 32;                    // bytes of one row of codes (H / 2)
+  const int sr0 = quad_row(r), sr1 = sr0 + 2;  // tile rows of mma rows r and r + 8
+  const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 8 * qp);  // gs, gb, us, ub [16][G]
+  const uint8_t *ga = tile + (r & 3) * qp + (r >> 2) * rowb + g * 32 + cq * 8;
+  const uint2 g0 = *reinterpret_cast<const uint2 *>(ga);
+  const uint2 g1 = *reinterpret_cast<const uint2 *>(ga + 2 * rowb);
+  const uint2 u0 = *reinterpret_cast<const uint2 *>(ga + 4 * qp);
+  const uint2 u1 = *reinterpret_cast<const uint2 *>(ga + 4 * qp + 2 * rowb);
   const uint4 bA = *reinterpret_cast<const uint4 *>(xrows + r * xp + g * 128 + cq * 32);
   const uint4 bB = *reinterpret_cast<const uint4 *>(xrows + r * xp + g * 128 + cq * 32 + 16);
   const uint32_t bb[8] = {bA.x, bA.y, bA.z, bA.w, bB.x, bB.y, bB.z, bB.w};
@@ -188,10 +191,10 @@ __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xro
   const float4 q0 = *reinterpret_cast<const float4 *>(xq + (2 * cq) * xqp + 4 * g);
   const float4 q1 = *reinterpret_cast<const float4 *>(xq + (2 * cq + 1) * xqp + 4 * g);
   const float xs0 = ((q0.x + q0.y) + q0.z) + q0.w, xs1 = ((q1.x + q1.y) + q1.z) + q1.w;
-  const float sg0 = bf16_bits_to_float(raw[r * G + g]) * kCodeScale, bg0 = bf16_bits_to_float(raw[16 * G + r * G + g]);
-  const float sg1 = bf16_bits_to_float(raw[(r + 8) * G + g]) * kCodeScale, bg1 = bf16_bits_to_float(raw[16 * G + (r + 8) * G + g]);
-  const float su0 = bf16_bits_to_float(raw[32 * G + r * G + g]) * kCodeScale, bu0 = bf16_bits_to_float(raw[48 * G + r * G + g]);
-  const float su1 = bf16_bits_to_float(raw[32 * G + (r + 8) * G + g]) * kCodeScale, bu1 = bf16_bits_to_float(raw[48 * G + (r + 8) * G + g]);
+  const float sg0 = bf16_bits_to_float(raw[sr0 * G + g]) * kCodeScale, bg0 = bf16_bits_to_float(raw[16 * G + sr0 * G + g]);
+  const float sg1 = bf16_bits_to_float(raw[sr1 * G + g]) * kCodeScale, bg1 = bf16_bits_to_float(raw[16 * G + sr1 * G + g]);
+  const float su0 = bf16_bits_to_float(raw[32 * G + sr0 * G + g]) * kCodeScale, bu0 = bf16_bits_to_float(raw[48 * G + sr0 * G + g]);
+  const float su1 = bf16_bits_to_float(raw[32 * G + sr1 * G + g]) * kCodeScale, bu1 = bf16_bits_to_float(raw[48 * G + sr1 * G + g]);
   tg[0] = fmaf(bg0, xs0, fmaf(sg0, ag[0], tg[0]));
   tg[1] = fmaf(bg0, xs1, fmaf(sg0, ag[1], tg[1]));
   tg[2] = fmaf(bg1, xs0, fmaf(sg1, ag[2], tg[2]));
@@ -364,16 +367,15 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         const int r0 = tile * kGuRows;
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(2 * kGuRows * (H / 2) + 4 * kGuRows * G * 2));
         __syncwarp();
-        {
-          const int m = lane >> 4, row = lane & 15;
-          bulk_g2s(dst + (m * kGuRows + row) * L.gu_qp,
-                   blob + (m == 0 ? a.w.off.gate_q : a.w.off.up_q) + (size_t)(r0 + row) * (H / 2), (uint32_t)(H / 2),
-                   bar);
-          if (lane < 4) {
-            const size_t off = lane == 0 ? a.w.off.gate_s : lane == 1 ? a.w.off.gate_b : lane == 2 ? a.w.off.up_s : a.w.off.up_b;
-            bulk_g2s(dst + 2 * kGuRows * L.gu_qp + lane * kGuRows * G * 2, blob + off + (size_t)r0 * G * 2,
-                     (uint32_t)(kGuRows * G * 2), bar);
-          }
+        if (lane < 8) {  // 4-row blocks: lanes 0-3 gate, 4-7 up
+          const int m = lane >> 2, q = lane & 3;
+          bulk_g2s(dst + lane * L.gu_qp, blob + (m == 0 ? a.w.off.gate_q : a.w.off.up_q) + (size_t)(r0 + 4 * q) * (H / 2),
+                   (uint32_t)(2 * H), bar);
+        } else if (lane < 12) {
+          const int f = lane - 8;
+          const size_t off = f == 0 ? a.w.off.gate_s : f == 1 ? a.w.off.gate_b : f == 2 ? a.w.off.up_s : a.w.off.up_b;
+          bulk_g2s(dst + 8 * L.gu_qp + f * kGuRows * G * 2, blob + off + (size_t)r0 * G * 2,
+                   (uint32_t)(kGuRows * G * 2), bar);
         }
         ++it;
         if (chg != cur) {
@@ -780,10 +782,10 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
             gs += red_g[w * 256 + idx * 32 + ln];
             us += red_g[w * 256 + (idx + 4) * 32 + ln];
           }
-          const int row = (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);
+          const int m = (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);  // mma row, token
           const float hv = fused::gelu_tanh(gs) * us;
           if (n < nt && !(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
-          s_hst_g[n * 16 + row] = __float2half_rn(hv);
+          s_hst_g[n * 16 + quad_row(m)] = __float2half_rn(hv);
         }
         gsync();
         if (gt < nt) {  // one thread per token writes its 16-row quarter of h
