@@ -71,10 +71,11 @@ struct PL {
   int ring, xb, red, grp, misc, total;
 };
 
-// Row pitches: 8-byte fragment loads of 8 rows hit disjoint banks when the
-// pitch is 8 mod 16 words (gate/up, down codes); 16-byte loads of 2 rows
-// when it is 64 mod 128 bytes (router codes) or 4 mod 8 words (operands);
-// quarter sums: see qsum_pitch.
+// Pitches: gate/up and router tiles arrive as 4-row blocks (quad_row in
+// common.cuh) whose pitch puts the four blocks in disjoint banks for the
+// fragment loads (8 mod 32 words for the 8-byte gate/up loads, 64 mod 128
+// bytes for the 16-byte router loads); down codes keep a row pitch of 8 mod
+// 16 words; operand rows 4 mod 8 words; quarter sums: see qsum_pitch.
 __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) {
   PL L;
   L.G = H / kGroup;
@@ -83,10 +84,10 @@ __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) 
   L.nrt_dn = (H + kDnRows - 1) / kDnRows;
   L.n_mt = (E + kRtRows - 1) / kRtRows;
   L.gu_qp = quad_pitch(H);
-  L.rt_qp = H + ((64 - H % 128) + 128) % 128;
+  L.rt_qp = 4 * H + ((64 - (4 * H) % 128) + 128) % 128;  // 4-row block pitch
   L.dn_qp = pw8(I / 8) * 4;
   const int gu = quad_tile_bytes(H);
-  const int rt = kRtRows * L.rt_qp;
+  const int rt = 4 * L.rt_qp;
   const int dn = kDnRows * L.dn_qp + 2 * kDnRows * L.GI * 2;
   L.wslot = al16(imax(gu, imax(rt, dn)));
   L.xp = 2 * H + 16;
@@ -135,8 +136,11 @@ __device__ __forceinline__ uint32_t bytes13(uint32_t w) { return __byte_perm(w, 
 __device__ __forceinline__ void rt_group(const uint8_t *tile, const uint8_t *rx, const float *rq, const uint16_t *rs,
                                          const uint16_t *rb, int qp, int G, int g, int r, int cq, float &t0,
                                          float &t1) {
-  const uint4 w0 = *reinterpret_cast<const uint4 *>(tile + r * qp + g * 64 + cq * 16);
-  const uint4 w1 = *reinterpret_cast<const uint4 *>(tile + (r + 8) * qp + g * 64 + cq * 16);
+  // mma rows r, r + 8 hold tile rows quad_row(r), quad_row(r) + 2 (4-row blocks at pitch qp)
+  const int rowb = G * 64, sr0 = quad_row(r), sr1 = sr0 + 2;
+  const uint8_t *wa = tile + (r & 3) * qp + (r >> 2) * rowb + g * 64 + cq * 16;
+  const uint4 w0 = *reinterpret_cast<const uint4 *>(wa);
+  const uint4 w1 = *reinterpret_cast<const uint4 *>(wa + 2 * rowb);
   uint4 b0 = make_uint4(0u, 0u, 0u, 0u), b1 = b0;
   if (r == 0) {
     b0 = *reinterpret_cast<const uint4 *>(rx + g * 128 + cq * 32);
@@ -152,9 +156,9 @@ __device__ __forceinline__ void rt_group(const uint8_t *tile, const uint8_t *rx,
   }
   const float4 q = *reinterpret_cast<const float4 *>(rq + 4 * g);
   const float xs = ((q.x + q.y) + q.z) + q.w;
-  t0 = fmaf(bf16_bits_to_float(rb[r * G + g]), xs, fmaf(bf16_bits_to_float(rs[r * G + g]) * kCodeScale, acc[0], t0));
-  t1 = fmaf(bf16_bits_to_float(rb[(r + 8) * G + g]), xs,
-            fmaf(bf16_bits_to_float(rs[(r + 8) * G + g]) * kCodeScale, acc[2], t1));
+  t0 = fmaf(bf16_bits_to_float(rb[sr0 * G + g]), xs, fmaf(bf16_bits_to_float(rs[sr0 * G + g]) * kCodeScale, acc[0], t0));
+  t1 = fmaf(bf16_bits_to_float(rb[sr1 * G + g]), xs,
+            fmaf(bf16_bits_to_float(rs[sr1 * G + g]) * kCodeScale, acc[2], t1));
 }
 
 // Gate/up: one 64-wide group for an 8-token tile: mma rows r, r+8 (tile rows
@@ -341,8 +345,9 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       uint64_t *bar = &full[it % kWSlots];
       if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows * H));
       __syncwarp();
-      for (int j = lane; j < rows; j += 32)
-        bulk_g2s(dst + j * L.rt_qp, a.w.router_q + (size_t)(e0 + j) * H, (uint32_t)H, bar);
+      if (lane < (rows + 3) / 4)  // 4-row blocks (the last one may be short)
+        bulk_g2s(dst + lane * L.rt_qp, a.w.router_q + (size_t)(e0 + 4 * lane) * H,
+                 (uint32_t)(min(4, rows - 4 * lane) * H), bar);
       ++it;
     }
     if (ok) ok = mbar_wait_idle(route, 0, 32) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
@@ -602,8 +607,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
 #pragma unroll
       for (int m = 0; m < 8; ++m)
         if (m < L.n_mt) {
-          red[warp * 128 + m * 16 + r] = rt0[m];
-          red[warp * 128 + m * 16 + r + 8] = rt1[m];
+          red[warp * 128 + m * 16 + quad_row(r)] = rt0[m];
+          red[warp * 128 + m * 16 + quad_row(r) + 2] = rt1[m];
         }
     }
     cons_sync();
