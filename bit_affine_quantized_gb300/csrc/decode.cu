@@ -43,7 +43,7 @@ struct FusedLayout {
   int n_gu, n_dn;   // gate/up units, down units
   int gu_qp;        // gate/up 4-row block pitch (bytes)
   int gu_bytes, dn_qp, dn_slot_bytes, dn_bytes, slot_bytes;
-  int ring, xnat, xperm, xsum, qsum, hperm, hsum, red, misc, total;
+  int ring, xperm, xsum, qsum, hperm, hsum, red, misc, total;
 };
 
 __host__ __device__ inline FusedLayout fused_layout(int H, int I, int k) {
@@ -61,8 +61,6 @@ __host__ __device__ inline FusedLayout fused_layout(int H, int I, int k) {
   int o = 0;
   L.ring = o;
   o += kSlots * L.slot_bytes;
-  L.xnat = o;
-  o = al16(o + H * 2);
   L.xperm = o;
   o = al16(o + H * 2);
   L.xsum = o;
@@ -75,8 +73,8 @@ __host__ __device__ inline FusedLayout fused_layout(int H, int I, int k) {
   o = al16(o + S * GI * 4);
   L.red = o;
   o = al16(o + kCons * 32 * 8 * 4);
-  L.misc = o;  // 8 partial logits, k ids, k weights, 2k+1 mbarriers, flags
-  o = al16(o + 256);
+  L.misc = o;  // partial sums, k ids, k weights, flags, 2*kSlots+1 mbarriers
+  o = al16(o + 512);
   L.total = o;
   return L;
 }
@@ -218,18 +216,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nb = gridDim.x, c = blockIdx.x;
   uint8_t *ring = smem + L.ring;
-  uint16_t *xnat = reinterpret_cast<uint16_t *>(smem + L.xnat);
   uint8_t *xperm = smem + L.xperm;
   float *xsum = reinterpret_cast<float *>(smem + L.xsum);
   float *qsum = reinterpret_cast<float *>(smem + L.qsum);
   uint8_t *hperm = smem + L.hperm;
   float *hsum = reinterpret_cast<float *>(smem + L.hsum);
   float *sred = reinterpret_cast<float *>(smem + L.red);
-  float *s_part = reinterpret_cast<float *>(smem + L.misc);        // [8]
-  int *s_sel = reinterpret_cast<int *>(smem + L.misc + 32);        // [8]
-  float *s_w = reinterpret_cast<float *>(smem + L.misc + 64);      // [8]
-  int *s_flag = reinterpret_cast<int *>(smem + L.misc + 96);       // [4]
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.misc + 128);  // [3]
+  float *s_part = reinterpret_cast<float *>(smem + L.misc);        // [2 * kCons]
+  int *s_sel = reinterpret_cast<int *>(smem + L.misc + 128);       // [kMaxTopK]
+  float *s_w = reinterpret_cast<float *>(smem + L.misc + 160);     // [kMaxTopK]
+  int *s_flag = reinterpret_cast<int *>(smem + L.misc + 192);      // [4]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.misc + 256);  // [3]
   uint64_t *empty = full + kSlots;                                     // [3]
   uint64_t *route = empty + kSlots;                                    // [1]
 
@@ -369,10 +366,13 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     if (n_dn_mine > 1) hres_pre1 = a.hres[(c_dn + nb) * kRowsU + tid];
   }
 
-  // ---- phase 1: x (one 16-element quarter per thread) and the logit
+  // ---- phase 1: x (one 16-element quarter per thread), its sum of squares
+  // and this block's router row against the raw input, in one pass: a single
+  // block reduction gives 1/rms and the dot product, so the logit
+  // (dot * 1/rms) goes out before the operand rows are staged.
   const int nquart = H / 16;
   uint32_t qin[8];
-  float qss = 0.f;
+  float qss = 0.f, lg = 0.f;
   const uint16_t *src = a.normalize ? a.hres : a.x;
   if (tid < nquart) {
     const uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(src) + 2 * tid);
@@ -386,15 +386,53 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
       qss = fmaf(hi, hi, qss);
     }
   }
-  if (a.normalize) {
+  if (has_row) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) qss += __shfl_xor_sync(0xffffffffu, qss, off);
-    if (lane == 0) s_part[warp] = qss;
-    cons_sync();
+    for (int j = 0; j < 4; ++j) {
+      const int wi = warp * wpw + lane + 32 * j;
+      if (lane + 32 * j < wpw && wi < nwords) {
+        const float s = bf16_bits_to_float(rsb[j] & 0xFFFFu), b = bf16_bits_to_float(rsb[j] >> 16);
+        const uint2 xv = __ldcg(reinterpret_cast<const uint2 *>(src) + wi);
+        const float xs[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
+                             __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float q = __uint_as_float(0x4B000000u | ((rq[j] >> (8 * i)) & 0xFFu)) - 8388608.0f;
+          lg = fmaf(fmaf(q, s, b), xs[i], lg);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    qss += __shfl_xor_sync(0xffffffffu, qss, off);
+    lg += __shfl_xor_sync(0xffffffffu, lg, off);
+  }
+  if (lane == 0) {
+    s_part[warp] = qss;
+    s_part[kCons + warp] = lg;
+  }
+  cons_sync();
+  float inv = 1.0f;
+  if (a.normalize) {
     float tot = 0.f;
+#pragma unroll
     for (int w = 0; w < kCons; ++w) tot += s_part[w];
-    const float inv = 1.0f / sqrtf(tot / (float)H + 1e-6f);
-    if (tid < nquart) {
+    inv = 1.0f / sqrtf(tot / (float)H + 1e-6f);
+  }
+  if (tid == 0) {
+    if (has_row) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCons; ++w) t += s_part[kCons + w];
+      a.logits[c] = t * inv + (a.w.logit_bias ? a.w.logit_bias[c] : 0.f);
+    }
+    // arrive at barrier 1 (the logit store above is this thread's own)
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar_count) : "memory");
+  }
+  // operand rows: normalised bf16 x -> permuted fp16, quarter and group sums
+  if (tid < nquart) {
+    if (a.normalize) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint16_t lb = float_to_bf16_bits(__uint_as_float(qin[i] << 16) * inv);
@@ -402,16 +440,10 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         qin[i] = (uint32_t)lb | ((uint32_t)hb << 16);
       }
     }
-    cons_sync();  // s_part is reused below
-  }
-  if (tid < nquart) {
-    uint4 *xn4 = reinterpret_cast<uint4 *>(xnat) + 2 * tid;
-    xn4[0] = make_uint4(qin[0], qin[1], qin[2], qin[3]);
-    xn4[1] = make_uint4(qin[4], qin[5], qin[6], qin[7]);
     if (c == 0 && a.xn_user) {
       uint4 *xu = reinterpret_cast<uint4 *>(a.xn_user) + 2 * tid;
-      xu[0] = xn4[0];
-      xu[1] = xn4[1];
+      xu[0] = make_uint4(qin[0], qin[1], qin[2], qin[3]);
+      xu[1] = make_uint4(qin[4], qin[5], qin[6], qin[7]);
     }
     uint32_t out[8];
     operand_quarter<true>(qin, out);  // bf16 x -> fp16 B operand
@@ -428,36 +460,10 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   }
   cons_sync();
   if (tid < G) xsum[tid] = ((qsum[4 * tid] + qsum[4 * tid + 1]) + qsum[4 * tid + 2]) + qsum[4 * tid + 3];
-  float lg = 0.f;
-  if (has_row) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int wi = warp * wpw + lane + 32 * j;
-      if (lane + 32 * j < wpw && wi < nwords) {
-        const float s = bf16_bits_to_float(rsb[j] & 0xFFFFu), b = bf16_bits_to_float(rsb[j] >> 16);
-        const uint2 xv = *reinterpret_cast<const uint2 *>(xnat + 4 * wi);
-        const float xs[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
-                             __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float q = __uint_as_float(0x4B000000u | ((rq[j] >> (8 * i)) & 0xFFu)) - 8388608.0f;
-          lg = fmaf(fmaf(q, s, b), xs[i], lg);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lg += __shfl_xor_sync(0xffffffffu, lg, off);
-  if (lane == 0) s_part[warp] = lg;
   cons_sync();
-  if (tid == 0 && has_row) {
-    float t = 0.f;
-    for (int w = 0; w < kCons; ++w) t += s_part[w];
-    a.logits[c] = t + (a.w.logit_bias ? a.w.logit_bias[c] : 0.f);
-  }
 
-  // ---- phase 2: arrive at the grid barrier; compute this block's shared
-  // gate/up units (their tiles and x are here) while the routing completes
+  // ---- phase 2: compute this block's shared gate/up units (their tiles and
+  // x are here) while barrier 1 completes
   const int r = lane >> 2, cq = lane & 3;
   int it = 0;
   bool ok = true;
@@ -507,7 +513,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     return true;
   };
 
-  grid_arrive(bar_count);
   for (; it < n_sh_mine && ok; ++it) ok = gu_unit(it);
   if (!grid_wait(bar_count, base + nb, a.err, &s_flag[0]) || !ok) {
     if (tid == 0) {
@@ -520,68 +525,73 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     }
     return;
   }
-  // ---- top-k, in every block: rank of logit i = number of logits above it
-  // (ties: lower id first); ranks below k are the selection, in order
-  {
-    unsigned *s_key = reinterpret_cast<unsigned *>(sred);  // [kMaxExperts]; 0 past E (below every key)
-    float *s_val = sred + kMaxExperts;                      // [k]
-    if (tid < kMaxExperts) {
-      unsigned key = 0u;
-      if (tid < E) {
-        float x = __ldcg(a.logits + tid);
-        if (!isfinite(x)) {
-          x = -INFINITY;
-          if (c == 0) set_error(a.err, kErrNonFinite);
-        }
-        key = ord_key(x);
-      }
-      s_key[tid] = key;
-    }
-    cons_sync();
-    const int i = tid >> 2, part = tid & 3;  // 4 threads per logit, 32 candidates each
-    int rank = 0;
-    const unsigned ki = s_key[i];
+  // ---- top-k, in warp 0 of every block: lane l holds the keys of experts
+  // 4l .. 4l+3 sorted (larger first, equal keys lower id first); each round
+  // takes the warp maximum of the lanes' heads, the lowest lane holding it
+  // (= the lowest id among equal keys) pops its head.  The softmax terms
+  // accumulate as the values come out, in selection order.
+  if (warp == 0) {
+    unsigned k0, k1, k2, k3;
+    bool bad = false;
     {
-      // the 32 candidates in registers first (eight 16-byte loads), then compared
-      // (the four parts start at different 16-byte chunks: no bank conflicts)
-      uint4 kv[8];
-      const uint4 *src4 = reinterpret_cast<const uint4 *>(s_key + 32 * part);
+      unsigned kq[4];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) kv[v] = src4[(v + 2 * part) & 7];
+      for (int i = 0; i < 4; ++i) {
+        const int e = 4 * lane + i;
+        kq[i] = 0u;  // below every real key: never picked while k <= E
+        if (e < E) {
+          float x = __ldcg(a.logits + e);
+          if (!isfinite(x)) {
+            x = -INFINITY;
+            bad = true;
+          }
+          kq[i] = ord_key(x);
+        }
+      }
+      k0 = kq[0]; k1 = kq[1]; k2 = kq[2]; k3 = kq[3];
+    }
+    if (c == 0 && bad) set_error(a.err, kErrNonFinite);
+    int i0 = 0, i1 = 1, i2 = 2, i3 = 3;
+    // (key descending, index ascending): ordered pairs need no swap
+    auto cswap = [](unsigned &ka, int &ia, unsigned &kb, int &ib) {
+      if (kb > ka || (kb == ka && ib < ia)) {
+        const unsigned tk = ka; ka = kb; kb = tk;
+        const int ti = ia; ia = ib; ib = ti;
+      }
+    };
+    cswap(k0, i0, k1, i1);
+    cswap(k2, i2, k3, i3);
+    cswap(k0, i0, k2, i2);
+    cswap(k1, i1, k3, i3);
+    cswap(k1, i1, k2, i2);
+    float v0 = 0.f, den = 0.f, myex = 0.f;
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const unsigned kk[4] = {kv[v].x, kv[v].y, kv[v].z, kv[v].w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int j = 32 * part + 4 * ((v + 2 * part) & 7) + w;
-          rank += (kk[w] > ki || (kk[w] == ki && j < i)) ? 1 : 0;
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k) {
+        const unsigned m = __reduce_max_sync(0xffffffffu, k0);
+        const int wl = __ffs(__ballot_sync(0xffffffffu, k0 == m)) - 1;
+        const float val = key_value(m);
+        if (j == 0) v0 = val;
+        const float ex = __expf(val - v0);
+        den += ex;
+        if (lane == j) myex = ex;
+        if (lane == wl) {
+          s_sel[j] = 4 * lane + i0;
+          k0 = k1; i0 = i1; k1 = k2; i1 = i2; k2 = k3; i2 = i3; k3 = 0u;
         }
       }
     }
-    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
-    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
-    if (i < E && part == 0 && rank < k) {
-      s_sel[rank] = i;
-      s_val[rank] = key_value(ki);
-    }
-    cons_sync();
-    if (warp == 0) {
-      float ex = 0.f;
-      if (lane < k) ex = __expf(s_val[lane] - s_val[0]);
-      float den = ex;
-#pragma unroll
-      for (int off = 1; off < 8; off <<= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-      if (lane < k) {
-        const float wj = ex / den;
-        s_w[lane] = wj;
-        if (c == 0) {
-          if (a.ids_user) a.ids_user[lane] = s_sel[lane];
-          if (a.wts_user) a.wts_user[lane] = wj;
-        }
+    __syncwarp();
+    if (lane < k) {
+      const float wj = myex / den;
+      s_w[lane] = wj;
+      if (c == 0) {
+        if (a.ids_user) a.ids_user[lane] = s_sel[lane];
+        if (a.wts_user) a.wts_user[lane] = wj;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(route, 0);  // routing known: producer may stream
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(route, 0);  // routing known: producer may stream
   }
   cons_sync();
   if (c == 0 && tid == 0) trace_max(a.trace, kTrLoaded);
