@@ -30,7 +30,7 @@ namespace moe {
 
 namespace {
 constexpr int kCons = 16;                    // consumer warps
-constexpr int kConsThreads = kCons * 32;     // 256
+constexpr int kConsThreads = kCons * 32;     // 512
 constexpr int kThreadsF = kConsThreads + 32; // + producer warp
 constexpr int kSlots = 3;                    // ring slots
 constexpr int kRowsU = 16;                   // rows per unit
@@ -206,7 +206,10 @@ __device__ __forceinline__ void down_item(const uint8_t *tile, const uint8_t *hp
 }
 }  // namespace
 
-size_t fused_decode_smem(const Dims &d) { return (size_t)fused_layout(d.H, d.I, d.k).total; }
+size_t fused_decode_smem(const Dims &d) {
+  if (d.H / 16 > kConsThreads) return 0;  // one 16-element quarter of x per consumer thread
+  return (size_t)fused_layout(d.H, d.I, d.k).total;
+}
 
 __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -284,6 +287,12 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         routed = true;
         if (!ok) break;
       }
+      // the down tiles wait until this block's last gate/up tile has landed,
+      // so they do not take HBM bandwidth from gate/up tiles still in flight
+      if (it == n_gu_mine && n_gu_mine > 0) {
+        ok = mbar_wait_idle(&full[(n_gu_mine - 1) % kSlots], ((n_gu_mine - 1) / kSlots) & 1);
+        if (!ok) break;
+      }
       if (is_gu) {
         const int r0 = rt * kRowsU;
         const uint8_t *blob = gslot == 0 ? a.w.shared : a.w.experts + (size_t)s_sel[gslot - 1] * a.w.stride;
@@ -334,19 +343,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   }
 
   // ============================================================ consumers
-  // router row of this block (expert e = c; E <= gridDim.x is checked on the host)
-  const int nwords = H / 4;
-  const int wpw = (nwords + kCons - 1) / kCons;  // words per warp
-  uint32_t rq[4], rsb[4];
+  // router row of this block (expert e = c; E <= gridDim.x is checked on the
+  // host), split like x below: thread t holds the 16 codes of elements
+  // 16t .. 16t+15 and the scale and bias of their group
+  const int nquart = H / 16;
   const bool has_row = c < E;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int wi = warp * wpw + lane + 32 * j;
-    if (has_row && lane + 32 * j < wpw && wi < nwords) {
-      rq[j] = __ldg(reinterpret_cast<const uint32_t *>(a.w.router_q + (size_t)c * H) + wi);
-      rsb[j] = (uint32_t)__ldg(a.w.router_s + (size_t)c * G + (wi >> 4)) |
-               ((uint32_t)__ldg(a.w.router_b + (size_t)c * G + (wi >> 4)) << 16);
-    }
+  uint4 rq = make_uint4(0u, 0u, 0u, 0u);
+  float rs = 0.f, rb = 0.f;
+  if (has_row && tid < nquart) {
+    rq = __ldg(reinterpret_cast<const uint4 *>(a.w.router_q + (size_t)c * H) + tid);
+    rs = bf16_bits_to_float(__ldg(a.w.router_s + (size_t)c * G + (tid >> 2)));
+    rb = bf16_bits_to_float(__ldg(a.w.router_b + (size_t)c * G + (tid >> 2)));
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -367,10 +374,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   }
 
   // ---- phase 1: x (one 16-element quarter per thread), its sum of squares
-  // and this block's router row against the raw input, in one pass: a single
-  // block reduction gives 1/rms and the dot product, so the logit
+  // and the router row's dot product with the raw input, in one pass: a
+  // single block reduction gives 1/rms and the dot product, so the logit
   // (dot * 1/rms) goes out before the operand rows are staged.
-  const int nquart = H / 16;
   uint32_t qin[8];
   float qss = 0.f, lg = 0.f;
   const uint16_t *src = a.normalize ? a.hres : a.x;
@@ -379,28 +385,18 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     const uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(src) + 2 * tid + 1);
     qin[0] = v0.x; qin[1] = v0.y; qin[2] = v0.z; qin[3] = v0.w;
     qin[4] = v1.x; qin[5] = v1.y; qin[6] = v1.z; qin[7] = v1.w;
+    const uint32_t rw[4] = {rq.x, rq.y, rq.z, rq.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float lo = __uint_as_float(qin[i] << 16), hi = __uint_as_float(qin[i] & 0xFFFF0000u);
       qss = fmaf(lo, lo, qss);
       qss = fmaf(hi, hi, qss);
-    }
-  }
-  if (has_row) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int wi = warp * wpw + lane + 32 * j;
-      if (lane + 32 * j < wpw && wi < nwords) {
-        const float s = bf16_bits_to_float(rsb[j] & 0xFFFFu), b = bf16_bits_to_float(rsb[j] >> 16);
-        const uint2 xv = __ldcg(reinterpret_cast<const uint2 *>(src) + wi);
-        const float xs[4] = {__uint_as_float(xv.x << 16), __uint_as_float(xv.x & 0xFFFF0000u),
-                             __uint_as_float(xv.y << 16), __uint_as_float(xv.y & 0xFFFF0000u)};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float q = __uint_as_float(0x4B000000u | ((rq[j] >> (8 * i)) & 0xFFu)) - 8388608.0f;
-          lg = fmaf(fmaf(q, s, b), xs[i], lg);
-        }
-      }
+      // codes of elements 2i, 2i+1: bytes 2i, 2i+1 of the quarter's 16 code bytes
+      const uint32_t w = rw[i >> 1] >> (16 * (i & 1));
+      const float qlo = __uint_as_float(0x4B000000u | (w & 0xFFu)) - 8388608.0f;
+      const float qhi = __uint_as_float(0x4B000000u | ((w >> 8) & 0xFFu)) - 8388608.0f;
+      lg = fmaf(fmaf(qlo, rs, rb), lo, lg);
+      lg = fmaf(fmaf(qhi, rs, rb), hi, lg);
     }
   }
 #pragma unroll
