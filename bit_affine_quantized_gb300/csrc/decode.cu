@@ -175,34 +175,44 @@ __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xpe
 }
 
 // One (expert slot, 64-wide group) item of a down unit: rows r, r+8 of the
-// 16-row tile, token column 0.  Returns the weighted partials.
-__device__ __forceinline__ void down_item(const uint8_t *tile, const uint8_t *hperm, const float *hsum,
-                                          const float *s_w, int s, int g, int r, int cq, int I, int GI, int dn_qp,
-                                          int dn_slot_bytes, float &t0, float &t2) {
-  const uint8_t *qb = tile + s * dn_slot_bytes + g * 32 + cq * 8;
-  const uint16_t *sb = reinterpret_cast<const uint16_t *>(tile + s * dn_slot_bytes + 16 * dn_qp);
-  const uint2 w0 = *reinterpret_cast<const uint2 *>(qb + r * dn_qp);
-  const uint2 w1 = *reinterpret_cast<const uint2 *>(qb + (r + 8) * dn_qp);
-  const uint8_t *hrow = hperm + (s * I + g * kGroup) * 2 + cq * 32;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int st = 0; st < 4; ++st) {
-    const uint2 bx = r == 0 ? *reinterpret_cast<const uint2 *>(hrow + st * 8) : make_uint2(0u, 0u);
-    const uint32_t x0 = (st >> 1) ? w0.y : w0.x, x1 = (st >> 1) ? w1.y : w1.x;
-    uint32_t A[4];
-    if ((st & 1) == 0) {
-      A[0] = codes_sub<0>(x0); A[1] = codes_sub<0>(x1); A[2] = codes_sub<1>(x0); A[3] = codes_sub<1>(x1);
-    } else {
-      A[0] = codes_sub<2>(x0); A[1] = codes_sub<2>(x1); A[2] = codes_sub<3>(x0); A[3] = codes_sub<3>(x1);
-    }
-    mma_f16(acc, A, bx.x, bx.y);
+// 16-row tile, token column 0 (valid in the lanes with cq == 0).
+//   tq   codes of the item in the tile, at this lane's 8 bytes (row 0)
+//   sq   scale of row 0 of the item (bf16); biases follow 16 rows later
+//   hq   the item's 64 operand values, at this lane's 32 bytes
+//   hsw  router weight of the item's expert times the group sum of h
+//   w24  router weight times 2^24 (undoes the code scale of the mma)
+// Accumulates weight * (s * sum(q h) + b * sum(h)) into t0 (row r) and t2
+// (row r + 8).
+__device__ __forceinline__ void down_item(const uint8_t *tq, const uint16_t *sq, const uint8_t *hq, float hsw,
+                                          float w24, int r, int qp_r0, int qp_r1, int GI, float &t0, float &t2) {
+  const uint2 w0 = *reinterpret_cast<const uint2 *>(tq + qp_r0);
+  const uint2 w1 = *reinterpret_cast<const uint2 *>(tq + qp_r1);
+  uint4 b01 = make_uint4(0u, 0u, 0u, 0u), b23 = make_uint4(0u, 0u, 0u, 0u);
+  if (r == 0) {
+    b01 = *reinterpret_cast<const uint4 *>(hq);
+    b23 = *reinterpret_cast<const uint4 *>(hq + 16);
   }
-  const float wt = s == 0 ? 1.0f : s_w[s - 1];
-  const float hs = hsum[s * GI + g];
-  const float s0 = bf16_bits_to_float(sb[r * GI + g]) * kCodeScale, b0 = bf16_bits_to_float(sb[16 * GI + r * GI + g]);
-  const float s1 = bf16_bits_to_float(sb[(r + 8) * GI + g]) * kCodeScale, b1 = bf16_bits_to_float(sb[16 * GI + (r + 8) * GI + g]);
-  t0 = fmaf(wt, fmaf(s0, acc[0], b0 * hs), t0);
-  t2 = fmaf(wt, fmaf(s1, acc[2], b1 * hs), t2);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    uint32_t A[4] = {codes_sub<0>(w0.x), codes_sub<0>(w1.x), codes_sub<1>(w0.x), codes_sub<1>(w1.x)};
+    mma_f16(acc, A, b01.x, b01.y);
+  }
+  {
+    uint32_t A[4] = {codes_sub<2>(w0.x), codes_sub<2>(w1.x), codes_sub<3>(w0.x), codes_sub<3>(w1.x)};
+    mma_f16(acc, A, b01.z, b01.w);
+  }
+  {
+    uint32_t A[4] = {codes_sub<0>(w0.y), codes_sub<0>(w1.y), codes_sub<1>(w0.y), codes_sub<1>(w1.y)};
+    mma_f16(acc, A, b23.x, b23.y);
+  }
+  {
+    uint32_t A[4] = {codes_sub<2>(w0.y), codes_sub<2>(w1.y), codes_sub<3>(w0.y), codes_sub<3>(w1.y)};
+    mma_f16(acc, A, b23.z, b23.w);
+  }
+  const float s0 = bf16_bits_to_float(sq[r * GI]), b0 = bf16_bits_to_float(sq[(16 + r) * GI]);
+  const float s1 = bf16_bits_to_float(sq[(r + 8) * GI]), b1 = bf16_bits_to_float(sq[(24 + r) * GI]);
+  t0 = fmaf(s0 * acc[0], w24, fmaf(b0, hsw, t0));
+  t2 = fmaf(s1 * acc[2], w24, fmaf(b1, hsw, t2));
 }
 }  // namespace
 
@@ -229,6 +239,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   int *s_sel = reinterpret_cast<int *>(smem + L.misc + 128);       // [kMaxTopK]
   float *s_w = reinterpret_cast<float *>(smem + L.misc + 160);     // [kMaxTopK]
   int *s_flag = reinterpret_cast<int *>(smem + L.misc + 192);      // [4]
+  float *s_w24 = reinterpret_cast<float *>(smem + L.misc + 320);   // [kMaxTopK + 1]
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.misc + 256);  // [3]
   uint64_t *empty = full + kSlots;                                     // [3]
   uint64_t *route = empty + kSlots;                                    // [1]
@@ -621,8 +632,14 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
       hq[q] = sum;
     }
     cons_sync();
-    for (int q = tid; q < S * GI; q += kConsThreads)
-      hsum[q] = ((hq[4 * q] + hq[4 * q + 1]) + hq[4 * q + 2]) + hq[4 * q + 3];
+    // per item: router weight of its expert times the group sum of h; per
+    // expert: the weight times 2^24 (the code scale the mma leaves in)
+    for (int q = tid; q < S * GI; q += kConsThreads) {
+      const int sl = q / GI;
+      const float wt = sl == 0 ? 1.0f : s_w[sl - 1];
+      hsum[q] = wt * (((hq[4 * q] + hq[4 * q + 1]) + hq[4 * q + 2]) + hq[4 * q + 3]);
+    }
+    if (tid < S) s_w24[tid] = (tid == 0 ? 1.0f : s_w[tid - 1]) * kCodeScale;
   }
   cons_sync();
   for (int jd = 0; jd < n_dn_mine; ++jd, ++it) {
@@ -636,26 +653,35 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     const int nitems = S * GI;
     const int per = (nitems + kCons - 1) / kCons;
     const int ib = warp * per, ie = min(nitems, ib + per);
-    // two independent accumulation chains per warp (items q and q+1); item
-    // q = (slot sa, group ga), advanced without divisions
+    // two independent accumulation chains per warp (items q and q+1); the
+    // item pointers advance by one group, or to the next expert's slice of
+    // the tile, without divisions
     float t0a = 0.f, t2a = 0.f, t0b = 0.f, t2b = 0.f;
-    int q = ib, sa = ib / GI, ga = ib - (ib / GI) * GI;
-    for (; q + 1 < ie; q += 2) {
-      int sb2 = sa, gb = ga + 1;
-      if (gb == GI) {
-        gb = 0;
-        ++sb2;
+    if (ib < ie) {
+      int sl = ib / GI, g = ib - (ib / GI) * GI;
+      const uint8_t *tq = tile + sl * L.dn_slot_bytes + g * 32 + cq * 8;
+      const uint16_t *sq = reinterpret_cast<const uint16_t *>(tile + sl * L.dn_slot_bytes + kRowsU * L.dn_qp) + g;
+      const int qp_r0 = r * L.dn_qp, qp_r1 = (r + 8) * L.dn_qp;
+      auto adv = [&]() {
+        ++g;
+        tq += 32;
+        ++sq;
+        if (g == GI) {
+          g = 0;
+          ++sl;
+          tq += L.dn_slot_bytes - GI * 32;
+          sq = reinterpret_cast<const uint16_t *>(reinterpret_cast<const uint8_t *>(sq) + L.dn_slot_bytes) - GI;
+        }
+      };
+      int q = ib;
+      for (; q + 1 < ie; q += 2) {
+        down_item(tq, sq, hperm + q * 128 + cq * 32, hsum[q], s_w24[sl], r, qp_r0, qp_r1, GI, t0a, t2a);
+        adv();
+        down_item(tq, sq, hperm + (q + 1) * 128 + cq * 32, hsum[q + 1], s_w24[sl], r, qp_r0, qp_r1, GI, t0b, t2b);
+        adv();
       }
-      down_item(tile, hperm, hsum, s_w, sa, ga, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0a, t2a);
-      down_item(tile, hperm, hsum, s_w, sb2, gb, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0b, t2b);
-      sa = sb2;
-      ga = gb + 1;
-      if (ga == GI) {
-        ga = 0;
-        ++sa;
-      }
+      if (q < ie) down_item(tq, sq, hperm + q * 128 + cq * 32, hsum[q], s_w24[sl], r, qp_r0, qp_r1, GI, t0a, t2a);
     }
-    if (q < ie) down_item(tile, hperm, hsum, s_w, sa, ga, r, cq, I, GI, L.dn_qp, L.dn_slot_bytes, t0a, t2a);
     if (cq == 0) {
       sred[warp * kRowsU + r] = t0a + t0b;
       sred[warp * kRowsU + r + 8] = t2a + t2b;
