@@ -44,6 +44,11 @@ constexpr size_t kSmemCap = 227 * 1024;
 constexpr size_t kSyncOffset = 256;
 constexpr size_t kPrefillSyncOffset = kSyncOffset + 16;
 constexpr size_t kDeviceWords = kSyncOffset + 64 + 1024;
+// kMboxOffset: the single-token kernel's logit mailboxes, [SM count][128]
+// 64-bit words (each launch tags its logits with its epoch; zero at start)
+constexpr size_t kMboxOffset = 1536;
+static_assert(kDeviceWords <= kMboxOffset, "mailboxes overlap the device words");
+size_t device_words(int n_sm) { return kMboxOffset + (size_t)n_sm * moe::kMaxExperts * 2; }
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -214,6 +219,7 @@ int run_fused(moe_handle *h, const moe_layer_weights *w, const void *x, void *hr
   a.hbuf = (__half *)(ws + L.h);
   a.y = (uint16_t *)y;
   a.sync = h->dwords + kSyncOffset;
+  a.mbox = reinterpret_cast<unsigned long long *>(h->dwords + kMboxOffset);
   a.err = h->dwords;
   a.trace = take_trace(h, 1);
   a.normalize = hres != nullptr;
@@ -318,11 +324,11 @@ int moe_create(moe_handle **out) {
   h->fused = !(fz && fz[0] == '0');
   const char *pz = getenv("MOE_PREFILL_FUSED");
   h->prefill = !(pz && pz[0] == '0');
-  if (cudaMalloc(&h->dwords, kDeviceWords * sizeof(unsigned)) != cudaSuccess) {
+  if (cudaMalloc(&h->dwords, device_words(h->n_sm) * sizeof(unsigned)) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
   }
-  if (cudaMemset(h->dwords, 0, kDeviceWords * sizeof(unsigned)) != cudaSuccess) {
+  if (cudaMemset(h->dwords, 0, device_words(h->n_sm) * sizeof(unsigned)) != cudaSuccess) {
     cudaFree(h->dwords);
     free(h);
     return MOE_ERR_CUDA;

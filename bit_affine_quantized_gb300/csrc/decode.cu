@@ -366,15 +366,19 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     rs = bf16_bits_to_float(__ldg(a.w.router_s + (size_t)c * G + (tid >> 2)));
     rb = bf16_bits_to_float(__ldg(a.w.router_b + (size_t)c * G + (tid >> 2)));
   }
+  const float lbias = has_row && a.w.logit_bias ? __ldg(a.w.logit_bias + c) : 0.f;
   pdl_wait();
   pdl_launch_dependents();
   if (c == 0 && tid == 0) trace_min(a.trace, kTrWaited);
-  // Barrier targets of this launch.  Every launch adds exactly 2*nb to the
-  // counter (two barriers); read after the dependency wait it is
-  // 2*nb*epoch + (arrivals of fast blocks at barrier 1, fewer than nb), so
-  // the epoch follows by division.
+  // Epoch of this launch.  Every launch adds exactly nb to the counter (one
+  // grid barrier); read after the dependency wait it is nb*epoch + (arrivals
+  // of fast blocks of this launch, fewer than nb: this block has not
+  // arrived), so the epoch follows by division.  It tags this launch's
+  // logits in the mailboxes.
   unsigned long long *bar_count = reinterpret_cast<unsigned long long *>(a.sync);
-  const unsigned long long base = (ld_acquire64(bar_count) / (2ull * nb)) * (2ull * nb);
+  const unsigned long long epoch = ld_acquire64(bar_count) / (unsigned long long)nb;
+  const unsigned long long base = epoch * (unsigned long long)nb;
+  const unsigned long long tag = (unsigned long long)(uint32_t)(epoch + 1ull) << 32;
 
   // Residual values of this block's down rows, needed only at the very end:
   // load them now.  Only this block writes these rows, after it read them.
@@ -420,6 +424,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     s_part[kCons + warp] = lg;
   }
   cons_sync();
+  // every thread forms 1/rms and the logit (same partials, same order)
   float inv = 1.0f;
   if (a.normalize) {
     float tot = 0.f;
@@ -427,15 +432,18 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     for (int w = 0; w < kCons; ++w) tot += s_part[w];
     inv = 1.0f / sqrtf(tot / (float)H + 1e-6f);
   }
-  if (tid == 0) {
-    if (has_row) {
-      float t = 0.f;
+  if (has_row) {
+    float t = 0.f;
 #pragma unroll
-      for (int w = 0; w < kCons; ++w) t += s_part[kCons + w];
-      a.logits[c] = t * inv + (a.w.logit_bias ? a.w.logit_bias[c] : 0.f);
-    }
-    // arrive at barrier 1 (the logit store above is this thread's own)
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar_count) : "memory");
+    for (int w = 0; w < kCons; ++w) t += s_part[kCons + w];
+    const float logit = t * inv + lbias;
+    // this launch's logit of expert c, tagged with the epoch, into every
+    // block's mailbox (one 8-byte store each: tag and value arrive together)
+    const unsigned long long v = tag | __float_as_uint(logit);
+    for (int b = tid; b < nb; b += kConsThreads)
+      asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a.mbox + (size_t)b * kMaxExperts + c), "l"(v)
+                   : "memory");
+    if (tid == 0) a.logits[c] = logit;
   }
   // operand rows: normalised bf16 x -> permuted fp16, quarter and group sums
   if (tid < nquart) {
@@ -521,22 +529,47 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   };
 
   for (; it < n_sh_mine && ok; ++it) ok = gu_unit(it);
-  if (!grid_wait(bar_count, base + nb, a.err, &s_flag[0]) || !ok) {
+  // ---- top-k, in warp 0 of every block, once this block's mailbox holds
+  // every logit of this launch (lane l polls experts 4l .. 4l+3); lane l
+  // holds the keys of experts 4l .. 4l+3 sorted (larger first, equal keys
+  // lower id first); each round
+  // takes the warp maximum of the lanes' heads, the lowest lane holding it
+  // (= the lowest id among equal keys) pops its head.  The softmax terms
+  // accumulate as the values come out, in selection order.
+  unsigned long long mv[4] = {0ull, 0ull, 0ull, 0ull};  // warp 0: the polled logits
+  if (warp == 0) {
+    bool got = ok;
+    if (got) {
+      const unsigned long long *mb = a.mbox + (size_t)c * kMaxExperts + 4 * lane;
+      const unsigned long long t0 = global_ns();
+      for (uint32_t pi = 0;; ++pi) {
+        asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(mv[0]), "=l"(mv[1]) : "l"(mb) : "memory");
+        asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(mv[2]), "=l"(mv[3]) : "l"(mb + 2) : "memory");
+        bool mine = true;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (4 * lane + i < E && (mv[i] & 0xFFFFFFFF00000000ull) != tag) mine = false;
+        if (__all_sync(0xffffffffu, mine)) break;
+        if ((pi & 7u) == 7u && __any_sync(0xffffffffu, global_ns() - t0 > kWaitLimitNs)) {
+          got = false;
+          break;
+        }
+      }
+    }
+    if (lane == 0) s_flag[0] = got ? 1 : 0;
+  }
+  cons_sync();
+  if (s_flag[0] == 0) {
     if (tid == 0) {
-      if (!ok) set_error(a.err, kErrTimeout);
+      set_error(a.err, kErrTimeout);
       s_flag[2] = 1;                     // no routing: the producer must not stream routed tiles
       mbar_arrive_expect_tx(route, 0);   // release it; it drains its copies and exits
-      // still count this block's second arrival: every launch moves the
-      // counter by exactly 2*nb
+      // still count this block's arrival: every launch moves the counter by
+      // exactly nb
       asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(bar_count) : "memory");
     }
     return;
   }
-  // ---- top-k, in warp 0 of every block: lane l holds the keys of experts
-  // 4l .. 4l+3 sorted (larger first, equal keys lower id first); each round
-  // takes the warp maximum of the lanes' heads, the lowest lane holding it
-  // (= the lowest id among equal keys) pops its head.  The softmax terms
-  // accumulate as the values come out, in selection order.
   if (warp == 0) {
     unsigned k0, k1, k2, k3;
     bool bad = false;
@@ -547,7 +580,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         const int e = 4 * lane + i;
         kq[i] = 0u;  // below every real key: never picked while k <= E
         if (e < E) {
-          float x = __ldcg(a.logits + e);
+          float x = __uint_as_float((uint32_t)mv[i]);
           if (!isfinite(x)) {
             x = -INFINITY;
             bad = true;
@@ -608,7 +641,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   if (!ok) set_error(a.err, kErrTimeout);
 
   // ---- phase 4: grid barrier (all of h written), then the down units
-  if (!grid_sync(bar_count, base + 2ull * nb, a.err, &s_flag[1]) || !ok) return;
+  if (!grid_sync(bar_count, base + nb, a.err, &s_flag[1]) || !ok) return;
   // stage every expert's h row (permuted fp16) one 16-wide quarter per
   // thread (all loads in one round), then the group sums in quarter order
   {

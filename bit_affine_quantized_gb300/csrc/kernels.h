@@ -64,6 +64,7 @@ struct DecodeArgs {
   __half *hbuf;             // fp16 [k+1, I]: slot 0 shared, slot j+1 = j-th selected
   uint16_t *y;              // nullable bf16 [H]
   unsigned *sync;           // 64-bit grid barrier counter (this kernel's own)
+  unsigned long long *mbox; // [grid][kMaxExperts] epoch-tagged logits, zero-initialised, this kernel's own
   unsigned *err;
   unsigned long long *trace;
   int normalize;

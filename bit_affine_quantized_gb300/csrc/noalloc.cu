@@ -7,8 +7,9 @@
 // and outputs, but cannot give this library a workspace or create a handle.
 // This entry point keeps the scratch of the fused single-token kernel (the
 // expert activations h, the logits when the caller passes none, the grid
-// barrier counter and the device error word) in one file-scope device array
-// and calls no cudaMalloc, cudaFree or allocating library routine.
+// barrier counter, the logit mailboxes and the device error word) in
+// file-scope device arrays and calls no cudaMalloc, cudaFree or allocating
+// library routine.
 #include <mutex>
 
 #include "kernels.h"
@@ -18,19 +19,24 @@ namespace {
 
 // Scratch shared by every call on a device (it lives until the process exits):
 //   [0, 256)      device error word (cleared by every call, not reported)
-//   [256, 512)    grid-barrier arrival counter (cleared by every call)
+//   [256, 512)    grid-barrier arrival counter (zero at load; it only grows:
+//                 its value gives each launch the epoch that tags its logits)
 //   [512, 1024)   logits when the caller passes none: fp32 [E], E <= 128
 //   [1024, 16 KiB) expert activations h: fp16 [(top_k + 1) * inter]
 //                  (the target model, top-8 of inter 704, needs 12,672 B)
 constexpr size_t kScratchBytes = 16 * 1024;
 constexpr size_t kErrOff = 0, kBarOff = 256, kLogitsOff = 512, kHOff = 1024;
 __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
+// logit mailboxes of the fused kernel: [grid][128] epoch-tagged 64-bit words
+constexpr int kMaxStaticSm = 160;
+__device__ __align__(256) unsigned long long g_static_mbox[kMaxStaticSm * moe::kMaxExperts];
 
 // The array's name is a host-side stand-in in host code: its device address
 // is looked up once per device, with that device current.
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 unsigned char *g_scratch_ptr[kMaxDevices];
+unsigned long long *g_mbox_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 
 int setup_device(int dev, unsigned char **ptr, int *n_sm) {
@@ -45,6 +51,9 @@ int setup_device(int dev, unsigned char **ptr, int *n_sm) {
     if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    void *mb = nullptr;
+    if (cudaGetSymbolAddress(&mb, g_static_mbox) != cudaSuccess || !mb) return MOE_ERR_CUDA;
+    g_mbox_ptr[dev] = static_cast<unsigned long long *>(mb);
     if (moe::decode_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
     g_sm_count[dev] = sms;
     g_scratch_ptr[dev] = static_cast<unsigned char *>(p);
@@ -86,12 +95,12 @@ extern "C" int moe_layer_forward_static(const void *x, const moe_layer_weights *
   if ((st = setup_device(dev, &scratch, &n_sm)) != MOE_OK) return st;
   const moe::Dims d{w->dims.hidden, w->dims.inter, w->dims.n_experts, w->dims.top_k, 1};
   // the fused kernel's own limits: one router row per block, one block per SM
-  if (w->dims.n_experts > n_sm || n_sm > 1024 || moe::fused_decode_smem(d) > 227 * 1024 ||
+  if (w->dims.n_experts > n_sm || n_sm > kMaxStaticSm || moe::fused_decode_smem(d) > 227 * 1024 ||
       moe::decode_blocks_per_sm(d) < 1)
     return MOE_ERR_UNSUPPORTED;
 
-  // error word and barrier counter ([0, 512)) start at zero for every call
-  if (cudaMemsetAsync(scratch + kErrOff, 0, kLogitsOff - kErrOff, (cudaStream_t)stream) != cudaSuccess)
+  // the error word starts at zero for every call
+  if (cudaMemsetAsync(scratch + kErrOff, 0, kBarOff - kErrOff, (cudaStream_t)stream) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   moe::DecodeArgs a;
@@ -115,6 +124,7 @@ extern "C" int moe_layer_forward_static(const void *x, const moe_layer_weights *
   a.hbuf = reinterpret_cast<__half *>(scratch + kHOff);
   a.y = (uint16_t *)y;
   a.sync = reinterpret_cast<unsigned *>(scratch + kBarOff);
+  a.mbox = g_mbox_ptr[dev];
   a.err = reinterpret_cast<unsigned *>(scratch + kErrOff);
   a.trace = nullptr;
   a.normalize = 0;
