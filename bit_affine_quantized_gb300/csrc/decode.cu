@@ -604,21 +604,37 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     cswap(k0, i0, k2, i2);
     cswap(k1, i1, k3, i3);
     cswap(k1, i1, k2, i2);
-    float v0 = 0.f, den = 0.f, myex = 0.f;
+    // all kMaxTopK rounds run (k <= E; rounds past k pick unused entries);
+    // the winner of a round is the lowest lane whose head equals the maximum
+    unsigned mk[kMaxTopK];
+    unsigned lt_mask;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt_mask));
+    // local indices packed one per byte, popped with a shift; the pop is
+    // branch-free (selects), only the winner's store is predicated
+    unsigned idx = (unsigned)i0 | ((unsigned)i1 << 8) | ((unsigned)i2 << 16) | ((unsigned)i3 << 24);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      const unsigned m = __reduce_max_sync(0xffffffffu, k0);
+      const bool eq = k0 == m;
+      const unsigned bal = __ballot_sync(0xffffffffu, eq);
+      const bool win = eq && (bal & lt_mask) == 0u;
+      mk[j] = m;
+      if (win) s_sel[j] = 4 * lane + (int)(idx & 0xFFu);
+      k0 = win ? k1 : k0;
+      k1 = win ? k2 : k1;
+      k2 = win ? k3 : k2;
+      k3 = win ? 0u : k3;
+      idx = win ? idx >> 8 : idx;
+    }
+    // softmax over the k selected values, in selection order
+    const float v0 = key_value(mk[0]);
+    float den = 0.f, myex = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j < k) {
-        const unsigned m = __reduce_max_sync(0xffffffffu, k0);
-        const int wl = __ffs(__ballot_sync(0xffffffffu, k0 == m)) - 1;
-        const float val = key_value(m);
-        if (j == 0) v0 = val;
-        const float ex = __expf(val - v0);
+        const float ex = __expf(key_value(mk[j]) - v0);
         den += ex;
         if (lane == j) myex = ex;
-        if (lane == wl) {
-          s_sel[j] = 4 * lane + i0;
-          k0 = k1; i0 = i1; k1 = k2; i1 = i2; k2 = k3; i2 = i3; k3 = 0u;
-        }
       }
     }
     __syncwarp();
