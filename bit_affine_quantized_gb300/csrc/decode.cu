@@ -383,9 +383,9 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   // Residual values of this block's down rows, needed only at the very end:
   // load them now.  Only this block writes these rows, after it read them.
   uint32_t hres_pre0 = 0, hres_pre1 = 0;
-  if (a.hres && tid < kRowsU) {
-    if (n_dn_mine > 0) hres_pre0 = a.hres[c_dn * kRowsU + tid];
-    if (n_dn_mine > 1) hres_pre1 = a.hres[(c_dn + nb) * kRowsU + tid];
+  if (a.hres && warp == kCons - 1 && lane < kRowsU) {  // the warp that runs the down epilogue
+    if (n_dn_mine > 0) hres_pre0 = a.hres[c_dn * kRowsU + lane];
+    if (n_dn_mine > 1) hres_pre1 = a.hres[(c_dn + nb) * kRowsU + lane];
   }
 
   // ---- phase 1: x (one 16-element quarter per thread), its sum of squares
@@ -505,26 +505,29 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     }
     if (g < G) gu_group(tile, xperm, xsum, g, r, cq, G, L.gu_qp, tg0a, tg2a, tu0a, tu2a);
     if (cq == 0) {
-      float *red = sred + warp * 64;
+      float *red = sred + (it & 1) * (kCons * 64) + warp * 64;
       red[r] = tg0a + tg0b;
       red[r + 8] = tg2a + tg2b;
       red[16 + r] = tu0a + tu0b;
       red[16 + r + 8] = tu2a + tu2b;
     }
     cons_sync();
-    if (tid < kRowsU) {
+    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);  // every warp is done with the tile
+    // epilogue in the last warp (the fewest groups), from this unit's half
+    // of sred: the next unit writes the other half, the one after waits for
+    // this warp at its own cons_sync
+    if (warp == kCons - 1 && lane < kRowsU) {
+      const float *rd = sred + (it & 1) * (kCons * 64);
       float gs = 0.f, us = 0.f;
 #pragma unroll
       for (int w = 0; w < kCons; ++w) {
-        gs += sred[w * 64 + tid];
-        us += sred[w * 64 + 16 + tid];
+        gs += rd[w * 64 + lane];
+        us += rd[w * 64 + 16 + lane];
       }
       const float hv = gelu_tanh_f(gs) * us;
       if (!(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
-      a.hbuf[(size_t)gslot * I + rt * kRowsU + quad_row(tid)] = __float2half_rn(hv);  // tid: mma row
+      a.hbuf[(size_t)gslot * I + rt * kRowsU + quad_row(lane)] = __float2half_rn(hv);  // lane: mma row
     }
-    cons_sync();
-    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);  // slot free
     return true;
   };
 
@@ -731,24 +734,25 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
       }
       if (q < ie) down_item(tq, sq, hperm + q * 128 + cq * 32, hsum[q], s_w24[sl], r, qp_r0, qp_r1, GI, t0a, t2a);
     }
+    float *red = sred + (jd & 1) * (kCons * kRowsU);
     if (cq == 0) {
-      sred[warp * kRowsU + r] = t0a + t0b;
-      sred[warp * kRowsU + r + 8] = t2a + t2b;
+      red[warp * kRowsU + r] = t0a + t0b;
+      red[warp * kRowsU + r + 8] = t2a + t2b;
     }
     cons_sync();
-    if (tid < kRowsU) {
+    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);  // every warp is done with the tile
+    // epilogue in the last warp (the fewest items), from this unit's half of sred
+    if (warp == kCons - 1 && lane < kRowsU) {
       float y = 0.f;
 #pragma unroll
-      for (int w = 0; w < kCons; ++w) y += sred[w * kRowsU + tid];
+      for (int w = 0; w < kCons; ++w) y += red[w * kRowsU + lane];
       const uint16_t yb = float_to_bf16_bits(y);
-      if (a.y) a.y[n0 + tid] = yb;
+      if (a.y) a.y[n0 + lane] = yb;
       if (a.hres) {
-        const uint32_t hb = jd == 0 ? hres_pre0 : jd == 1 ? hres_pre1 : a.hres[n0 + tid];
-        a.hres[n0 + tid] = float_to_bf16_bits(bf16_bits_to_float(hb) + bf16_bits_to_float(yb));
+        const uint32_t hb = jd == 0 ? hres_pre0 : jd == 1 ? hres_pre1 : a.hres[n0 + lane];
+        a.hres[n0 + lane] = float_to_bf16_bits(bf16_bits_to_float(hb) + bf16_bits_to_float(yb));
       }
     }
-    cons_sync();
-    if (tid == 0) mbar_arrive_expect_tx(&empty[slot], 0);
   }
   if (tid == 0) trace_max(a.trace, kTrExit);
 }
