@@ -298,12 +298,6 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         routed = true;
         if (!ok) break;
       }
-      // the down tiles wait until this block's last gate/up tile has landed,
-      // so they do not take HBM bandwidth from gate/up tiles still in flight
-      if (it == n_gu_mine && n_gu_mine > 0) {
-        ok = mbar_wait_idle(&full[(n_gu_mine - 1) % kSlots], ((n_gu_mine - 1) / kSlots) & 1);
-        if (!ok) break;
-      }
       if (is_gu) {
         const int r0 = rt * kRowsU;
         const uint8_t *blob = gslot == 0 ? a.w.shared : a.w.experts + (size_t)s_sel[gslot - 1] * a.w.stride;
