@@ -83,6 +83,7 @@ def load_library(path: str = LIB_PATH):
         "moe_selftest_wait_timeout": (I, [V, ctypes.c_ulonglong, V]),
         "moe_set_trace": (I, [V, V, I]),
         "moe_layer_forward_static": (I, [V, P(LayerWeights), V, V, V, V, V]),
+        "moe_layer_forward_stack": (I, [V, V, I, P(LayerWeights), V, Z, V]),
         "moe_get_error": (I, [V, P(I)]),
     }
     for name, (res, args) in proto.items():
@@ -203,6 +204,14 @@ class Moe:
                                                         _ptr(x_out), _ptr(ids_out), _ptr(logits_out), _ptr(ws),
                                                         ws.numel() * ws.element_size(), _stream(stream)),
                     "moe_layer_forward_residual")
+
+    def layer_forward_stack(self, hidden, layers, ws, stream=None):
+        """Single-token layers of a residual stack in one call (hidden bf16 [H]
+        updated in place); `layers` is a sequence of LayerWeights."""
+        arr = (LayerWeights * len(layers))(*layers)
+        self._check(self.lib.moe_layer_forward_stack(self.h, _ptr(hidden), len(layers), arr, _ptr(ws),
+                                                     ws.numel() * ws.element_size(), _stream(stream)),
+                    "moe_layer_forward_stack")
 
     def set_trace(self, buffer=None, n_launches: int = 0):
         """Record per-launch device timestamps into `buffer` (u64 x 4 x n)."""

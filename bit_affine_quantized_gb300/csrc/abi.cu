@@ -462,6 +462,21 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens, const 
   return run_ffn(h, w, n_tokens, wsb + L.xn, routing_in(wsb, L), 1, y_out, hidden, wsb, (cudaStream_t)stream);
 }
 
+int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe_layer_weights *layers, void *ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  if (!h || !hidden || !layers || n_layers < 1) return MOE_ERR_INVALID_ARG;
+  int st;
+  for (int l = 0; l < n_layers; ++l) {
+    if ((st = check_weights_impl(&layers[l]))) return st;
+    if (memcmp(&layers[l].dims, &layers[0].dims, sizeof(moe_dims)) != 0) return MOE_ERR_INVALID_ARG;
+  }
+  for (int l = 0; l < n_layers; ++l)
+    if ((st = moe_layer_forward_residual(h, hidden, 1, &layers[l], nullptr, nullptr, nullptr, nullptr, ws, ws_bytes,
+                                         stream)))
+      return st;
+  return MOE_OK;
+}
+
 int moe_set_trace(moe_handle *h, unsigned long long *buffer, int n_launches) {
   if (!h || (buffer && n_launches < 1) || (buffer && !aligned(buffer, 8))) return MOE_ERR_INVALID_ARG;
   h->trace = buffer;

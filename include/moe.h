@@ -187,6 +187,18 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
                                int32_t *ids_out, float *logits_out, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* n_layers single-token layers of a residual stack in one call (the decode
+ * step of the section "Decode": every layer's router input is the residual
+ * stream normalised, its block output is added back):
+ *   for l in 0 .. n_layers-1:  hidden <- bf16(hidden + MoE_l(rmsnorm(hidden)))
+ * with MoE_l the block of layers[l] (all with the same dims); the same
+ * launches as n_layers calls of moe_layer_forward_residual with n_tokens = 1.
+ *   hidden   bf16 [H] in/out;  layers: host array of n_layers weight sets;
+ *   ws       workspace of moe_workspace_bytes(dims, 1)
+ * Validates every layer before the first launch; capturable. */
+int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe_layer_weights *layers,
+                            void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Single-token layer call that allocates nothing (the pages have no
  * counterpart: it exists for hosts that cannot allocate device memory,
  * e.g. a program whose own pool owns the whole device, or a per-token loop
@@ -203,8 +215,9 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
  * conditions (n_experts <= SM count, its shared memory fits); otherwise
  * MOE_ERR_UNSUPPORTED and nothing is launched.  The first call on a device
  * looks up the array's device address and sets kernel attributes, so make
- * it before any stream capture.  Every call clears the counter and error
- * word, then launches; the array keeps the last call's contents.  Calls
+ * it before any stream capture.  Every call clears the error word, then
+ * launches; the grid-barrier counter only grows (its value gives each launch
+ * the epoch that tags its logits); the array keeps the last call's contents.  Calls
  * that overlap on the GPU (different streams, or the same array from two
  * threads) race on the shared scratch.  Device-side error flags of this
  * call (bounded-wait timeouts, non-finite logits) are not reported. */

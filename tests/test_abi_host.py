@@ -80,6 +80,9 @@ def test_calls_without_handle_are_rejected(lib):
                                  1 << 30, None) == bq.MOE_ERR_INVALID_ARG
     assert lib.moe_route_sort(None, V(1 << 40), 1, ctypes.byref(d), V(16), V(16), V(16), V(16),
                               None) == bq.MOE_ERR_INVALID_ARG
+    layers = (bq.LayerWeights * 2)(w, w)
+    assert lib.moe_layer_forward_stack(None, V(1 << 40), 2, layers, V(1 << 40), 1 << 30,
+                                       None) == bq.MOE_ERR_INVALID_ARG
     assert lib.moe_get_error(None, None) == bq.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == bq.MOE_ERR_INVALID_ARG
 

@@ -110,3 +110,43 @@ def test_prefill_stack_30_layers(stack):
     against the oracle."""
     results = _run_stack(stack, 128, 1, zipf=True)
     _check_step(stack, results[0], 128, True, sampled={0, 29})
+
+
+def _stack_vs_layers(stack, n_layers: int, steps: int):
+    moe = bq.Moe()
+    ws_list = [_weights(L, False) for L in stack[:n_layers]]
+    ws = torch.empty(moe.workspace_bytes(ws_list[0].dims, 1), dtype=torch.uint8, device="cuda")
+    h_ref = torch.empty((1, H), dtype=torch.int16, device="cuda")
+    h_st = torch.empty_like(h_ref)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        h_st.copy_(to_dev_bf16(hidden(1000, 0, 1, rms=False)))
+        moe.layer_forward_stack(h_st, ws_list, ws, stream=stream)  # warm the path outside the capture
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            moe.layer_forward_stack(h_st, ws_list, ws, stream=stream)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        h0 = to_dev_bf16(hidden(1000, s, 1, rms=False))
+        with torch.cuda.stream(stream):
+            h_ref.copy_(h0)
+            for w in ws_list:
+                moe.layer_forward_residual(h_ref, 1, w, ws, stream=stream)
+            h_st.copy_(h0)
+            graph.replay()
+        torch.cuda.synchronize()
+        assert moe.get_error() == bq.MOE_OK
+        assert torch.equal(h_ref, h_st), f"step {s}: the stack call differs from the layer calls"
+    moe.close()
+
+
+def test_stack_call_30_layers_matches_layer_calls(stack):
+    """moe_layer_forward_stack (one call for the decode step, captured in a
+    graph) against 30 moe_layer_forward_residual calls: bit-identical
+    residual streams over 3 replays."""
+    _stack_vs_layers(stack, N_LAYERS, 3)
+
+
+@pytest.mark.parametrize("n_layers", [1, 2, 5])
+def test_stack_call_short_stacks(stack, n_layers):
+    _stack_vs_layers(stack, n_layers, 2)
