@@ -109,7 +109,7 @@ WsLayout ws_layout(const moe_dims &d, int T) {
   L.h = take(((size_t)T * k + T) * I * 2);
   L.o = moe::use_down_decode(to_dims(d, T)) ? off : take(((size_t)T * k + T) * H * 4);
   // quarter sums of the fused prefill kernel (its operand rows reuse xn and h)
-  L.xq = T > 1 ? take((size_t)T * (H / 16) * 4) : off;
+  L.xq = T > 1 ? take((size_t)T * 4 * ((H / 64 + 15) & ~(size_t)15)) : off;  // x group sums, bf16 hi/lo
   L.hq = T > 1 ? take(((size_t)T * k + T) * (I / 16) * 4) : off;
   L.total = off;
   return L;
@@ -252,7 +252,7 @@ int run_prefill(moe_handle *h, const moe_layer_weights *w, int T, const void *x,
   a.wts_user = wts;
   a.r = routing_in(ws, L);
   a.xperm = (__half *)(ws + L.xn);
-  a.xq = (float *)(ws + L.xq);
+  a.xs = (uint16_t *)(ws + L.xq);
   a.hperm = (__half *)(ws + L.h);
   a.hq = (float *)(ws + L.hq);
   a.obuf = (float *)(ws + L.o);

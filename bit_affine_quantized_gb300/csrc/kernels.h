@@ -82,7 +82,7 @@ struct PrefillArgs {
   float *wts_user;          // nullable [T, k]
   Routing r;                // ids, wts used
   __half *xperm;            // fp16 [T, H] permuted operand rows
-  float *xq;                // fp32 [T, H/16] quarter sums of x
+  uint16_t *xs;             // bf16 [T][2][G rounded up to 16]: group sums of x, hi and lo parts
   __half *hperm;            // fp16 [T*k + T, I] permuted h rows per sorted position
   float *hq;                // fp32 [T*k + T, I/16] quarter sums of h
   float *obuf;              // fp32 [T*k + T, H] weighted expert outputs

@@ -63,7 +63,8 @@ __host__ __device__ inline int qsum_pitch(int n) { return n + ((4 - n % 16) + 16
 struct PL {
   int G, GI, nrt, nrt_dn, n_mt;
   int gu_qp, rt_qp, dn_qp, wslot;   // W slot: gate/up 4-row block pitch, code row pitches, slot bytes
-  int xp, xqp, x_xq;                // X as gate/up operand: row pitch (B), quarter-sum pitch (floats), offset
+  int xp, gp, x_xs;                 // X as gate/up operand: row pitch (B); group sums as bf16 hi/lo
+                                    // [2][gp] per token (gp = G rounded up to 16, zero padded), offset
   int hp, hqp, x_hq;                // X as down operand
   int rx_q, rx_sb;                  // X as router operand: quarter sums after the fp16 row, then the
                                     // router's scales and biases (bf16 [16 n_mt][G] each)
@@ -91,14 +92,14 @@ __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) 
   const int dn = kDnRows * L.dn_qp + 2 * kDnRows * L.GI * 2;
   L.wslot = al16(imax(gu, imax(rt, dn)));
   L.xp = 2 * H + 16;
-  L.xqp = qsum_pitch(H / 16);
-  L.x_xq = kTC * L.xp;
+  L.gp = (L.G + 15) & ~15;
+  L.x_xs = kTC * L.xp;
   L.hp = 2 * I + 16;
   L.hqp = qsum_pitch(I / 16);
   L.x_hq = kTC * L.hp;
   L.rx_q = 2 * H;
   L.rx_sb = al16(L.rx_q + (H / 16) * 4);
-  L.xbuf = al16(imax(L.x_xq + kTC * L.xqp * 4, imax(L.x_hq + kTC * L.hqp * 4, L.rx_sb + 2 * kRtRows * L.n_mt * L.G * 2)));
+  L.xbuf = al16(imax(L.x_xs + kTC * 4 * L.gp, imax(L.x_hq + kTC * L.hqp * 4, L.rx_sb + 2 * kRtRows * L.n_mt * L.G * 2)));
   int o = 0;
   L.ring = o;
   o += kWSlots * L.wslot;
@@ -161,10 +162,12 @@ __device__ __forceinline__ void rt_group(const uint8_t *tile, const uint8_t *rx,
             fmaf(bf16_bits_to_float(rs[sr1 * G + g]) * kCodeScale, acc[2], t1));
 }
 
-// Gate/up: one 64-wide group for an 8-token tile: mma rows r, r+8 (tile rows
-// quad_row(r), quad_row(r + 8)) of gate and up, token columns 2cq, 2cq+1.
-__device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xrows, const float *xq, int qp, int xp,
-                                         int xqp, int G, int g, int r, int cq, float (&tg)[4], float (&tu)[4]) {
+// One 64-wide group of a gate/up unit for the chunk's 8 tokens: mma rows r,
+// r+8 (tile rows quad_row(r), quad_row(r) + 2), token columns 2cq, 2cq+1.
+// Accumulates the scaled code products s*acc per row and token; the bias
+// terms b*sum(x) of all groups come from gu_bias once per unit.
+__device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xrows, int qp, int xp, int G, int g,
+                                         int r, int cq, float (&tg)[4], float (&tu)[4]) {
   const int rowb = G * 32;                    // bytes of one row of codes (H / 2)
   const int sr0 = quad_row(r), sr1 = sr0 + 2;  // tile rows of mma rows r and r + 8
   const uint16_t *raw = reinterpret_cast<const uint16_t *>(tile + 8 * qp);  // gs, gb, us, ub [16][G]
@@ -192,21 +195,55 @@ __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xro
     mma_f16(ag, A, bb[2 * s], bb[2 * s + 1]);
     mma_f16(au, B, bb[2 * s], bb[2 * s + 1]);
   }
-  const float4 q0 = *reinterpret_cast<const float4 *>(xq + (2 * cq) * xqp + 4 * g);
-  const float4 q1 = *reinterpret_cast<const float4 *>(xq + (2 * cq + 1) * xqp + 4 * g);
-  const float xs0 = ((q0.x + q0.y) + q0.z) + q0.w, xs1 = ((q1.x + q1.y) + q1.z) + q1.w;
-  const float sg0 = bf16_bits_to_float(raw[sr0 * G + g]) * kCodeScale, bg0 = bf16_bits_to_float(raw[16 * G + sr0 * G + g]);
-  const float sg1 = bf16_bits_to_float(raw[sr1 * G + g]) * kCodeScale, bg1 = bf16_bits_to_float(raw[16 * G + sr1 * G + g]);
-  const float su0 = bf16_bits_to_float(raw[32 * G + sr0 * G + g]) * kCodeScale, bu0 = bf16_bits_to_float(raw[48 * G + sr0 * G + g]);
-  const float su1 = bf16_bits_to_float(raw[32 * G + sr1 * G + g]) * kCodeScale, bu1 = bf16_bits_to_float(raw[48 * G + sr1 * G + g]);
-  tg[0] = fmaf(bg0, xs0, fmaf(sg0, ag[0], tg[0]));
-  tg[1] = fmaf(bg0, xs1, fmaf(sg0, ag[1], tg[1]));
-  tg[2] = fmaf(bg1, xs0, fmaf(sg1, ag[2], tg[2]));
-  tg[3] = fmaf(bg1, xs1, fmaf(sg1, ag[3], tg[3]));
-  tu[0] = fmaf(bu0, xs0, fmaf(su0, au[0], tu[0]));
-  tu[1] = fmaf(bu0, xs1, fmaf(su0, au[1], tu[1]));
-  tu[2] = fmaf(bu1, xs0, fmaf(su1, au[2], tu[2]));
-  tu[3] = fmaf(bu1, xs1, fmaf(su1, au[3], tu[3]));
+  const float sg0 = bf16_bits_to_float(raw[sr0 * G + g]) * kCodeScale;
+  const float sg1 = bf16_bits_to_float(raw[sr1 * G + g]) * kCodeScale;
+  const float su0 = bf16_bits_to_float(raw[32 * G + sr0 * G + g]) * kCodeScale;
+  const float su1 = bf16_bits_to_float(raw[32 * G + sr1 * G + g]) * kCodeScale;
+  tg[0] = fmaf(sg0, ag[0], tg[0]);
+  tg[1] = fmaf(sg0, ag[1], tg[1]);
+  tg[2] = fmaf(sg1, ag[2], tg[2]);
+  tg[3] = fmaf(sg1, ag[3], tg[3]);
+  tu[0] = fmaf(su0, au[0], tu[0]);
+  tu[1] = fmaf(su0, au[1], tu[1]);
+  tu[2] = fmaf(su1, au[2], tu[2]);
+  tu[3] = fmaf(su1, au[3], tu[3]);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The bias terms of one matrix of a gate/up unit over all G groups, in the
+// fragment layout of gu_group's accumulators: t[row][token] +=
+// sum_g b[row][g] * sum(x[token], group g), as a bf16 tensor-core product of
+// the tile's biases (A: rows, groups) with the chunk's group sums split in
+// bf16 hi + lo parts (B: groups, tokens).  boff: offset of the bias rows in
+// the tile's scale/bias area (16*G gate, 48*G up); xs: [kTC][2][gp].
+__device__ __forceinline__ void gu_bias(const uint8_t *tile, const uint16_t *xs, int qp, int G, int gp, int boff,
+                                        int r, int cq, float (&t)[4]) {
+  const uint16_t *b = reinterpret_cast<const uint16_t *>(tile + 8 * qp) + boff;
+  const int sr0 = quad_row(r), sr1 = sr0 + 2;
+  auto pairv = [&](int row, int g) -> uint32_t {  // biases g, g+1 of a row (zero past G)
+    const uint32_t lo = g < G ? b[row * G + g] : 0u, hi = g + 1 < G ? b[row * G + g + 1] : 0u;
+    return lo | (hi << 16);
+  };
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 < gp; k0 += 16) {
+    const int g0 = k0 + 2 * cq;
+    const uint32_t A[4] = {pairv(sr0, g0), pairv(sr1, g0), pairv(sr0, g0 + 8), pairv(sr1, g0 + 8)};
+    const uint32_t *xr = reinterpret_cast<const uint32_t *>(xs + r * 2 * gp);  // token r: hi then lo
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const uint32_t *xp = xr + (part * gp + g0) / 2;
+      mma_bf16(acc, A, xp[0], xp[4]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t[i] += acc[i];
 }
 
 // Down: one 64-wide group; rows row0 + r, +8 of the 128-row tile, token
@@ -386,7 +423,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         if (chg != cur) {
           if (xk >= 1) ok = mbar_wait_idle(xempty, (xk - 1) & 1, 32);
           if (!ok) break;
-          if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(x.nt * (H * 2 + (H / 16) * 4)));
+          if (lane == 0) mbar_arrive_expect_tx(xfull, (uint32_t)(x.nt * (H * 2 + 4 * L.gp)));
           __syncwarp();
           if (lane < 2 * x.nt) {
             const int j = lane >> 1;
@@ -394,7 +431,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
             if ((lane & 1) == 0)
               bulk_g2s(xbuf + j * L.xp, a.xperm + (size_t)tok * H, (uint32_t)(H * 2), xfull);
             else
-              bulk_g2s(xbuf + L.x_xq + j * L.xqp * 4, a.xq + (size_t)tok * (H / 16), (uint32_t)((H / 16) * 4), xfull);
+              bulk_g2s(xbuf + L.x_xs + j * 4 * L.gp, a.xs + (size_t)tok * 2 * L.gp, (uint32_t)(4 * L.gp), xfull);
           }
           ++xk;
           cur = chg;
@@ -562,7 +599,6 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         s += __uint_as_float(qin[i] << 16);
         s += __uint_as_float(qin[i] & 0xFFFF0000u);
       }
-      a.xq[(size_t)t * nquart + tid] = s;
       // router operand: fp16 pairs (x0,x2)(x1,x3)(x4,x6)(x5,x7)... of this quarter
       uint32_t h[8];
 #pragma unroll
@@ -579,6 +615,18 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       reinterpret_cast<float *>(xbuf + L.rx_q)[tid] = s;
     }
     cons_sync();  // rx complete
+    // group sums of x for the gate/up bias terms, as bf16 hi + lo (zero padded to gp)
+    if (tid < L.gp) {
+      uint16_t hi = 0, lo = 0;
+      if (tid < G) {
+        const float *q = reinterpret_cast<const float *>(xbuf + L.rx_q) + 4 * tid;
+        const float gs = ((q[0] + q[1]) + q[2]) + q[3];
+        hi = float_to_bf16_bits(gs);
+        lo = float_to_bf16_bits(gs - bf16_bits_to_float(hi));
+      }
+      a.xs[(size_t)t * 2 * L.gp + tid] = hi;
+      a.xs[(size_t)t * 2 * L.gp + L.gp + tid] = lo;
+    }
     float rt0[8], rt1[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
@@ -761,15 +809,19 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
           break;
         }
         const uint8_t *wt = ring + slot * L.wslot;
-        const float *xq = reinterpret_cast<const float *>(xbuf + L.x_xq);
+        const uint16_t *xs = reinterpret_cast<const uint16_t *>(xbuf + L.x_xs);
         float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
         float tg2[4] = {0.f, 0.f, 0.f, 0.f}, tu2[4] = {0.f, 0.f, 0.f, 0.f};
         int g = wl;
         for (; g + 8 < G; g += 16) {
-          gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
-          gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g + 8, r, cq, tg2, tu2);
+          gu_group(wt, xbuf, L.gu_qp, L.xp, G, g, r, cq, tg, tu);
+          gu_group(wt, xbuf, L.gu_qp, L.xp, G, g + 8, r, cq, tg2, tu2);
         }
-        if (g < G) gu_group(wt, xbuf, xq, L.gu_qp, L.xp, L.xqp, G, g, r, cq, tg, tu);
+        if (g < G) gu_group(wt, xbuf, L.gu_qp, L.xp, G, g, r, cq, tg, tu);
+        // bias terms: gate in the group's last warp, up in the one before
+        // (the warps with the fewest groups)
+        if (wl == 7) gu_bias(wt, xs, L.gu_qp, G, L.gp, 16 * G, r, cq, tg2);
+        if (wl == 6) gu_bias(wt, xs, L.gu_qp, G, L.gp, 48 * G, r, cq, tu2);
         release_g(slot);
         // reduction over the group's 8 warps, transposed (conflict-free): red[w][i][lane]
         float *red_g = red + gi * 8 * 256;
