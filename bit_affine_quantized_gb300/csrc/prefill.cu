@@ -248,8 +248,8 @@ __device__ __forceinline__ void gu_bias(const uint8_t *tile, const uint16_t *xs,
 
 // Down: one 64-wide group; rows row0 + r, +8 of the 128-row tile, token
 // columns 2cq, 2cq+1.
-__device__ __forceinline__ void dn_group(const uint8_t *tile, const uint8_t *hrows, const float *hq, int qp, int hp,
-                                         int hqp, int GI, int row0, int g, int r, int cq, float (&t)[4]) {
+__device__ __forceinline__ void dn_group(const uint8_t *tile, const uint8_t *hrows, int qp, int hp, int GI, int row0,
+                                         int g, int r, int cq, float (&t)[4]) {
   const uint16_t *sb = reinterpret_cast<const uint16_t *>(tile + kDnRows * qp);  // scales [128][GI], biases [128][GI]
   const uint2 w0 = *reinterpret_cast<const uint2 *>(tile + (row0 + r) * qp + g * 32 + cq * 8);
   const uint2 w1 = *reinterpret_cast<const uint2 *>(tile + (row0 + r + 8) * qp + g * 32 + cq * 8);
@@ -268,17 +268,39 @@ __device__ __forceinline__ void dn_group(const uint8_t *tile, const uint8_t *hro
     }
     mma_f16(acc, A, bb[2 * st], bb[2 * st + 1]);
   }
-  const float4 q0 = *reinterpret_cast<const float4 *>(hq + (2 * cq) * hqp + 4 * g);
-  const float4 q1 = *reinterpret_cast<const float4 *>(hq + (2 * cq + 1) * hqp + 4 * g);
-  const float hs0 = ((q0.x + q0.y) + q0.z) + q0.w, hs1 = ((q1.x + q1.y) + q1.z) + q1.w;
   const float s0 = bf16_bits_to_float(sb[(row0 + r) * GI + g]) * kCodeScale;
-  const float b0 = bf16_bits_to_float(sb[kDnRows * GI + (row0 + r) * GI + g]);
   const float s1 = bf16_bits_to_float(sb[(row0 + r + 8) * GI + g]) * kCodeScale;
-  const float b1 = bf16_bits_to_float(sb[kDnRows * GI + (row0 + r + 8) * GI + g]);
-  t[0] = fmaf(b0, hs0, fmaf(s0, acc[0], t[0]));
-  t[1] = fmaf(b0, hs1, fmaf(s0, acc[1], t[1]));
-  t[2] = fmaf(b1, hs0, fmaf(s1, acc[2], t[2]));
-  t[3] = fmaf(b1, hs1, fmaf(s1, acc[3], t[3]));
+  t[0] = fmaf(s0, acc[0], t[0]);
+  t[1] = fmaf(s0, acc[1], t[1]);
+  t[2] = fmaf(s1, acc[2], t[2]);
+  t[3] = fmaf(s1, acc[3], t[3]);
+}
+
+// The bias terms of a warp's 16 rows of a down unit over all GI groups:
+// t[row][token] += sum_g b[row][g] * sum(h[token], group g), a bf16
+// tensor-core product of the tile's biases with the chunk's group sums of h
+// (hi + lo parts, hs: [kTC][2][gip]).
+__device__ __forceinline__ void dn_bias(const uint8_t *tile, const uint16_t *hs, int qp, int GI, int gip, int row0,
+                                        int r, int cq, float (&t)[4]) {
+  const uint16_t *b = reinterpret_cast<const uint16_t *>(tile + kDnRows * qp) + kDnRows * GI;
+  auto pairv = [&](int row, int g) -> uint32_t {
+    const uint32_t lo = g < GI ? b[row * GI + g] : 0u, hi = g + 1 < GI ? b[row * GI + g + 1] : 0u;
+    return lo | (hi << 16);
+  };
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 < gip; k0 += 16) {
+    const int g0 = k0 + 2 * cq;
+    const uint32_t A[4] = {pairv(row0 + r, g0), pairv(row0 + r + 8, g0), pairv(row0 + r, g0 + 8),
+                           pairv(row0 + r + 8, g0 + 8)};
+    const uint32_t *hr = reinterpret_cast<const uint32_t *>(hs + r * 2 * gip);  // token r: hi then lo
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const uint32_t *hp2 = hr + (part * gip + g0) / 2;
+      mma_bf16(acc, A, hp2[0], hp2[4]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t[i] += acc[i];
 }
 
 // Decoded work unit: active slot, chunk within it, tile within the chunk.
@@ -881,6 +903,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     mbar_arrive_expect_tx(hready, 0);
   }
 
+  const int gip = (GI + 15) & ~15;  // padded group count of the h group-sum tables
+  uint16_t *hs_g = reinterpret_cast<uint16_t *>(red + gi * 8 * 256);
   // ---- D: down units [c * n_dn / nb, (c + 1) * n_dn / nb) -> weighted outputs,
   // in the same two-group steps.  A group's warp w owns rows 16w..16w+15 of its
   // 128-row unit over the whole K, so its results leave straight from registers.
@@ -910,6 +934,21 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
           set_error(a.err, kErrTimeout);
           break;
         }
+        // the chunk's group sums of h, bf16 hi + lo, in this group's table
+        // (its reduction area, unused by the down units)
+        if (gt < kTC * gip) {
+          const int tok = gt / gip, gg = gt - tok * gip;
+          uint16_t hi = 0, lo = 0;
+          if (gg < GI) {
+            const float *q = reinterpret_cast<const float *>(xbuf + L.x_hq) + tok * L.hqp + 4 * gg;
+            const float v = ((q[0] + q[1]) + q[2]) + q[3];
+            hi = float_to_bf16_bits(v);
+            lo = float_to_bf16_bits(v - bf16_bits_to_float(hi));
+          }
+          hs_g[tok * 2 * gip + gg] = hi;
+          hs_g[tok * 2 * gip + gip + gg] = lo;
+        }
+        gsync();
       }
       const int mine = gi == 0 ? u : (pair ? u + 1 : -1);
       if (mine >= 0) {
@@ -920,14 +959,14 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
           break;
         }
         const uint8_t *wt = ring + slot * L.wslot;
-        const float *hq = reinterpret_cast<const float *>(xbuf + L.x_hq);
         float t4[4] = {0.f, 0.f, 0.f, 0.f}, t4b[4] = {0.f, 0.f, 0.f, 0.f};
         int g = 0;
         for (; g + 1 < GI; g += 2) {
-          dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * wl, g, r, cq, t4);
-          dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * wl, g + 1, r, cq, t4b);
+          dn_group(wt, xbuf, L.dn_qp, L.hp, GI, 16 * wl, g, r, cq, t4);
+          dn_group(wt, xbuf, L.dn_qp, L.hp, GI, 16 * wl, g + 1, r, cq, t4b);
         }
-        if (g < GI) dn_group(wt, xbuf, hq, L.dn_qp, L.hp, L.hqp, GI, 16 * wl, g, r, cq, t4);
+        if (g < GI) dn_group(wt, xbuf, L.dn_qp, L.hp, GI, 16 * wl, g, r, cq, t4);
+        dn_bias(wt, hs_g, L.dn_qp, GI, gip, 16 * wl, r, cq, t4b);
         release_g(slot);
         const int n0 = tile * kDnRows, rows = min(kDnRows, H - n0);
 #pragma unroll
