@@ -164,8 +164,9 @@ __device__ __forceinline__ void rt_group(const uint8_t *tile, const uint8_t *rx,
 
 // One 64-wide group of a gate/up unit for the chunk's 8 tokens: mma rows r,
 // r+8 (tile rows quad_row(r), quad_row(r) + 2), token columns 2cq, 2cq+1.
-// Accumulates the scaled code products s*acc per row and token; the bias
-// terms b*sum(x) of all groups come from gu_bias once per unit.
+// Accumulates s*acc per row and token, which carries the 2^-24 of the code
+// operands (the epilogue multiplies by 2^24 once); the bias terms
+// b*sum(x)*2^-24 of all groups come from gu_bias once per unit.
 __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xrows, int qp, int xp, int G, int g,
                                          int r, int cq, float (&tg)[4], float (&tu)[4]) {
   const int rowb = G * 32;                    // bytes of one row of codes (H / 2)
@@ -195,10 +196,8 @@ __device__ __forceinline__ void gu_group(const uint8_t *tile, const uint8_t *xro
     mma_f16(ag, A, bb[2 * s], bb[2 * s + 1]);
     mma_f16(au, B, bb[2 * s], bb[2 * s + 1]);
   }
-  const float sg0 = bf16_bits_to_float(raw[sr0 * G + g]) * kCodeScale;
-  const float sg1 = bf16_bits_to_float(raw[sr1 * G + g]) * kCodeScale;
-  const float su0 = bf16_bits_to_float(raw[32 * G + sr0 * G + g]) * kCodeScale;
-  const float su1 = bf16_bits_to_float(raw[32 * G + sr1 * G + g]) * kCodeScale;
+  const float sg0 = bf16_bits_to_float(raw[sr0 * G + g]), sg1 = bf16_bits_to_float(raw[sr1 * G + g]);
+  const float su0 = bf16_bits_to_float(raw[32 * G + sr0 * G + g]), su1 = bf16_bits_to_float(raw[32 * G + sr1 * G + g]);
   tg[0] = fmaf(sg0, ag[0], tg[0]);
   tg[1] = fmaf(sg0, ag[1], tg[1]);
   tg[2] = fmaf(sg1, ag[2], tg[2]);
@@ -268,8 +267,8 @@ __device__ __forceinline__ void dn_group(const uint8_t *tile, const uint8_t *hro
     }
     mma_f16(acc, A, bb[2 * st], bb[2 * st + 1]);
   }
-  const float s0 = bf16_bits_to_float(sb[(row0 + r) * GI + g]) * kCodeScale;
-  const float s1 = bf16_bits_to_float(sb[(row0 + r + 8) * GI + g]) * kCodeScale;
+  const float s0 = bf16_bits_to_float(sb[(row0 + r) * GI + g]);
+  const float s1 = bf16_bits_to_float(sb[(row0 + r + 8) * GI + g]);
   t[0] = fmaf(s0, acc[0], t[0]);
   t[1] = fmaf(s0, acc[1], t[1]);
   t[2] = fmaf(s1, acc[2], t[2]);
@@ -642,7 +641,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       uint16_t hi = 0, lo = 0;
       if (tid < G) {
         const float *q = reinterpret_cast<const float *>(xbuf + L.rx_q) + 4 * tid;
-        const float gs = ((q[0] + q[1]) + q[2]) + q[3];
+        const float gs = (((q[0] + q[1]) + q[2]) + q[3]) * (1.0f / kCodeScale);  // 2^-24, as the code products
         hi = float_to_bf16_bits(gs);
         lo = float_to_bf16_bits(gs - bf16_bits_to_float(hi));
       }
@@ -862,7 +861,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
             us += red_g[w * 256 + (idx + 4) * 32 + ln];
           }
           const int m = (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);  // mma row, token
-          const float hv = fused::gelu_tanh(gs) * us;
+          const float hv = fused::gelu_tanh(gs * kCodeScale) * (us * kCodeScale);
           if (n < nt && !(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
           s_hst_g[n * 16 + quad_row(m)] = __float2half_rn(hv);
         }
@@ -941,7 +940,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
           uint16_t hi = 0, lo = 0;
           if (gg < GI) {
             const float *q = reinterpret_cast<const float *>(xbuf + L.x_hq) + tok * L.hqp + 4 * gg;
-            const float v = ((q[0] + q[1]) + q[2]) + q[3];
+            const float v = (((q[0] + q[1]) + q[2]) + q[3]) * (1.0f / kCodeScale);
             hi = float_to_bf16_bits(v);
             lo = float_to_bf16_bits(v - bf16_bits_to_float(hi));
           }
@@ -972,7 +971,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = 16 * wl + r + 8 * (i >> 1), n = 2 * cq + (i & 1);
-          if (n < nt && row < rows) a.obuf[(size_t)(p0 + n) * H + n0 + row] = s_wt_g[n] * (t4[i] + t4b[i]);
+          if (n < nt && row < rows)
+            a.obuf[(size_t)(p0 + n) * H + n0 + row] = s_wt_g[n] * ((t4[i] + t4b[i]) * kCodeScale);
         }
       }
       u += pair ? 2 : 1;
