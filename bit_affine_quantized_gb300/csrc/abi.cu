@@ -138,6 +138,8 @@ int check_weights_impl(const moe_layer_weights *w) {
   for (int i = 0; i < 5; ++i)
     if (!ptrs[i] || !aligned(ptrs[i], 16)) return MOE_ERR_INVALID_ARG;
   if (w->logit_bias && !aligned(w->logit_bias, 4)) return MOE_ERR_INVALID_ARG;
+  if (w->router_scale && !aligned(w->router_scale, 16)) return MOE_ERR_INVALID_ARG;
+  if (w->per_expert_scale && !aligned(w->per_expert_scale, 4)) return MOE_ERR_INVALID_ARG;
   const size_t offs[9] = {w->layout.gate_q, w->layout.gate_s, w->layout.gate_b, w->layout.up_q, w->layout.up_s,
                           w->layout.up_b,   w->layout.down_q, w->layout.down_s, w->layout.down_b};
   for (size_t o : offs)
@@ -158,6 +160,8 @@ moe::LayerPtrs layer_ptrs(const moe_layer_weights &w) {
                     w.layout.up_b,   w.layout.down_q, w.layout.down_s, w.layout.down_b};
   p.blob_bytes = blob_extent(w);
   p.logit_bias = w.logit_bias;
+  p.router_scale = (const uint16_t *)w.router_scale;
+  p.expert_scale = w.per_expert_scale;
   return p;
 }
 

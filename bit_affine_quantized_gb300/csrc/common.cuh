@@ -57,6 +57,8 @@ struct LayerPtrs {
   Blob off;
   size_t blob_bytes;            // extent of one blob's sub-tensors (max end offset)
   const float *logit_bias;      // nullable [E]
+  const uint16_t *router_scale; // nullable bf16 [H]: router input x * router_scale / sqrt(H)
+  const float *expert_scale;    // nullable [E]: factor of a selected expert's routing weight
 };
 
 struct Dims {

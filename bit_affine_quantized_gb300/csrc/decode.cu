@@ -43,7 +43,7 @@ struct FusedLayout {
   int n_gu, n_dn;   // gate/up units, down units
   int gu_qp;        // gate/up 4-row block pitch (bytes)
   int gu_bytes, dn_qp, dn_slot_bytes, dn_bytes, slot_bytes;
-  int ring, xperm, xsum, qsum, hperm, hsum, red, misc, total;
+  int ring, xperm, xsum, qsum, hperm, hsum, red, misc, rsc, pes, total;
 };
 
 __host__ __device__ inline FusedLayout fused_layout(int H, int I, int k) {
@@ -75,6 +75,10 @@ __host__ __device__ inline FusedLayout fused_layout(int H, int I, int k) {
   o = al16(o + kCons * 32 * 8 * 4);
   L.misc = o;  // partial sums, k ids, k weights, flags, 2*kSlots+1 mbarriers
   o = al16(o + 512);
+  L.rsc = o;  // the router scale (when given), bf16 [H]
+  o = al16(o + H * 2);
+  L.pes = o;  // per-expert routing-weight scales (when given), fp32 [E]
+  o = al16(o + kMaxExperts * 4);
   L.total = o;
   return L;
 }
@@ -221,6 +225,9 @@ size_t fused_decode_smem(const Dims &d) {
   return (size_t)fused_layout(d.H, d.I, d.k).total;
 }
 
+// kScales: the layer has learned router scales (the router-scale code is
+// compiled out of the plain instance).
+template <bool kScales>
 __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int H = a.d.H, I = a.d.I, E = a.d.E, k = a.d.k;
@@ -361,6 +368,17 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     rb = bf16_bits_to_float(__ldg(a.w.router_b + (size_t)c * G + (tid >> 2)));
   }
   const float lbias = has_row && a.w.logit_bias ? __ldg(a.w.logit_bias + c) : 0.f;
+  // the router's learned scales, when given, staged in shared memory before
+  // the dependency wait (weights: they do not depend on the previous launch)
+  uint16_t *s_rsc = reinterpret_cast<uint16_t *>(smem + L.rsc);
+  float *s_pes = reinterpret_cast<float *>(smem + L.pes);
+  const bool rscale = kScales && a.w.router_scale != nullptr, escale = kScales && a.w.expert_scale != nullptr;
+  if (rscale && tid < nquart) {
+    const uint4 *src4 = reinterpret_cast<const uint4 *>(a.w.router_scale) + 2 * tid;
+    reinterpret_cast<uint4 *>(s_rsc)[2 * tid] = __ldg(src4);
+    reinterpret_cast<uint4 *>(s_rsc)[2 * tid + 1] = __ldg(src4 + 1);
+  }
+  if (escale && tid < E) s_pes[tid] = __ldg(a.w.expert_scale + tid);
   pdl_wait();
   pdl_launch_dependents();
   if (c == 0 && tid == 0) trace_min(a.trace, kTrWaited);
@@ -404,8 +422,15 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
       const uint32_t w = rw[i >> 1] >> (16 * (i & 1));
       const float qlo = __uint_as_float(0x4B000000u | (w & 0xFFu)) - 8388608.0f;
       const float qhi = __uint_as_float(0x4B000000u | ((w >> 8) & 0xFFu)) - 8388608.0f;
-      lg = fmaf(fmaf(qlo, rs, rb), lo, lg);
-      lg = fmaf(fmaf(qhi, rs, rb), hi, lg);
+      if (rscale) {  // router input x * router_scale / sqrt(H)
+        const uint32_t sc = reinterpret_cast<const uint32_t *>(s_rsc)[8 * tid + i];
+        const float inv_sqrt_h = rsqrtf((float)H);
+        lg = fmaf(fmaf(qlo, rs, rb), lo * (__uint_as_float(sc << 16) * inv_sqrt_h), lg);
+        lg = fmaf(fmaf(qhi, rs, rb), hi * (__uint_as_float(sc & 0xFFFF0000u) * inv_sqrt_h), lg);
+      } else {
+        lg = fmaf(fmaf(qlo, rs, rb), lo, lg);
+        lg = fmaf(fmaf(qhi, rs, rb), hi, lg);
+      }
     }
   }
 #pragma unroll
@@ -636,7 +661,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     }
     __syncwarp();
     if (lane < k) {
-      const float wj = myex / den;
+      const float wj = myex / den * (escale ? s_pes[s_sel[lane]] : 1.0f);
       s_w[lane] = wj;
       if (c == 0) {
         if (a.ids_user) a.ids_user[lane] = s_sel[lane];
@@ -752,19 +777,26 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
 }
 
 cudaError_t launch_decode_fused(const DecodeArgs &a, int n_blocks, cudaStream_t st, bool pdl) {
-  return launch_k(decode_layer_kernel, dim3(n_blocks), dim3(kThreadsF), fused_decode_smem(a.d), st, pdl, a);
+  const bool scales = a.w.router_scale != nullptr || a.w.expert_scale != nullptr;
+  return launch_k(scales ? decode_layer_kernel<true> : decode_layer_kernel<false>, dim3(n_blocks), dim3(kThreadsF),
+                  fused_decode_smem(a.d), st, pdl, a);
 }
 
 cudaError_t decode_set_attributes() {
-  return cudaFuncSetAttribute(decode_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  const cudaError_t e =
+      cudaFuncSetAttribute(decode_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
 }
 
 int decode_blocks_per_sm(const Dims &d) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel, kThreadsF, fused_decode_smem(d)) !=
-      cudaSuccess)
+  int n = 0, n2 = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_layer_kernel<false>, kThreadsF, fused_decode_smem(d)) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n2, decode_layer_kernel<true>, kThreadsF, fused_decode_smem(d)) !=
+          cudaSuccess)
     return 0;
-  return n;
+  return n < n2 ? n : n2;
 }
 
 }  // namespace moe

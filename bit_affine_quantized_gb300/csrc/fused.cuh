@@ -80,7 +80,7 @@ __device__ __forceinline__ float key_value(unsigned k) {
 // Non-finite logits count as -inf and set *nonfinite.  `logits` is read with
 // plain loads: shared memory, or global memory this block wrote itself.
 __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int32_t *ids_out, float *wts_out,
-                                          bool *nonfinite) {
+                                          const float *expert_scale, bool *nonfinite) {
   const int lane = threadIdx.x & 31;
   unsigned key[4];
   bool bad = false;
@@ -131,7 +131,7 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
   for (int j = 0; j < kMaxTopK; ++j)
     if (j < k && lane == j) {
       ids_out[j] = seli[j];
-      wts_out[j] = ex[j] / den;
+      wts_out[j] = ex[j] / den * (expert_scale ? expert_scale[seli[j]] : 1.0f);
     }
 }
 

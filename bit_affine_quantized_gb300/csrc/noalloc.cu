@@ -114,6 +114,8 @@ extern "C" int moe_layer_forward_static(const void *x, const moe_layer_weights *
                       w->layout.up_b,   w->layout.down_q, w->layout.down_s, w->layout.down_b};
   a.w.blob_bytes = extent(*w);
   a.w.logit_bias = w->logit_bias;
+  a.w.router_scale = (const uint16_t *)w->router_scale;
+  a.w.expert_scale = w->per_expert_scale;
   a.d = d;
   a.x = (const uint16_t *)x;
   a.hres = nullptr;

@@ -68,6 +68,7 @@ struct PL {
   int hp, hqp, x_hq;                // X as down operand
   int rx_q, rx_sb;                  // X as router operand: quarter sums after the fp16 row, then the
                                     // router's scales and biases (bf16 [16 n_mt][G] each)
+  int rx_xq;                        // quarter sums of x itself when the router operand is scaled x
   int xbuf;
   int ring, xb, red, grp, misc, total;
 };
@@ -99,7 +100,8 @@ __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) 
   L.x_hq = kTC * L.hp;
   L.rx_q = 2 * H;
   L.rx_sb = al16(L.rx_q + (H / 16) * 4);
-  L.xbuf = al16(imax(L.x_xs + kTC * 4 * L.gp, imax(L.x_hq + kTC * L.hqp * 4, L.rx_sb + 2 * kRtRows * L.n_mt * L.G * 2)));
+  L.rx_xq = al16(L.rx_sb + 2 * kRtRows * L.n_mt * L.G * 2);
+  L.xbuf = al16(imax(L.x_xs + kTC * 4 * L.gp, imax(L.x_hq + kTC * L.hqp * 4, L.rx_xq + (H / 16) * 4)));
   int o = 0;
   L.ring = o;
   o += kWSlots * L.wslot;
@@ -334,6 +336,9 @@ struct PrefillParams {
 };
 }  // namespace
 
+// kScales: the layer has learned router scales (the router-scale code is
+// compiled out of the plain instance).
+template <bool kScales>
 __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const PrefillParams prm) {
   extern __shared__ __align__(128) uint8_t smem[];
   const PrefillArgs &a = prm.a;
@@ -620,10 +625,30 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
         s += __uint_as_float(qin[i] << 16);
         s += __uint_as_float(qin[i] & 0xFFFF0000u);
       }
-      // router operand: fp16 pairs (x0,x2)(x1,x3)(x4,x6)(x5,x7)... of this quarter
+      // router operand: fp16 pairs (x0,x2)(x1,x3)(x4,x6)(x5,x7)... of this
+      // quarter, of x or (router scale given) of x * router_scale / sqrt(H);
+      // its sum over the quarter feeds the router's bias terms
       uint32_t h[8];
+      float rsum = s;
+      if (kScales && a.w.router_scale) {
+        const uint4 *rs4 = reinterpret_cast<const uint4 *>(a.w.router_scale) + 2 * tid;
+        const uint4 r0 = __ldg(rs4), r1 = __ldg(rs4 + 1);
+        const uint32_t rw8[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        const float isq = rsqrtf((float)H);
+        rsum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = bf16x2_to_f16x2(qin[i]);
+        for (int i = 0; i < 8; ++i) {
+          const __half2 hv = __floats2half2_rn(
+              __uint_as_float(qin[i] << 16) * (__uint_as_float(rw8[i] << 16) * isq),
+              __uint_as_float(qin[i] & 0xFFFF0000u) * (__uint_as_float(rw8[i] & 0xFFFF0000u) * isq));
+          h[i] = *reinterpret_cast<const uint32_t *>(&hv);
+          rsum += __low2float(hv);
+          rsum += __high2float(hv);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = bf16x2_to_f16x2(qin[i]);
+      }
       uint32_t rp[8];
 #pragma unroll
       for (int s2 = 0; s2 < 4; ++s2) {
@@ -633,14 +658,15 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       uint4 *rx = reinterpret_cast<uint4 *>(xbuf + tid * 32);
       rx[0] = make_uint4(rp[0], rp[1], rp[2], rp[3]);
       rx[1] = make_uint4(rp[4], rp[5], rp[6], rp[7]);
-      reinterpret_cast<float *>(xbuf + L.rx_q)[tid] = s;
+      reinterpret_cast<float *>(xbuf + L.rx_q)[tid] = rsum;
+      if (kScales && a.w.router_scale) reinterpret_cast<float *>(xbuf + L.rx_xq)[tid] = s;
     }
     cons_sync();  // rx complete
     // group sums of x for the gate/up bias terms, as bf16 hi + lo (zero padded to gp)
     if (tid < L.gp) {
       uint16_t hi = 0, lo = 0;
       if (tid < G) {
-        const float *q = reinterpret_cast<const float *>(xbuf + L.rx_q) + 4 * tid;
+        const float *q = reinterpret_cast<const float *>(xbuf + (kScales && a.w.router_scale ? L.rx_xq : L.rx_q)) + 4 * tid;
         const float gs = (((q[0] + q[1]) + q[2]) + q[3]) * (1.0f / kCodeScale);  // 2^-24, as the code products
         hi = float_to_bf16_bits(gs);
         lo = float_to_bf16_bits(gs - bf16_bits_to_float(hi));
@@ -692,7 +718,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     cons_sync();
     if (warp == 0) {
       bool bad = false;
-      fused::warp_topk(s_logit, E, k, a.r.ids + t * k, a.r.wts + t * k, &bad);
+      fused::warp_topk(s_logit, E, k, a.r.ids + t * k, a.r.wts + t * k, kScales ? a.w.expert_scale : nullptr, &bad);
       if (bad && lane == 0) set_error(a.err, kErrNonFinite);
       __syncwarp();
       if (lane < k) {
@@ -1027,20 +1053,28 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
 
 cudaError_t launch_prefill_fused(const PrefillArgs &a, int n_blocks, cudaStream_t st, bool pdl) {
   const PrefillParams prm{a, prefill_layout(a.d.H, a.d.I, a.d.E, a.d.k, a.d.T)};
-  return launch_k(prefill_layer_kernel, dim3(n_blocks), dim3(fused::kThreads), prefill_fused_smem(a.d), st, pdl, prm);
+  const bool scales = a.w.router_scale != nullptr || a.w.expert_scale != nullptr;
+  return launch_k(scales ? prefill_layer_kernel<true> : prefill_layer_kernel<false>, dim3(n_blocks),
+                  dim3(fused::kThreads), prefill_fused_smem(a.d), st, pdl, prm);
 }
 
 cudaError_t prefill_set_attributes() {
-  return cudaFuncSetAttribute(prefill_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  const cudaError_t e =
+      cudaFuncSetAttribute(prefill_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
 }
 
 int prefill_blocks_per_sm(const Dims &d) {
   const size_t smem = prefill_fused_smem(d);
   if (smem == 0) return 0;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_layer_kernel, fused::kThreads, smem) != cudaSuccess)
+  int n = 0, n2 = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_layer_kernel<false>, fused::kThreads, smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n2, prefill_layer_kernel<true>, fused::kThreads, smem) !=
+          cudaSuccess)
     return 0;
-  return n;
+  return n < n2 ? n : n2;
 }
 
 }  // namespace moe

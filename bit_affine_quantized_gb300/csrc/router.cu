@@ -217,7 +217,7 @@ __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
 // Ids come out by descending logit, ties to the lower id; weights are the
 // softmax over the k selected logits.
 __device__ void topk_token(const float *logits_row, int E, int k, int32_t *ids_out, float *wts_out,
-                           int32_t *ids_user, float *wts_user, unsigned *err) {
+                           int32_t *ids_user, float *wts_user, const float *expert_scale, unsigned *err) {
   const int lane = threadIdx.x & 31;
   float v[4];
   int id[4];
@@ -280,7 +280,7 @@ __device__ void topk_token(const float *logits_row, int E, int k, int32_t *ids_o
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) {
     if (j < k && lane == j) {
-      const float wj = ex[j] / den;
+      const float wj = ex[j] / den * (expert_scale ? expert_scale[sel_i[j]] : 1.0f);
       ids_out[j] = sel_i[j];
       wts_out[j] = wj;
       if (ids_user) ids_user[j] = sel_i[j];
@@ -394,6 +394,16 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterArgs a) {
           f[2 * q] = lo;
           f[2 * q + 1] = hi;
         }
+        if (a.w.router_scale) {  // router input x * router_scale / sqrt(H)
+          const uint4 rv = __ldg(reinterpret_cast<const uint4 *>(a.w.router_scale) + idx);
+          const uint32_t r4[4] = {rv.x, rv.y, rv.z, rv.w};
+          const float isq = rsqrtf((float)H);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            f[2 * q] *= __uint_as_float(r4[q] << 16) * isq;
+            f[2 * q + 1] *= __uint_as_float(r4[q] & 0xFFFF0000u) * isq;
+          }
+        }
         float4 *dst = reinterpret_cast<float4 *>(sx + n * H + 8 * idx);
         dst[0] = make_float4(f[0], f[1], f[2], f[3]);
         dst[1] = make_float4(f[4], f[5], f[6], f[7]);
@@ -467,7 +477,8 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterArgs a) {
     if (warp == 0) {
       for (int t = 0; t < T; ++t)
         topk_token(a.logits + (size_t)t * E, E, k, a.r.ids + t * k, a.r.wts + t * k,
-                   a.ids_user ? a.ids_user + t * k : nullptr, a.wts_user ? a.wts_user + t * k : nullptr, a.err);
+                   a.ids_user ? a.ids_user + t * k : nullptr, a.wts_user ? a.wts_user + t * k : nullptr,
+                   a.w.expert_scale, a.err);
       __syncwarp();
       group_pairs_warp(a.r.ids, T, k, E, a.r, 1, a.err);
       if (lane == 0) {
@@ -479,7 +490,8 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterArgs a) {
   }
   for (int t = warp; t < T; t += kWarps)
     topk_token(a.logits + (size_t)t * E, E, k, a.r.ids + t * k, a.r.wts + t * k,
-               a.ids_user ? a.ids_user + t * k : nullptr, a.wts_user ? a.wts_user + t * k : nullptr, a.err);
+               a.ids_user ? a.ids_user + t * k : nullptr, a.wts_user ? a.wts_user + t * k : nullptr,
+                   a.w.expert_scale, a.err);
   __syncthreads();
   group_pairs(a.r.ids, T, k, E, a.r, 1, a.err);
   if (tid == 0) {

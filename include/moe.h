@@ -112,6 +112,15 @@ typedef struct {
   moe_blob_layout layout;   /* sub-tensor offsets (routed and shared blobs)   */
   const void *shared;       /* the shared expert's blob                       */
   const float *logit_bias;  /* nullable [E]: added to the logits before top-k */
+  /* The router's learned scales (section "Decode", router description),
+   * both nullable (null: identity):
+   *   router_scale      bf16 [H], 16-byte aligned: the router projects
+   *                     x * router_scale / sqrt(H) instead of x (the experts
+   *                     still take x);
+   *   per_expert_scale  fp32 [E]: the routing weight of a selected expert e
+   *                     is softmax(...) * per_expert_scale[e]. */
+  const void *router_scale;
+  const float *per_expert_scale;
 } moe_layer_weights;
 
 typedef struct moe_handle moe_handle;

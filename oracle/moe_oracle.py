@@ -21,10 +21,14 @@ Sources (page "TurboFieldfare - System design", by section):
     the router logits have no softcap; shared and routed FFNs run in parallel
     on the same input.
   * Section "Decode", router description: normalise, scale, project with the
-    8-bit affine weights, take the 8 highest logits, softmax over those 8.
-    The block here receives an already normalised input and the learned
-    router/expert scales are identity, so the router is logits = W_r x
-    (+ an optional per-expert logit offset used by the skewed workloads).
+    8-bit affine weights, take the 8 highest logits, softmax over those 8,
+    times the selected experts' learned scales.  The block here receives an
+    already normalised input x; the router projects x * router_scale /
+    sqrt(H) when a learned router scale (one value per input feature) is
+    given, else x; the routing weights are softmax(selected logits) *
+    per_expert_scale[id] when per-expert scales are given, else the softmax
+    alone (+ an optional per-expert logit offset used by the skewed
+    workloads).
   * Section "Metal execution": the routed kernels fuse affine decode, GeGLU
     and the weighted reduction over the selected experts.  GeGLU here is
     h = gelu_tanh(W_gate x) * (W_up x), out = W_down h (Gemma's gated FFN;
@@ -115,9 +119,13 @@ def dequantize(words, scale_bits, bias_bits, bits: int) -> np.ndarray:
 
 
 # ------------------------------------------------------------- router
-def router_logits(x_bits, router: dict, logit_bias=None) -> np.ndarray:
-    """logits[t, e] = sum_k W_r[e, k] x[t, k] (+ offset[e]); float64 [T, E]."""
+def router_logits(x_bits, router: dict, logit_bias=None, router_scale=None) -> np.ndarray:
+    """logits[t, e] = sum_k W_r[e, k] x'[t, k] (+ offset[e]); float64 [T, E].
+
+    x' = x, or x * router_scale / sqrt(H) with router_scale bf16 bits [H]."""
     x = bf16_to_f64(x_bits)
+    if router_scale is not None:
+        x = x * bf16_to_f64(router_scale)[None, :] / np.sqrt(x.shape[1])
     w_r = dequantize(router["q"], router["s"], router["b"], 8)
     logits = x @ w_r.T
     if logit_bias is not None:
@@ -143,12 +151,16 @@ def select_top_k(logits, k: int) -> np.ndarray:
     return ids
 
 
-def routing_weights(logits, ids) -> np.ndarray:
-    """softmax over the selected logits of each token, float64 [T, k]."""
+def routing_weights(logits, ids, per_expert_scale=None) -> np.ndarray:
+    """softmax over the selected logits of each token, float64 [T, k], times
+    per_expert_scale[id] of each selected expert when given."""
     lg = np.take_along_axis(np.asarray(logits, dtype=np.float64), np.asarray(ids), axis=1)
     m = lg.max(axis=1, keepdims=True)
     e = np.exp(lg - m)
-    return e / e.sum(axis=1, keepdims=True)
+    w = e / e.sum(axis=1, keepdims=True)
+    if per_expert_scale is not None:
+        w = w * np.asarray(per_expert_scale, dtype=np.float64)[np.asarray(ids)]
+    return w
 
 
 # ------------------------------------------------------------- experts
@@ -202,7 +214,8 @@ def route_sort(ids, n_experts: int):
 
 
 # ------------------------------------------------------------- block
-def moe_block(x_bits, router: dict, get_expert, shared: dict, k: int, logit_bias=None, ids=None):
+def moe_block(x_bits, router: dict, get_expert, shared: dict, k: int, logit_bias=None, ids=None,
+              router_scale=None, per_expert_scale=None):
     """One MoE FFN block on bf16 hidden rows x [T, H].
 
     get_expert(e) -> expert dict (q/s/b of gate, up, down); shared likewise.
@@ -211,11 +224,11 @@ def moe_block(x_bits, router: dict, get_expert, shared: dict, k: int, logit_bias
 
     Returns dict: logits [T,E], ids [T,k], weights [T,k], y [T,H] float64,
     y_bf16 bits [T,H]."""
-    logits = router_logits(x_bits, router, logit_bias)
+    logits = router_logits(x_bits, router, logit_bias, router_scale)
     if ids is None:
         ids = select_top_k(logits, k)
     ids = np.asarray(ids, dtype=np.int64)
-    weights = routing_weights(logits, ids)
+    weights = routing_weights(logits, ids, per_expert_scale)
     y = expert_mix(x_bits, ids, weights, get_expert, shared)
     return {"logits": logits, "ids": ids, "weights": weights, "y": y, "y_bf16": f64_to_bf16(y)}
 

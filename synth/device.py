@@ -65,7 +65,7 @@ class DeviceLayer:
     """All weights of one synthetic MoE layer in one device buffer."""
 
     def __init__(self, layer_seed: int, hidden: int, inter: int, n_experts: int, device="cuda",
-                 zipf: bool = False, threads: int = 8):
+                 zipf: bool = False, threads: int = 8, router_scales: bool = False):
         import torch
         self.seed = layer_seed
         self.hidden, self.inter, self.n_experts = hidden, inter, n_experts
@@ -116,6 +116,11 @@ class DeviceLayer:
         self.logit_bias = None
         if zipf:
             self.logit_bias = torch.from_numpy(gen.zipf_logit_bias(layer_seed, n_experts)).to(self.buf.device)
+        self.router_scale = self.per_expert_scale = None
+        if router_scales:
+            rs, pes = gen.router_scales(layer_seed, n_experts, hidden)
+            self.router_scale = torch.from_numpy(rs.view(np.int16).copy()).to(self.buf.device)
+            self.per_expert_scale = torch.from_numpy(pes).to(self.buf.device)
         torch.cuda.synchronize(self.buf.device)
 
     def _mats(self):
@@ -139,6 +144,8 @@ class DeviceLayer:
             "shared": base + self.shared_off,
             "layout": {k: v for k, v in self.bl.items() if k not in ("bytes", "stride")},
             "logit_bias": None if self.logit_bias is None else self.logit_bias.data_ptr(),
+            "router_scale": None if self.router_scale is None else self.router_scale.data_ptr(),
+            "per_expert_scale": None if self.per_expert_scale is None else self.per_expert_scale.data_ptr(),
         }
 
     # host copies for the oracle (regenerated, never read back from the device)
@@ -150,6 +157,12 @@ class DeviceLayer:
 
     def host_shared(self) -> dict:
         return gen.expert_weights(self.seed, gen.SHARED_ID, self.hidden, self.inter)
+
+    def host_router_scales(self):
+        """(router_scale bf16 bits [H], per_expert_scale float32 [E]), or (None, None)."""
+        if self.router_scale is None:
+            return None, None
+        return gen.router_scales(self.seed, self.n_experts, self.hidden)
 
     def host_logit_bias(self):
         return None if self.logit_bias is None else gen.zipf_logit_bias(self.seed, self.n_experts)

@@ -52,6 +52,7 @@ M2 = 0x94D049BB133111EB
 STREAM_WEIGHTS = 1
 STREAM_INPUT = 2
 STREAM_ZIPF = 3
+STREAM_ROUTER_SCALES = 4  # learned router scales of the optional-scale tests
 # weight tuple fields
 ROUTER_ID = 2000          # "expert" slot of the router projection
 SHARED_ID = 1000          # "expert" slot of the dense shared expert
@@ -189,6 +190,15 @@ def zipf_logit_bias(layer_seed: int, n_experts: int, s: float = 1.1, top: float 
         perm[i], perm[j] = perm[j], perm[i]
     rank = 1.0 + np.asarray(perm, dtype=np.float64)
     return (top * rank ** (-s)).astype(np.float32)
+
+
+def router_scales(layer_seed: int, n_experts: int, hidden: int):
+    """Learned router scales for the tests of that option: router_scale bf16
+    bits [H] = bf16(sqrt(H) * U(0.5, 1.5)) (so x * scale / sqrt(H) stays near
+    x) and per_expert_scale float32 [E] = U(0.5, 1.5)."""
+    u = uniform(stream_key(STREAM_ROUTER_SCALES, layer_seed, 0), hidden)
+    v = uniform(stream_key(STREAM_ROUTER_SCALES, layer_seed, 1), n_experts)
+    return to_bf16_bits(np.sqrt(hidden) * (0.5 + u)), (0.5 + v).astype(np.float32)
 
 
 # ---------------------------------------------------------------- inputs

@@ -69,8 +69,9 @@ class HostExperts:
 
 def oracle_layer(layer: DeviceLayer, x_bits, k, ids, experts: HostExperts | None = None):
     experts = experts or HostExperts(layer)
+    rs, pes = layer.host_router_scales()
     return O.moe_block(x_bits, layer.host_router(), experts, layer.host_shared(), k,
-                       layer.host_logit_bias(), ids=ids)
+                       layer.host_logit_bias(), ids=ids, router_scale=rs, per_expert_scale=pes)
 
 
 def hidden(seed: int, chunk: int, n_tokens: int, hidden_dim: int = H, rms: bool = True) -> np.ndarray:

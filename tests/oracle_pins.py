@@ -20,6 +20,8 @@ What pins what:
                        batch invariance, exact doubling of W_down
   pin_route_sort       stable counting sort vs numpy's stable argsort
   pin_rmsnorm          closed-form rows
+  pin_router_scales    scaled router vs brute force on exactly scaled rows,
+                       per-expert scales on the softmax, zero / doubled scales
 """
 from __future__ import annotations
 
@@ -291,5 +293,43 @@ def pin_rmsnorm(o):
     assert np.all(o.rmsnorm_no_scale(zero) == 0)
 
 
+def pin_router_scales(o):
+    """The learned router scale and per-expert scales (page "TurboFieldfare -
+    System design", section "Decode", router description)."""
+    hidden, inter, n_experts, k, t = 256, 64, 8, 3, 4      # sqrt(hidden) = 16 exactly
+    router, experts, shared = _tiny_layer(31, hidden, inter, n_experts)
+    x = gen.hidden_states(31, 0, t, hidden, rms_normalize=True)
+    # router_scale = 16 * 2^j per feature: x * scale / 16 is x * 2^j, an exact
+    # bf16 value, so the scaled router equals the brute-force router on that row
+    j = np.random.default_rng(3).integers(-2, 3, size=hidden)
+    rs = np.array([_bf16_bits_exact(16.0 * 2.0 ** int(v)) for v in j], dtype=np.uint16)
+    got = o.router_logits(x, router, router_scale=rs)
+    rr = router_rows(router)
+    for ti in range(t):
+        xs = [_brute.bf16(v) * 2.0 ** int(e) for v, e in zip(x[ti].tolist(), j)]
+        ref = _brute.matvec(rr, 8, xs)
+        assert np.max(np.abs(got[ti] - np.array(ref))) <= 1e-12 * max(1.0, max(abs(a) for a in ref))
+    # a constant scale of 16 is the identity
+    same = np.full(hidden, _bf16_bits_exact(16.0), dtype=np.uint16)
+    assert np.array_equal(o.router_logits(x, router, router_scale=same), o.router_logits(x, router))
+    # per-expert scales multiply the softmax weight of each selected expert
+    pes = (0.5 + np.random.default_rng(4).random(n_experts)).astype(np.float32)
+    base = o.moe_block(x, router, lambda e: experts[e], shared, k)
+    sc = o.moe_block(x, router, lambda e: experts[e], shared, k, per_expert_scale=pes)
+    assert np.array_equal(sc["ids"], base["ids"])
+    for ti in range(t):
+        lg = [float(base["logits"][ti, e]) for e in base["ids"][ti]]
+        ex = [math.exp(v - max(lg)) for v in lg]
+        want = [a / sum(ex) * float(pes[e]) for a, e in zip(ex, base["ids"][ti])]
+        assert np.max(np.abs(sc["weights"][ti] - np.array(want))) <= 1e-14
+    # zero scales leave the shared expert alone; doubling them doubles the routed part
+    zero = o.moe_block(x, router, lambda e: experts[e], shared, k, per_expert_scale=np.zeros(n_experts, np.float32))
+    sh = o.expert_ffn(o.bf16_to_f64(x), o.dense_expert(shared))
+    assert np.max(np.abs(zero["y"] - sh)) <= 1e-13 * np.max(np.abs(sh))
+    two = o.moe_block(x, router, lambda e: experts[e], shared, k, per_expert_scale=np.full(n_experts, 2.0, np.float32))
+    assert np.max(np.abs((two["y"] - sh) - 2.0 * (base["y"] - sh))) <= 1e-12 * np.max(np.abs(base["y"]))
+
+
 ALL_PINS = [pin_layout_sizes, pin_dequant_golden, pin_bf16_rounding, pin_gelu, pin_topk, pin_softmax_full,
-            pin_integer_layer, pin_brute_force, pin_invariants, pin_route_sort, pin_rmsnorm]
+            pin_integer_layer, pin_brute_force, pin_invariants, pin_route_sort, pin_rmsnorm,
+            pin_router_scales]

@@ -41,9 +41,10 @@ def layer0_zipf():
 def _check_routing(out, layer, x_bits, k):
     ids, logits = out["ids"], out["logits"]
     assert np.array_equal(ids, O.select_top_k(logits, k)), "ids differ from the top-k of the GPU's own logits"
-    ref_logits = O.router_logits(x_bits, layer.host_router(), layer.host_logit_bias())
+    rs, pes = layer.host_router_scales()
+    ref_logits = O.router_logits(x_bits, layer.host_router(), layer.host_logit_bias(), rs)
     assert_close(logits, ref_logits, "logits")
-    assert_close(out["weights"], O.routing_weights(logits.astype(np.float64), ids), "routing weights")
+    assert_close(out["weights"], O.routing_weights(logits.astype(np.float64), ids, pes), "routing weights")
 
 
 @pytest.mark.parametrize("n_tokens,zipf", [(1, False), (13, False), (64, False), (100, True), (128, True)],
@@ -267,6 +268,53 @@ def test_fused_and_chained_paths_agree(layer0, layer0_zipf, residual, n_tokens):
         outs[fused] = out
         m.close()
     assert np.array_equal(outs["1"]["ids"], outs["0"]["ids"])
+
+
+@pytest.fixture(scope="module")
+def layer0_scaled():
+    return DeviceLayer(0, H, I, E, zipf=True, router_scales=True)
+
+
+@pytest.mark.parametrize("fused", ["1", "0"])
+@pytest.mark.parametrize("n_tokens", [1, 37, 128])
+def test_router_scales(layer0_scaled, n_tokens, fused):
+    """The learned router scale (x * router_scale / sqrt(H) into the router) and
+    the per-expert scales (softmax weight times the selected expert's scale),
+    on the fused kernels and on the chained launches."""
+    import os
+    var = "MOE_DECODE_FUSED" if n_tokens == 1 else "MOE_PREFILL_FUSED"
+    old = os.environ.get(var)
+    os.environ[var] = fused
+    try:
+        m = bq.Moe()
+    finally:
+        if old is None:
+            del os.environ[var]
+        else:
+            os.environ[var] = old
+    try:
+        x = hidden(31, n_tokens, n_tokens)
+        out = run_layer(m, layer0_scaled, x)
+        assert out["status"] == bq.MOE_OK
+        _check_routing(out, layer0_scaled, x, K)
+        # the scales change the routing: compare with the same layer unscaled
+        plain = O.select_top_k(O.router_logits(x, layer0_scaled.host_router(), layer0_scaled.host_logit_bias()), K)
+        assert not np.array_equal(plain, out["ids"])
+        ref = oracle_layer(layer0_scaled, x, K, out["ids"])
+        assert_close(bf16_bits_to_f64(out["y"]), ref["y"], f"y with router scales (T={n_tokens}, fused={fused})")
+    finally:
+        m.close()
+
+
+@pytest.mark.parametrize("hidden_dim,inter,n_experts,k,n_tokens", [(128, 64, 8, 2, 1), (192, 128, 16, 8, 17)])
+def test_router_scales_small_shapes(moe, hidden_dim, inter, n_experts, k, n_tokens):
+    layer = DeviceLayer(9, hidden_dim, inter, n_experts, router_scales=True)
+    x = hidden(9, n_tokens, n_tokens, hidden_dim)
+    out = run_layer(moe, layer, x, k)
+    assert out["status"] == bq.MOE_OK
+    _check_routing(out, layer, x, k)
+    ref = oracle_layer(layer, x, k, out["ids"])
+    assert_close(bf16_bits_to_f64(out["y"]), ref["y"], "small-shape y with router scales")
 
 
 def test_argument_errors(moe, layer0):

@@ -28,6 +28,9 @@ MUTATIONS = {
     "unstable_sort": ("for p, e in enumerate(flat):", "for p, e in reversed(list(enumerate(flat))):"),
     "rms_without_eps": ("np.mean(h * h, axis=1, keepdims=True) + eps", "np.mean(h * h, axis=1, keepdims=True)"),
     "bf16_truncation": ("keep = keep + up.astype(np.uint64)", "keep = keep"),
+    "router_scale_not_normalised": ("bf16_to_f64(router_scale)[None, :] / np.sqrt(x.shape[1])", "bf16_to_f64(router_scale)[None, :]"),
+    "router_scale_transposed": ("bf16_to_f64(router_scale)[None, :]", "bf16_to_f64(router_scale)[::-1][None, :]"),
+    "per_expert_scale_dropped": ("w = w * np.asarray(per_expert_scale, dtype=np.float64)[np.asarray(ids)]", "w = w"),
     "router_bias_dropped": ("logits = logits + np.asarray(logit_bias", "logits = logits + 0 * np.asarray(logit_bias"),
 }
 
