@@ -44,7 +44,12 @@ Readings where the pages are silent (listed again in the design notes):
   * y = sum_j w_j * o_j (j in selection order) + o_shared, float64; the
     block's bf16 output is the round-to-nearest-even of that value;
   * stacked layers: x_l = bf16(rmsnorm_no_scale(h_l)), eps = 1e-6,
-    h_{l+1} = bf16(h_l + bf16(y_l)).
+    h_{l+1} = bf16(h_l + bf16(y_l));
+  * the layer tail (section "Decode", cb2 phase: after the combine, the
+    post-FFN norms, the residual and a learned layer scalar), when a layer
+    has one: one RMS norm with a learned per-feature weight g on the combined
+    output y (eps 1e-6), then the residual add, then the scalar lambda:
+    h_{l+1} = bf16(lambda * bf16(h_l + bf16(g * y / rms(y)))).
 """
 from __future__ import annotations
 
@@ -267,6 +272,27 @@ def rmsnorm_no_scale(h_bits, eps: float = RMS_EPS) -> np.ndarray:
 def residual_add(h_bits, y_bf16_bits) -> np.ndarray:
     """bf16(h + y) with y the block's bf16 output."""
     return f64_to_bf16(bf16_to_f64(h_bits) + bf16_to_f64(y_bf16_bits))
+
+
+def post_ffn_norm(y_bits, post_norm_bits, eps: float = RMS_EPS) -> np.ndarray:
+    """z = y / sqrt(mean(y^2) + eps) * g per row, float64 [T, H]; y the block's
+    bf16 output, g the learned norm weight (bf16 bits [H])."""
+    y = bf16_to_f64(y_bits)
+    r = np.sqrt(np.mean(y * y, axis=1, keepdims=True) + eps)
+    return y / r * bf16_to_f64(post_norm_bits)[None, :]
+
+
+def layer_tail(h_bits, y_bits, post_norm_bits=None, layer_scalar=None) -> np.ndarray:
+    """The layer tail after the combine (section "Decode", cb2 phase): post-FFN
+    norm, residual, layer scalar.  Each step's result is a bf16 tensor:
+    z = bf16(post_ffn_norm(y)) (z = y without a norm weight),
+    s = bf16(h + z), h' = bf16(layer_scalar * s) (h' = s without a scalar).
+    Returns bf16 bits [T, H]."""
+    z = y_bits if post_norm_bits is None else f64_to_bf16(post_ffn_norm(y_bits, post_norm_bits))
+    s = f64_to_bf16(bf16_to_f64(h_bits) + bf16_to_f64(z))
+    if layer_scalar is None:
+        return s
+    return f64_to_bf16(float(np.float32(layer_scalar)) * bf16_to_f64(s))
 
 
 def stack_layer(h_bits, router, get_expert, shared, k: int, logit_bias=None, ids=None):

@@ -22,6 +22,8 @@ What pins what:
   pin_rmsnorm          closed-form rows
   pin_router_scales    scaled router vs brute force on exactly scaled rows,
                        per-expert scales on the softmax, zero / doubled scales
+  pin_layer_tail       closed forms, eps on small rows, a plain-Python brute force
+                       with hand rounding, zero rows and weights
 """
 from __future__ import annotations
 
@@ -330,6 +332,52 @@ def pin_router_scales(o):
     assert np.max(np.abs((two["y"] - sh) - 2.0 * (base["y"] - sh))) <= 1e-12 * np.max(np.abs(base["y"]))
 
 
+def _rne_bf16(v: float) -> float:
+    """Round a float to the nearest bf16 value (ties to even), in plain Python:
+    v / 2^(e-7) is exact, and round() on a float rounds half to even."""
+    if v == 0.0 or not math.isfinite(v):
+        return v
+    e = math.frexp(v)[1] - 1
+    step = 2.0 ** (e - 7)
+    return round(v / step) * step
+
+
+def pin_layer_tail(o):
+    """Post-FFN norm, residual and layer scalar (page "TurboFieldfare - System
+    design", section "Decode", cb2 phase)."""
+    f = o.f64_to_bf16
+    # closed form: y = 2 everywhere -> y / rms(y) rounds to 1; 0.5 + 1 = 1.5; 2 * 1.5 = 3
+    y, h, g = f(np.full((1, 64), 2.0)), f(np.full((1, 64), 0.5)), f(np.ones(64))
+    assert np.all(o.bf16_to_f64(o.layer_tail(h, y, g, 2.0)) == 3.0)
+    # eps matters for small rows: c / sqrt(c^2 + 1e-6)
+    c = float(o.bf16_to_f64(f(np.array([1e-3])))[0])
+    want = _rne_bf16(c / math.sqrt(c * c + 1e-6))
+    got = o.bf16_to_f64(o.layer_tail(f(np.zeros((1, 64))), f(np.full((1, 64), c)), g))
+    assert np.all(got == want) and abs(want - 0.7071) < 0.01
+    # brute force on random rows: plain-Python sums, hand rounding
+    rng = np.random.default_rng(17)
+    hb, yb = f(rng.normal(size=(3, 64))), f(rng.normal(size=(3, 64)) * 0.3)
+    gb = f(0.5 + rng.random(64))
+    lam = float(np.float32(0.5 + rng.random()))
+    got = o.bf16_to_f64(o.layer_tail(hb, yb, gb, lam))
+    for t in range(3):
+        yr = [_brute.bf16(v) for v in yb[t].tolist()]
+        rms = math.sqrt(math.fsum(v * v for v in yr) / 64 + 1e-6)
+        for j in range(64):
+            z = _rne_bf16(yr[j] / rms * _brute.bf16(int(gb[j])))
+            sj = _rne_bf16(_brute.bf16(int(hb[t, j])) + z)
+            assert got[t, j] == _rne_bf16(lam * sj), (t, j)
+    # y = 0 leaves lambda * h; a zero norm weight leaves lambda * h on that feature
+    zero = o.layer_tail(hb, f(np.zeros((3, 64))), gb, lam)
+    assert np.array_equal(o.bf16_to_f64(zero), np.vectorize(_rne_bf16)(lam * o.bf16_to_f64(hb)))
+    g0 = gb.copy()
+    g0[5] = 0
+    one = o.bf16_to_f64(o.layer_tail(hb, yb, g0, lam))
+    assert np.array_equal(one[:, 5], np.vectorize(_rne_bf16)(lam * o.bf16_to_f64(hb[:, 5])))
+    # no norm weight and no scalar: the plain residual add
+    assert np.array_equal(o.layer_tail(hb, yb), o.residual_add(hb, yb))
+
+
 ALL_PINS = [pin_layout_sizes, pin_dequant_golden, pin_bf16_rounding, pin_gelu, pin_topk, pin_softmax_full,
             pin_integer_layer, pin_brute_force, pin_invariants, pin_route_sort, pin_rmsnorm,
-            pin_router_scales]
+            pin_router_scales, pin_layer_tail]

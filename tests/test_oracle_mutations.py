@@ -31,6 +31,11 @@ MUTATIONS = {
     "router_scale_not_normalised": ("bf16_to_f64(router_scale)[None, :] / np.sqrt(x.shape[1])", "bf16_to_f64(router_scale)[None, :]"),
     "router_scale_transposed": ("bf16_to_f64(router_scale)[None, :]", "bf16_to_f64(router_scale)[::-1][None, :]"),
     "per_expert_scale_dropped": ("w = w * np.asarray(per_expert_scale, dtype=np.float64)[np.asarray(ids)]", "w = w"),
+    "tail_scalar_dropped": ("return f64_to_bf16(float(np.float32(layer_scalar)) * bf16_to_f64(s))", "return s"),
+    "tail_norm_weight_dropped": ("return y / r * bf16_to_f64(post_norm_bits)[None, :]", "return y / r"),
+    "tail_norm_sum_not_mean": ("np.sqrt(np.mean(y * y, axis=1, keepdims=True) + eps)", "np.sqrt(np.sum(y * y, axis=1, keepdims=True) + eps)"),
+    "tail_eps_dropped": ("np.sqrt(np.mean(y * y, axis=1, keepdims=True) + eps)", "np.sqrt(np.mean(y * y, axis=1, keepdims=True))"),
+    "tail_residual_dropped": ("s = f64_to_bf16(bf16_to_f64(h_bits) + bf16_to_f64(z))", "s = f64_to_bf16(bf16_to_f64(z))"),
     "router_bias_dropped": ("logits = logits + np.asarray(logit_bias", "logits = logits + 0 * np.asarray(logit_bias"),
 }
 
