@@ -49,7 +49,8 @@ class BlobLayout(ctypes.Structure):
 class LayerWeights(ctypes.Structure):
     _fields_ = [("dims", Dims), ("router", QMat), ("experts", ctypes.c_void_p), ("expert_stride", ctypes.c_size_t),
                 ("layout", BlobLayout), ("shared", ctypes.c_void_p), ("logit_bias", ctypes.c_void_p),
-                ("router_scale", ctypes.c_void_p), ("per_expert_scale", ctypes.c_void_p)]
+                ("router_scale", ctypes.c_void_p), ("per_expert_scale", ctypes.c_void_p),
+                ("post_norm", ctypes.c_void_p), ("layer_scalar", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -134,11 +135,11 @@ def make_dims(hidden: int, inter: int, n_experts: int, top_k: int, group: int = 
 
 def make_layer_weights(dims: Dims, router_q: int, router_s: int, router_b: int, experts: int, expert_stride: int,
                        layout: dict, shared: int, logit_bias=None, router_scale=None,
-                       per_expert_scale=None) -> LayerWeights:
+                       per_expert_scale=None, post_norm=None, layer_scalar=None) -> LayerWeights:
     """LayerWeights from device addresses; `layout` maps gate_q .. down_b to byte offsets."""
     return LayerWeights(dims, QMat(router_q, router_s, router_b), experts, expert_stride,
                         BlobLayout(*[layout[n] for n in _BLOB_FIELDS]), shared, _ptr(logit_bias),
-                        _ptr(router_scale), _ptr(per_expert_scale))
+                        _ptr(router_scale), _ptr(per_expert_scale), _ptr(post_norm), _ptr(layer_scalar))
 
 
 def layer_forward_static(x, w: LayerWeights, y, ids_out=None, logits_out=None, weights_out=None, stream=None):
@@ -231,7 +232,9 @@ class Moe:
 
 def layer_weights_from(dims: Dims, addr: dict) -> LayerWeights:
     """LayerWeights from a dict with router_q/router_s/router_b/experts/stride/
-    shared/layout/logit_bias entries (device addresses and byte offsets)."""
+    shared/layout entries and optional logit_bias/router_scale/per_expert_scale/
+    post_norm/layer_scalar entries (device addresses and byte offsets)."""
     return make_layer_weights(dims, addr["router_q"], addr["router_s"], addr["router_b"], addr["experts"],
                               addr["stride"], addr["layout"], addr["shared"], addr.get("logit_bias"),
-                              addr.get("router_scale"), addr.get("per_expert_scale"))
+                              addr.get("router_scale"), addr.get("per_expert_scale"), addr.get("post_norm"),
+                              addr.get("layer_scalar"))

@@ -82,7 +82,7 @@ size_t blob_extent(const moe_layer_weights &w) {
 }
 
 struct WsLayout {
-  size_t logits, ids, wts, counts, offsets, perm, pos, act_e, act_beg, act_cnt, n_act, xn, h, o, xq, hq, total;
+  size_t logits, ids, wts, counts, offsets, perm, pos, act_e, act_beg, act_cnt, n_act, xn, h, o, xq, hq, y, total;
 };
 
 WsLayout ws_layout(const moe_dims &d, int T) {
@@ -111,6 +111,7 @@ WsLayout ws_layout(const moe_dims &d, int T) {
   // quarter sums of the fused prefill kernel (its operand rows reuse xn and h)
   L.xq = T > 1 ? take((size_t)T * 4 * ((H / 64 + 15) & ~(size_t)15)) : off;  // x group sums, bf16 hi/lo
   L.hq = T > 1 ? take(((size_t)T * k + T) * (I / 16) * 4) : off;
+  L.y = take((size_t)T * H * 2);  // block output ahead of a layer tail
   L.total = off;
   return L;
 }
@@ -140,6 +141,8 @@ int check_weights_impl(const moe_layer_weights *w) {
   if (w->logit_bias && !aligned(w->logit_bias, 4)) return MOE_ERR_INVALID_ARG;
   if (w->router_scale && !aligned(w->router_scale, 16)) return MOE_ERR_INVALID_ARG;
   if (w->per_expert_scale && !aligned(w->per_expert_scale, 4)) return MOE_ERR_INVALID_ARG;
+  if (w->post_norm && !aligned(w->post_norm, 16)) return MOE_ERR_INVALID_ARG;
+  if (w->layer_scalar && !aligned(w->layer_scalar, 4)) return MOE_ERR_INVALID_ARG;
   const size_t offs[9] = {w->layout.gate_q, w->layout.gate_s, w->layout.gate_b, w->layout.up_q, w->layout.up_s,
                           w->layout.up_b,   w->layout.down_q, w->layout.down_s, w->layout.down_b};
   for (size_t o : offs)
@@ -174,7 +177,7 @@ int check_ws(const moe_dims &d, int T, const void *ws, size_t ws_bytes) {
 }
 
 int run_router(moe_handle *h, const moe_layer_weights *w, int T, const void *x, void *hres, void *x_out,
-               float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st) {
+               float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st, bool normalize) {
   const WsLayout L = ws_layout(w->dims, T);
   moe::RouterArgs a;
   a.w = layer_ptrs(*w);
@@ -190,7 +193,7 @@ int run_router(moe_handle *h, const moe_layer_weights *w, int T, const void *x, 
   a.counter = h->dwords + 1;
   a.err = h->dwords;
   a.trace = take_trace(h, 1);
-  a.normalize = hres != nullptr;
+  a.normalize = normalize;
   a.prefetch_bytes_max = h->prefetch_max;
   return cuda_status(moe::launch_router(a, st, h->pdl));
 }
@@ -209,7 +212,7 @@ bool use_fused(moe_handle *h, const moe_layer_weights *w, int T) {
 }
 
 int run_fused(moe_handle *h, const moe_layer_weights *w, const void *x, void *hres, void *y, void *x_out,
-              float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st) {
+              float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st, bool normalize) {
   const WsLayout L = ws_layout(w->dims, 1);
   moe::DecodeArgs a;
   a.w = layer_ptrs(*w);
@@ -226,7 +229,7 @@ int run_fused(moe_handle *h, const moe_layer_weights *w, const void *x, void *hr
   a.mbox = reinterpret_cast<unsigned long long *>(h->dwords + kMboxOffset);
   a.err = h->dwords;
   a.trace = take_trace(h, 1);
-  a.normalize = hres != nullptr;
+  a.normalize = normalize;
   return cuda_status(moe::launch_decode_fused(a, h->n_sm, st, h->pdl));
 }
 
@@ -243,7 +246,7 @@ bool use_prefill(moe_handle *h, const moe_layer_weights *w, int T) {
 }
 
 int run_prefill(moe_handle *h, const moe_layer_weights *w, int T, const void *x, void *hres, void *y, void *x_out,
-                float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st) {
+                float *logits, int32_t *ids, float *wts, uint8_t *ws, cudaStream_t st, bool normalize) {
   const WsLayout L = ws_layout(w->dims, T);
   moe::PrefillArgs a;
   a.w = layer_ptrs(*w);
@@ -264,7 +267,7 @@ int run_prefill(moe_handle *h, const moe_layer_weights *w, int T, const void *x,
   a.sync = h->dwords + kPrefillSyncOffset;
   a.err = h->dwords;
   a.trace = take_trace(h, 1);
-  a.normalize = hres != nullptr;
+  a.normalize = normalize;
   return cuda_status(moe::launch_prefill_fused(a, h->n_sm, st, h->pdl));
 }
 
@@ -367,7 +370,8 @@ int moe_router_topk(moe_handle *h, const void *x, int n_tokens, const moe_layer_
   if ((st = check_tokens(n_tokens))) return st;
   if (!aligned(x, 16) || (logits && !aligned(logits, 16))) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
-  return run_router(h, w, n_tokens, x, nullptr, nullptr, logits, ids, weights, (uint8_t *)ws, (cudaStream_t)stream);
+  return run_router(h, w, n_tokens, x, nullptr, nullptr, logits, ids, weights, (uint8_t *)ws, (cudaStream_t)stream,
+                    false);
 }
 
 int moe_route_sort(moe_handle *h, const int32_t *ids, int n_tokens, const moe_dims *dims, int32_t *counts,
@@ -431,12 +435,13 @@ int moe_layer_forward(moe_handle *h, const void *x, int n_tokens, const moe_laye
   if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
   uint8_t *wsb = (uint8_t *)ws;
   if (use_fused(h, w, n_tokens))
-    return run_fused(h, w, x, nullptr, y, nullptr, logits_out, ids_out, weights_out, wsb, (cudaStream_t)stream);
+    return run_fused(h, w, x, nullptr, y, nullptr, logits_out, ids_out, weights_out, wsb, (cudaStream_t)stream,
+                     false);
   if (use_prefill(h, w, n_tokens))
     return run_prefill(h, w, n_tokens, x, nullptr, y, nullptr, logits_out, ids_out, weights_out, wsb,
-                       (cudaStream_t)stream);
+                       (cudaStream_t)stream, false);
   if ((st = run_router(h, w, n_tokens, x, nullptr, nullptr, logits_out, ids_out, weights_out, wsb,
-                       (cudaStream_t)stream)))
+                       (cudaStream_t)stream, false)))
     return st;
   return run_ffn(h, w, n_tokens, x, routing_in(wsb, ws_layout(w->dims, n_tokens)), 1, y, nullptr, wsb,
                  (cudaStream_t)stream);
@@ -455,15 +460,29 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens, const 
   if ((st = check_ws(w->dims, n_tokens, ws, ws_bytes))) return st;
   uint8_t *wsb = (uint8_t *)ws;
   const WsLayout L = ws_layout(w->dims, n_tokens);
+  const cudaStream_t s = (cudaStream_t)stream;
+  // With a layer tail the block reads the residual stream as its input only
+  // (x = hidden, normalised), writes y, and the tail launch updates hidden.
+  const bool tail = w->post_norm != nullptr || w->layer_scalar != nullptr;
+  void *res = tail ? nullptr : hidden;
+  const void *xin = tail ? hidden : nullptr;
+  void *yb = tail && !y_out ? (void *)(wsb + L.y) : y_out;
   if (use_fused(h, w, n_tokens))
-    return run_fused(h, w, nullptr, hidden, y_out, x_out, logits_out, ids_out, nullptr, wsb, (cudaStream_t)stream);
-  if (use_prefill(h, w, n_tokens))
-    return run_prefill(h, w, n_tokens, nullptr, hidden, y_out, x_out, logits_out, ids_out, nullptr, wsb,
-                       (cudaStream_t)stream);
-  if ((st = run_router(h, w, n_tokens, nullptr, hidden, x_out, logits_out, ids_out, nullptr, wsb,
-                       (cudaStream_t)stream)))
-    return st;
-  return run_ffn(h, w, n_tokens, wsb + L.xn, routing_in(wsb, L), 1, y_out, hidden, wsb, (cudaStream_t)stream);
+    st = run_fused(h, w, xin, res, yb, x_out, logits_out, ids_out, nullptr, wsb, s, true);
+  else if (use_prefill(h, w, n_tokens))
+    st = run_prefill(h, w, n_tokens, xin, res, yb, x_out, logits_out, ids_out, nullptr, wsb, s, true);
+  else if (!(st = run_router(h, w, n_tokens, xin, res, x_out, logits_out, ids_out, nullptr, wsb, s, true)))
+    st = run_ffn(h, w, n_tokens, wsb + L.xn, routing_in(wsb, L), 1, yb, res, wsb, s);
+  if (st || !tail) return st;
+  moe::TailArgs ta;
+  ta.y = (const uint16_t *)yb;
+  ta.h = (uint16_t *)hidden;
+  ta.post_norm = (const uint16_t *)w->post_norm;
+  ta.layer_scalar = w->layer_scalar;
+  ta.T = n_tokens;
+  ta.H = w->dims.hidden;
+  ta.trace = take_trace(h, 1);
+  return cuda_status(moe::launch_tail(ta, s, h->pdl));
 }
 
 int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe_layer_weights *layers, void *ws,

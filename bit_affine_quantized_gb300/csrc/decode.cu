@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   // (dot * 1/rms) goes out before the operand rows are staged.
   uint32_t qin[8];
   float qss = 0.f, lg = 0.f;
-  const uint16_t *src = a.normalize ? a.hres : a.x;
+  const uint16_t *src = a.hres ? a.hres : a.x;
   if (tid < nquart) {
     const uint4 v0 = __ldcg(reinterpret_cast<const uint4 *>(src) + 2 * tid);
     const uint4 v1 = __ldcg(reinterpret_cast<const uint4 *>(src) + 2 * tid + 1);

@@ -12,8 +12,8 @@ namespace moe {
 struct RouterArgs {
   LayerPtrs w;
   Dims d;
-  const uint16_t *x;       // bf16 [T, H] block input (normalize == 0)
-  uint16_t *hres;          // bf16 [T, H] residual stream (normalize == 1)
+  const uint16_t *x;       // bf16 [T, H] block input (normalised first when normalize == 1 and hres is null)
+  uint16_t *hres;          // nullable bf16 [T, H] residual stream (normalize == 1)
   uint16_t *xn;            // bf16 [T, H] normalised input out (normalize == 1)
   uint16_t *xn_user;       // nullable copy of xn
   float *logits;           // fp32 [T, E]
@@ -55,8 +55,8 @@ struct SortArgs {
 struct DecodeArgs {
   LayerPtrs w;
   Dims d;                   // T == 1
-  const uint16_t *x;        // bf16 [H] block input (normalize == 0)
-  uint16_t *hres;           // bf16 [H] residual stream (normalize == 1), updated in place
+  const uint16_t *x;        // bf16 [H] block input (normalised first when normalize == 1 and hres is null)
+  uint16_t *hres;           // nullable bf16 [H] residual stream (normalize == 1), updated in place
   uint16_t *xn_user;        // nullable: normalised input out
   float *logits;            // fp32 [E] (user buffer or workspace)
   int32_t *ids_user;        // nullable [k]
@@ -74,8 +74,8 @@ struct DecodeArgs {
 struct PrefillArgs {
   LayerPtrs w;
   Dims d;
-  const uint16_t *x;        // bf16 [T, H] block input (normalize == 0)
-  uint16_t *hres;           // bf16 [T, H] residual stream (normalize == 1), updated in place
+  const uint16_t *x;        // bf16 [T, H] block input (normalised first when normalize == 1 and hres is null)
+  uint16_t *hres;           // nullable bf16 [T, H] residual stream (normalize == 1), updated in place
   uint16_t *xn_user;        // nullable: normalised input out
   float *logits;            // fp32 [T, E] (user buffer or workspace)
   int32_t *ids_user;        // nullable [T, k]
@@ -92,6 +92,17 @@ struct PrefillArgs {
   unsigned long long *trace;
   int normalize;
 };
+
+// Layer tail (tail.cu): post-FFN norm, residual, layer scalar; one block per token.
+struct TailArgs {
+  const uint16_t *y;          // bf16 [T, H] block output
+  uint16_t *h;                // bf16 [T, H] residual stream, updated in place
+  const uint16_t *post_norm;  // nullable bf16 [H]: norm weight (null: no norm)
+  const float *layer_scalar;  // nullable fp32 [1] (null: 1)
+  int T, H;
+  unsigned long long *trace;
+};
+cudaError_t launch_tail(const TailArgs &a, cudaStream_t st, bool pdl);
 
 size_t prefill_fused_smem(const Dims &d);  // 0: shape not supported
 int prefill_blocks_per_sm(const Dims &d);

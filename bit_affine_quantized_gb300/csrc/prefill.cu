@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     if (lane == 0) fused::mbar_arrive_cnt(&empty[slot], 2);
   };
   auto gsync = [&]() { asm volatile("bar.sync %0, 256;" ::"r"(2 + gi) : "memory"); };
-  const uint16_t *src = a.normalize ? a.hres : a.x;
+  const uint16_t *src = a.hres ? a.hres : a.x;
   const int nquart = H / 16;
   const int r = lane >> 2, cq = lane & 3;
   int it = 0, xk = 0;

@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(const RouterArgs a) {
     for (int v = 0; v < kMaxVec; ++v) {
       const int idx = tid + kThreads * v;
       if (n < tb && idx < nvec) {
-        const uint16_t *src = (a.normalize ? a.hres : a.x) + (size_t)(t0 + n) * H;
+        const uint16_t *src = (a.hres ? a.hres : a.x) + (size_t)(t0 + n) * H;
         u[n][v] = *reinterpret_cast<const uint4 *>(src + 8 * idx);
       }
     }

@@ -121,6 +121,15 @@ typedef struct {
    *                     is softmax(...) * per_expert_scale[e]. */
   const void *router_scale;
   const float *per_expert_scale;
+  /* The layer tail (section "Decode", cb2 phase: post-FFN norm, residual,
+   * learned layer scalar), both nullable; read only by the residual calls
+   * (moe_layer_forward_residual, moe_layer_forward_stack):
+   *   post_norm     bf16 [H], 16-byte aligned: norm weight g of
+   *                 z = bf16(y / sqrt(mean(y^2) + 1e-6) * g) (null: z = y);
+   *   layer_scalar  fp32 [1] on the device: h <- bf16(layer_scalar * bf16(h + z))
+   *                 (null: h <- bf16(h + z)). */
+  const void *post_norm;
+  const float *layer_scalar;
 } moe_layer_weights;
 
 typedef struct moe_handle moe_handle;
@@ -187,9 +196,12 @@ int moe_layer_forward(moe_handle *h, const void *x, int n_tokens, const moe_laye
 /* One layer of a residual stack (the decode/prefill harness around the
  * block): x = bf16(h / sqrt(mean(h^2) + 1e-6)) (rmsnorm without scale, as
  * the router's input normalisation in section "Decode"); y = MoE(x);
- * h <- bf16(h + y) in place.
+ * h <- bf16(h + y) in place.  With a layer tail in w (post_norm and/or
+ * layer_scalar set), h <- bf16(lambda * bf16(h + bf16(g * y / rms(y))))
+ * instead, by one more launch after the block.
  *   hidden   bf16 [T, H] in/out
- *   y_out    nullable bf16 [T, H]: the block output before the add
+ *   y_out    nullable bf16 [T, H]: the block output before the add (and
+ *            before the tail)
  *   x_out    nullable bf16 [T, H]: the normalised block input */
 int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
                                const moe_layer_weights *w, void *y_out, void *x_out,
@@ -200,6 +212,7 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
  * step of the section "Decode": every layer's router input is the residual
  * stream normalised, its block output is added back):
  *   for l in 0 .. n_layers-1:  hidden <- bf16(hidden + MoE_l(rmsnorm(hidden)))
+ * (or layer l's tail around it, as in moe_layer_forward_residual)
  * with MoE_l the block of layers[l] (all with the same dims); the same
  * launches as n_layers calls of moe_layer_forward_residual with n_tokens = 1.
  *   hidden   bf16 [H] in/out;  layers: host array of n_layers weight sets;

@@ -65,7 +65,7 @@ class DeviceLayer:
     """All weights of one synthetic MoE layer in one device buffer."""
 
     def __init__(self, layer_seed: int, hidden: int, inter: int, n_experts: int, device="cuda",
-                 zipf: bool = False, threads: int = 8, router_scales: bool = False):
+                 zipf: bool = False, threads: int = 8, router_scales: bool = False, tail: bool = False):
         import torch
         self.seed = layer_seed
         self.hidden, self.inter, self.n_experts = hidden, inter, n_experts
@@ -121,6 +121,11 @@ class DeviceLayer:
             rs, pes = gen.router_scales(layer_seed, n_experts, hidden)
             self.router_scale = torch.from_numpy(rs.view(np.int16).copy()).to(self.buf.device)
             self.per_expert_scale = torch.from_numpy(pes).to(self.buf.device)
+        self.post_norm = self.layer_scalar = None
+        if tail:
+            g, lam = gen.layer_tail(layer_seed, hidden)
+            self.post_norm = torch.from_numpy(g.view(np.int16).copy()).to(self.buf.device)
+            self.layer_scalar = torch.tensor([lam], dtype=torch.float32, device=self.buf.device)
         torch.cuda.synchronize(self.buf.device)
 
     def _mats(self):
@@ -146,6 +151,8 @@ class DeviceLayer:
             "logit_bias": None if self.logit_bias is None else self.logit_bias.data_ptr(),
             "router_scale": None if self.router_scale is None else self.router_scale.data_ptr(),
             "per_expert_scale": None if self.per_expert_scale is None else self.per_expert_scale.data_ptr(),
+            "post_norm": None if self.post_norm is None else self.post_norm.data_ptr(),
+            "layer_scalar": None if self.layer_scalar is None else self.layer_scalar.data_ptr(),
         }
 
     # host copies for the oracle (regenerated, never read back from the device)
@@ -163,6 +170,12 @@ class DeviceLayer:
         if self.router_scale is None:
             return None, None
         return gen.router_scales(self.seed, self.n_experts, self.hidden)
+
+    def host_layer_tail(self):
+        """(post_norm bf16 bits [H], layer_scalar float32), or (None, None)."""
+        if self.post_norm is None:
+            return None, None
+        return gen.layer_tail(self.seed, self.hidden)
 
     def host_logit_bias(self):
         return None if self.logit_bias is None else gen.zipf_logit_bias(self.seed, self.n_experts)

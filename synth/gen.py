@@ -53,6 +53,7 @@ STREAM_WEIGHTS = 1
 STREAM_INPUT = 2
 STREAM_ZIPF = 3
 STREAM_ROUTER_SCALES = 4  # learned router scales of the optional-scale tests
+STREAM_LAYER_TAIL = 5     # post-FFN norm weight and layer scalar of the layer-tail tests
 # weight tuple fields
 ROUTER_ID = 2000          # "expert" slot of the router projection
 SHARED_ID = 1000          # "expert" slot of the dense shared expert
@@ -199,6 +200,14 @@ def router_scales(layer_seed: int, n_experts: int, hidden: int):
     u = uniform(stream_key(STREAM_ROUTER_SCALES, layer_seed, 0), hidden)
     v = uniform(stream_key(STREAM_ROUTER_SCALES, layer_seed, 1), n_experts)
     return to_bf16_bits(np.sqrt(hidden) * (0.5 + u)), (0.5 + v).astype(np.float32)
+
+
+def layer_tail(layer_seed: int, hidden: int):
+    """Layer-tail weights for the tests of that option: post-FFN norm weight
+    bf16 bits [H] = bf16(U(0.5, 1.5)) and the layer scalar float32 U(0.5, 1.5)."""
+    u = uniform(stream_key(STREAM_LAYER_TAIL, layer_seed, 0), hidden)
+    v = uniform(stream_key(STREAM_LAYER_TAIL, layer_seed, 1), 1)
+    return to_bf16_bits(0.5 + u), np.float32(0.5 + v[0])
 
 
 # ---------------------------------------------------------------- inputs

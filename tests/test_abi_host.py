@@ -69,6 +69,15 @@ def test_check_weights(lib):
     assert lib.moe_check_weights(ctypes.byref(bad)) == bq.MOE_ERR_INVALID_ARG
     bad = _weights(bq.make_dims(2816, 704, 128, 8, group=128))
     assert lib.moe_check_weights(ctypes.byref(bad)) == bq.MOE_ERR_UNSUPPORTED
+    # optional vectors: null is fine, set they must be aligned
+    for field, ok, misaligned in (("router_scale", 1 << 40, (1 << 40) + 8), ("per_expert_scale", 1 << 40, (1 << 40) + 2),
+                                  ("post_norm", 1 << 40, (1 << 40) + 8), ("layer_scalar", 1 << 40, (1 << 40) + 2)):
+        good = _weights(d)
+        setattr(good, field, ok)
+        assert lib.moe_check_weights(ctypes.byref(good)) == bq.MOE_OK, field
+        bad = _weights(d)
+        setattr(bad, field, misaligned)
+        assert lib.moe_check_weights(ctypes.byref(bad)) == bq.MOE_ERR_INVALID_ARG, field
     assert lib.moe_check_weights(None) == bq.MOE_ERR_INVALID_ARG
 
 
