@@ -136,7 +136,12 @@ def make_dims(hidden: int, inter: int, n_experts: int, top_k: int, group: int = 
 def make_layer_weights(dims: Dims, router_q: int, router_s: int, router_b: int, experts: int, expert_stride: int,
                        layout: dict, shared: int, logit_bias=None, router_scale=None,
                        per_expert_scale=None, post_norm=None, layer_scalar=None) -> LayerWeights:
-    """LayerWeights from device addresses; `layout` maps gate_q .. down_b to byte offsets."""
+    """LayerWeights from device addresses; `layout` maps gate_q .. down_b to byte offsets.
+
+    Optional entries (device address, CUDA tensor or None): logit_bias fp32
+    [E]; router_scale bf16 [H] and per_expert_scale fp32 [E], the router's
+    learned scales; post_norm bf16 [H] and layer_scalar fp32 [1], the layer
+    tail, which only the residual calls apply."""
     return LayerWeights(dims, QMat(router_q, router_s, router_b), experts, expert_stride,
                         BlobLayout(*[layout[n] for n in _BLOB_FIELDS]), shared, _ptr(logit_bias),
                         _ptr(router_scale), _ptr(per_expert_scale), _ptr(post_norm), _ptr(layer_scalar))
@@ -204,6 +209,10 @@ class Moe:
 
     def layer_forward_residual(self, hidden, n_tokens, w: LayerWeights, ws, y_out=None, x_out=None, ids_out=None,
                                logits_out=None, stream=None):
+        """One layer of a residual stack: hidden <- hidden + MoE(rmsnorm(hidden))
+        in place, or with the layer's tail hidden <- lambda * (hidden +
+        post_norm * y / rms(y)); y_out / x_out receive the block output and
+        its normalised input."""
         self._check(self.lib.moe_layer_forward_residual(self.h, _ptr(hidden), n_tokens, ctypes.byref(w), _ptr(y_out),
                                                         _ptr(x_out), _ptr(ids_out), _ptr(logits_out), _ptr(ws),
                                                         ws.numel() * ws.element_size(), _stream(stream)),
