@@ -57,7 +57,8 @@ STREAM_LAYER_TAIL = 5     # post-FFN norm weight and layer scalar of the layer-t
 # weight tuple fields
 ROUTER_ID = 2000          # "expert" slot of the router projection
 SHARED_ID = 1000          # "expert" slot of the dense shared expert
-MAT_GATE, MAT_UP, MAT_DOWN, MAT_ROUTER = 0, 1, 2, 3
+HEAD_ID = 3000            # "expert" slot of the tied head / embedding
+MAT_GATE, MAT_UP, MAT_DOWN, MAT_ROUTER, MAT_HEAD = 0, 1, 2, 3, 4
 FIELD_Q, FIELD_S, FIELD_B = 0, 1, 2
 
 GROUP = 64
@@ -180,6 +181,45 @@ def router_weights(layer_seed: int, n_experts: int, hidden: int) -> dict:
     b_bits = to_bf16_bits(-128.0 * bf16_bits_to_f64(s_bits))
     return {"q": q.reshape(n_experts, hidden // 4), "s": s_bits.reshape(n_experts, ng),
             "b": b_bits.reshape(n_experts, ng)}
+
+
+def head_weights(seed: int, vocab: int, hidden: int, rows=None) -> dict:
+    """The tied 4-bit head [vocab, hidden] (the embedding shares it): codes
+    uniform 0..15, scale bf16(U(0.5, 1.5) / (8 sqrt(H))), bias
+    bf16(-8 scale + 0.01 scale N(0, 1)), like the experts.  With `rows`, only
+    those rows (the same values as in the whole matrix)."""
+    ng, nw = hidden // GROUP, hidden // 8
+    idx = np.arange(vocab) if rows is None else np.asarray(rows, dtype=np.int64)
+    kq, ks, kb = (weight_key(seed, HEAD_ID, MAT_HEAD, f) for f in (FIELD_Q, FIELD_S, FIELD_B))
+    q = np.empty((idx.size, nw), dtype=np.uint32)
+    u = np.empty((idx.size, ng), dtype=np.float64)
+    z = np.empty((idx.size, ng), dtype=np.float64)
+    if rows is None:
+        q[:] = words(kq, vocab * nw).reshape(vocab, nw)
+        u[:] = uniform(ks, vocab * ng).reshape(vocab, ng)
+        z[:] = normal(kb, vocab * ng).reshape(vocab, ng)
+    else:
+        for i, r in enumerate(idx):
+            d = draws(kq, nw // 2, int(r) * (nw // 2))      # word 2j/2j+1 = halves of draw j
+            q[i, 0::2] = (d & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+            q[i, 1::2] = (d >> np.uint64(32)).astype(np.uint32)
+            u[i] = (draws(ks, ng, int(r) * ng) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+            z[i] = _normal_at(kb, ng, int(r) * ng)
+    s_bits = to_bf16_bits((0.5 + u) / (8.0 * np.sqrt(float(hidden))))
+    b_bits = to_bf16_bits(-8.0 * bf16_bits_to_f64(s_bits) + (0.01 * bf16_bits_to_f64(s_bits)) * z)
+    return {"q": q, "s": s_bits, "b": b_bits}
+
+
+def _normal_at(key: int, n: int, start: int) -> np.ndarray:
+    """normal(key, start + n)[start:] for even start and n (whole Box-Muller pairs)."""
+    d = draws(key, n, start)
+    u1 = ((d[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+    u2 = (d[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    r = np.sqrt(-2.0 * np.log(u1))
+    z = np.empty(n, dtype=np.float64)
+    z[0::2] = r * np.cos(2.0 * np.pi * u2)
+    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return z
 
 
 def zipf_logit_bias(layer_seed: int, n_experts: int, s: float = 1.1, top: float = 2.0) -> np.ndarray:

@@ -11,7 +11,9 @@ import pytest
 
 import oracle_pins
 
-ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "moe_oracle.py")
+ORACLE_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+ORACLE_SRC = os.path.join(ORACLE_DIR, "moe_oracle.py")
+HEAD_SRC = os.path.join(ORACLE_DIR, "head_oracle.py")
 
 MUTATIONS = {
     "reversed_code_order": ("(w >> np.uint32(bits * pos))", "(w >> np.uint32(bits * (per - 1 - pos)))"),
@@ -56,6 +58,38 @@ def test_mutation_is_caught(name):
     mod = _mutant(name)
     caught = []
     for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mod)
+        except (AssertionError, ValueError, ZeroDivisionError, FloatingPointError, IndexError) as exc:
+            caught.append((pin.__name__, type(exc).__name__))
+    assert caught, f"no pin caught mutation {name}"
+
+
+HEAD_MUTATIONS = {
+    "softcap_outer_cap_dropped": ("return cap * np.tanh(np.asarray(z, dtype=np.float64) / cap)",
+                                  "return np.tanh(np.asarray(z, dtype=np.float64) / cap)"),
+    "softcap_inner_unscaled": ("return cap * np.tanh(np.asarray(z, dtype=np.float64) / cap)",
+                               "return cap * np.tanh(np.asarray(z, dtype=np.float64))"),
+    "softcap_dropped": ("out[:, b0:b0 + sel.size] = softcap(x @ w.T, cap)", "out[:, b0:b0 + sel.size] = x @ w.T"),
+    "greedy_ties_to_higher": ("out[t] = int(np.flatnonzero(lg[t] == m)[0])", "out[t] = int(np.flatnonzero(lg[t] == m)[-1])"),
+    "greedy_argmin": ("m = lg[t].max()", "m = lg[t].min()"),
+    "row_block_short": ("sel = idx[b0:b0 + ROW_BLOCK]", "sel = idx[b0:b0 + ROW_BLOCK - 1]"),
+    "embed_unrounded_rows_shifted": ("w = dequantize(head[\"q\"][ids], head[\"s\"][ids], head[\"b\"][ids], 4)",
+                                     "w = dequantize(head[\"q\"][ids], head[\"s\"][ids[::-1]], head[\"b\"][ids], 4)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HEAD_MUTATIONS))
+def test_head_mutation_is_caught(name):
+    import head_pins
+    old, new = HEAD_MUTATIONS[name]
+    with open(HEAD_SRC) as f:
+        src = f.read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mod = types.ModuleType(f"head_mutant_{name}")
+    exec(compile(src.replace(old, new, 1), f"<mutant {name}>", "exec"), mod.__dict__)
+    caught = []
+    for pin in head_pins.ALL_HEAD_PINS:
         try:
             pin(mod)
         except (AssertionError, ValueError, ZeroDivisionError, FloatingPointError, IndexError) as exc:
