@@ -53,6 +53,10 @@ class LayerWeights(ctypes.Structure):
                 ("post_norm", ctypes.c_void_p), ("layer_scalar", ctypes.c_void_p)]
 
 
+class HeadWeights(ctypes.Structure):
+    _fields_ = [("vocab", ctypes.c_int), ("hidden", ctypes.c_int), ("w", QMat)]
+
+
 class MoeError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -87,6 +91,8 @@ def load_library(path: str = LIB_PATH):
         "moe_layer_forward_static": (I, [V, P(LayerWeights), V, V, V, V, V]),
         "moe_layer_forward_stack": (I, [V, V, I, P(LayerWeights), V, Z, V]),
         "moe_get_error": (I, [V, P(I)]),
+        "moe_head_forward": (I, [V, V, I, P(HeadWeights), ctypes.c_float, V, V, V]),
+        "moe_embed": (I, [V, V, I, P(HeadWeights), V, V]),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
@@ -145,6 +151,11 @@ def make_layer_weights(dims: Dims, router_q: int, router_s: int, router_b: int, 
     return LayerWeights(dims, QMat(router_q, router_s, router_b), experts, expert_stride,
                         BlobLayout(*[layout[n] for n in _BLOB_FIELDS]), shared, _ptr(logit_bias),
                         _ptr(router_scale), _ptr(per_expert_scale), _ptr(post_norm), _ptr(layer_scalar))
+
+
+def make_head_weights(vocab: int, hidden: int, q: int, scales: int, biases: int) -> HeadWeights:
+    """HeadWeights from device addresses (or CUDA tensors) of the tied head."""
+    return HeadWeights(vocab, hidden, QMat(_ptr(q), _ptr(scales), _ptr(biases)))
 
 
 def layer_forward_static(x, w: LayerWeights, y, ids_out=None, logits_out=None, weights_out=None, stream=None):
@@ -225,6 +236,18 @@ class Moe:
         self._check(self.lib.moe_layer_forward_stack(self.h, _ptr(hidden), len(layers), arr, _ptr(ws),
                                                      ws.numel() * ws.element_size(), _stream(stream)),
                     "moe_layer_forward_stack")
+
+    def head_forward(self, x, n_tokens, hw: HeadWeights, softcap: float = 30.0, logits=None, tokens=None,
+                     stream=None):
+        """The tied head on n_tokens (<= 8) rows of x: logits (fp32 [T, V])
+        and/or greedy tokens (int32 [T])."""
+        self._check(self.lib.moe_head_forward(self.h, _ptr(x), n_tokens, ctypes.byref(hw), ctypes.c_float(softcap),
+                                              _ptr(logits), _ptr(tokens), _stream(stream)), "moe_head_forward")
+
+    def embed(self, ids, n, hw: HeadWeights, out, stream=None):
+        """Tied embedding rows (bf16 [n, H]) of int32 token ids on the device."""
+        self._check(self.lib.moe_embed(self.h, _ptr(ids), n, ctypes.byref(hw), _ptr(out), _stream(stream)),
+                    "moe_embed")
 
     def set_trace(self, buffer=None, n_launches: int = 0):
         """Record per-launch device timestamps into `buffer` (u64 x 4 x n)."""

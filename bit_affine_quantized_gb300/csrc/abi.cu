@@ -21,6 +21,7 @@ struct moe_handle {
   int fused_key[3], fused_ok; // cached shape check (hidden, inter, top_k) -> usable
   bool prefill;               // multi-token layer calls use the fused prefill kernel
   int prefill_key[4], prefill_ok;  // cached check (hidden, inter, n_experts, top_k) -> usable
+  bool head_ready;            // the head kernel's attributes are set (first head call)
 };
 
 namespace {
@@ -42,6 +43,10 @@ constexpr size_t kSmemCap = 227 * 1024;
 // kPrefillSyncOffset the prefill kernel's (each launch of a kernel adds a
 // fixed multiple of its grid size to its own counter, so they stay apart)
 constexpr size_t kSyncOffset = 256;
+// kHeadStateOffset: the head's greedy state, [kHeadMaxTokens] 64-bit maxima
+// then its finished-block ticket (zero between launches)
+constexpr size_t kHeadStateOffset = 64;
+static_assert(kHeadStateOffset + 2 * moe::kHeadMaxTokens + 1 <= kSyncOffset, "head state overlaps");
 constexpr size_t kPrefillSyncOffset = kSyncOffset + 16;
 constexpr size_t kDeviceWords = kSyncOffset + 64 + 1024;
 // kMboxOffset: the single-token kernel's logit mailboxes, [SM count][128]
@@ -169,6 +174,16 @@ moe::LayerPtrs layer_ptrs(const moe_layer_weights &w) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int check_head(const moe_head_weights *w) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (w->hidden < 64 || w->hidden > 4096 || w->hidden % 64) return MOE_ERR_UNSUPPORTED;
+  if (w->vocab < 16 || w->vocab % 16 || w->vocab > (1 << 28)) return MOE_ERR_UNSUPPORTED;
+  const void *p[3] = {w->w.q, w->w.scales, w->w.biases};
+  for (const void *q : p)
+    if (!q || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
 
 int check_ws(const moe_dims &d, int T, const void *ws, size_t ws_bytes) {
   if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
@@ -498,6 +513,61 @@ int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe
                                          stream)))
       return st;
   return MOE_OK;
+}
+
+int moe_head_forward(moe_handle *h, const void *x, int n_tokens, const moe_head_weights *w, float softcap,
+                     float *logits, int32_t *tokens, moe_stream_t stream) {
+  if (!h || !x || (!logits && !tokens)) return MOE_ERR_INVALID_ARG;
+  int st = check_head(w);
+  if (st) return st;
+  if (n_tokens < 1 || n_tokens > moe::kHeadMaxTokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (logits && !aligned(logits, 4)) || (tokens && !aligned(tokens, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if (!(softcap == softcap)) return MOE_ERR_INVALID_ARG;
+  if (!h->head_ready) {
+    if (moe::head_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+    h->head_ready = true;
+  }
+  const int per_sm = moe::head_blocks_per_sm(w->hidden, n_tokens);
+  if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
+  // the fewest warps that still give every warp the same number of 16-row units
+  const long long n_units = w->vocab / 16, max_warps = (long long)h->n_sm * per_sm * 8;
+  const long long per_warp = (n_units + max_warps - 1) / max_warps;
+  const long long warps = (n_units + per_warp - 1) / per_warp;
+  moe::HeadArgs a;
+  a.x = (const uint16_t *)x;
+  a.q = (const uint32_t *)w->w.q;
+  a.s = (const uint16_t *)w->w.scales;
+  a.b = (const uint16_t *)w->w.biases;
+  a.logits = logits;
+  a.tokens = tokens;
+  a.best = reinterpret_cast<unsigned long long *>(h->dwords + kHeadStateOffset);
+  a.counter = h->dwords + kHeadStateOffset + 2 * moe::kHeadMaxTokens;
+  a.softcap = softcap;
+  a.T = n_tokens;
+  a.V = w->vocab;
+  a.H = w->hidden;
+  a.err = h->dwords;
+  a.trace = take_trace(h, 1);
+  return cuda_status(moe::launch_head(a, (int)((warps + 7) / 8), (cudaStream_t)stream, h->pdl));
+}
+
+int moe_embed(moe_handle *h, const int32_t *ids, int n, const moe_head_weights *w, void *out, moe_stream_t stream) {
+  if (!h || !ids || !out || n < 1) return MOE_ERR_INVALID_ARG;
+  int st = check_head(w);
+  if (st) return st;
+  if (!aligned(ids, 4) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  moe::EmbedArgs a;
+  a.ids = ids;
+  a.q = (const uint32_t *)w->w.q;
+  a.s = (const uint16_t *)w->w.scales;
+  a.b = (const uint16_t *)w->w.biases;
+  a.out = (uint16_t *)out;
+  a.n = n;
+  a.V = w->vocab;
+  a.H = w->hidden;
+  a.err = h->dwords;
+  return cuda_status(moe::launch_embed(a, (cudaStream_t)stream, h->pdl));
 }
 
 int moe_set_trace(moe_handle *h, unsigned long long *buffer, int n_launches) {

@@ -104,6 +104,35 @@ struct TailArgs {
 };
 cudaError_t launch_tail(const TailArgs &a, cudaStream_t st, bool pdl);
 
+// Tied head and embedding (head.cu).
+constexpr int kHeadMaxTokens = 8;
+struct HeadArgs {
+  const uint16_t *x;          // bf16 [T, H]
+  const uint32_t *q;          // [V, H/8] packed 4-bit codes
+  const uint16_t *s, *b;      // bf16 [V, H/64]
+  float *logits;              // nullable fp32 [T, V]
+  int32_t *tokens;            // nullable [T]: greedy token ids
+  unsigned long long *best;   // [8] packed (logit, id) maxima: zero between launches
+  unsigned *counter;          // finished-block ticket: zero between launches
+  float softcap;              // <= 0: none
+  int T, V, H;
+  unsigned *err;
+  unsigned long long *trace;
+};
+struct EmbedArgs {
+  const int32_t *ids;         // [n]
+  const uint32_t *q;
+  const uint16_t *s, *b;
+  uint16_t *out;              // bf16 [n, H]
+  int n, V, H;
+  unsigned *err;
+};
+size_t head_smem(int H, int T);
+cudaError_t head_set_attributes();
+int head_blocks_per_sm(int H, int T);
+cudaError_t launch_head(const HeadArgs &a, int n_blocks, cudaStream_t st, bool pdl);
+cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t st, bool pdl);
+
 size_t prefill_fused_smem(const Dims &d);  // 0: shape not supported
 int prefill_blocks_per_sm(const Dims &d);
 cudaError_t prefill_set_attributes();

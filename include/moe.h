@@ -246,6 +246,37 @@ int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe
 int moe_layer_forward_static(const void *x, const moe_layer_weights *w, void *y, int32_t *ids_out,
                              float *logits_out, float *weights_out, moe_stream_t stream);
 
+/* ---- The tied 4-bit head and embedding (section "Why the runtime has this
+ * shape": the embedding and the language-model head share one 4-bit affine
+ * matrix, and the model ends with a logit softcap of 30; section "Decode":
+ * the head returns the argmax token in a pure-greedy configuration, else the
+ * full logits vector). */
+typedef struct {
+  int vocab;   /* V rows: a multiple of 16, at most 2^28                       */
+  int hidden;  /* H columns: 64 .. 4096, a multiple of 64                      */
+  moe_qmat w;  /* q uint32 [V, H/8] (code i at bits 4*(i%8) of word i/8),
+                  scales and biases bf16 [V, H/64]; all 16-byte aligned        */
+} moe_head_weights;
+
+/* The head on up to 8 rows:
+ *   logits[t, v] = cap * tanh((W x_t)[v] / cap)   (cap <= 0: no softcap)
+ *   tokens[t]    = argmax_v logits[t, v], ties to the lower id
+ *   x        bf16 [T, H], 16-byte aligned, T in [1, 8]
+ *   logits   nullable fp32 [T, V];  tokens nullable int32 [T]; not both null
+ * One kernel launch, graph-capturable.  The argmax state lives in the
+ * handle (cleared by the launch that used it), so head calls on one handle
+ * must not overlap on the GPU.  A non-finite logit is skipped by the argmax
+ * and records MOE_ERR_NONFINITE. */
+int moe_head_forward(moe_handle *h, const void *x, int n_tokens, const moe_head_weights *w, float softcap,
+                     float *logits, int32_t *tokens, moe_stream_t stream);
+
+/* The tied embedding: out[i] = bf16(q[ids[i], :] * scale + bias), the
+ * dequantised row rounded once to bf16 (no scale factor).
+ *   ids int32 [n] on the device, n >= 1;  out bf16 [n, H], 16-byte aligned.
+ * An id outside [0, V) gives a zero row and records MOE_ERR_BAD_EXPERT_ID. */
+int moe_embed(moe_handle *h, const int32_t *ids, int n, const moe_head_weights *w, void *out,
+              moe_stream_t stream);
+
 /* Launch tracing (diagnostics).  With a non-null device buffer of
  * 4 * n_launches u64, each subsequent kernel launch by this handle takes the
  * next 4 slots (wrapping) and records %globaltimer values, combined with

@@ -61,6 +61,43 @@ def fill_words(addr: int, n_words: int, key: int, stream: int = 0) -> None:
         raise RuntimeError(f"synth_fill_words failed ({st})")
 
 
+class DeviceHead:
+    """The synthetic tied 4-bit head [vocab, hidden] on the device: codes from
+    the device filler, scales and biases generated on the host (the same
+    values as gen.head_weights)."""
+
+    def __init__(self, seed: int, vocab: int, hidden: int, device="cuda"):
+        import torch
+        self.seed, self.vocab, self.hidden = seed, vocab, hidden
+        ng = hidden // gen.GROUP
+        self.q = torch.empty(vocab * hidden // 8, dtype=torch.int32, device=device)
+        stream = torch.cuda.current_stream(self.q.device).cuda_stream
+        fill_words(self.q.data_ptr(), vocab * hidden // 8,
+                   gen.weight_key(seed, gen.HEAD_ID, gen.MAT_HEAD, gen.FIELD_Q), stream)
+        s, b = self._scale_bias()
+        self.s = torch.from_numpy(s.reshape(-1).view(np.int16).copy()).to(device)
+        self.b = torch.from_numpy(b.reshape(-1).view(np.int16).copy()).to(device)
+        assert self.s.numel() == vocab * ng
+        torch.cuda.synchronize(self.q.device)
+
+    def _scale_bias(self):
+        # the generator's scales and biases without its codes (those come from the device filler)
+        ng = self.hidden // gen.GROUP
+        u = gen.uniform(gen.weight_key(self.seed, gen.HEAD_ID, gen.MAT_HEAD, gen.FIELD_S), self.vocab * ng)
+        z = gen.normal(gen.weight_key(self.seed, gen.HEAD_ID, gen.MAT_HEAD, gen.FIELD_B), self.vocab * ng)
+        s_bits = gen.to_bf16_bits((0.5 + u) / (8.0 * np.sqrt(float(self.hidden))))
+        s = gen.bf16_bits_to_f64(s_bits)
+        b_bits = gen.to_bf16_bits(-8.0 * s + (0.01 * s) * z)
+        return s_bits, b_bits
+
+    def addresses(self):
+        return self.q.data_ptr(), self.s.data_ptr(), self.b.data_ptr()
+
+    def host_rows(self, rows=None) -> dict:
+        """Host copy of the given rows (all rows if None), regenerated from the seed."""
+        return gen.head_weights(self.seed, self.vocab, self.hidden, rows)
+
+
 class DeviceLayer:
     """All weights of one synthetic MoE layer in one device buffer."""
 

@@ -94,6 +94,10 @@ def test_calls_without_handle_are_rejected(lib):
                                        None) == bq.MOE_ERR_INVALID_ARG
     assert lib.moe_get_error(None, None) == bq.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == bq.MOE_ERR_INVALID_ARG
+    hw = bq.make_head_weights(262144, 2816, 1 << 40, 1 << 41, 1 << 42)
+    assert lib.moe_head_forward(None, V(1 << 40), 1, ctypes.byref(hw), 30.0, V(1 << 40), None,
+                                None) == bq.MOE_ERR_INVALID_ARG
+    assert lib.moe_embed(None, V(1 << 40), 1, ctypes.byref(hw), V(1 << 40), None) == bq.MOE_ERR_INVALID_ARG
 
 
 def test_create_without_gpu_fails_cleanly(lib):
