@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const HeadArgs a) {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       if (2 * cq + i < T && best[i] != 0ull) atomicMax(a.best + 2 * cq + i, best[i]);
+    __threadfence();  // this thread's maxima are visible before the block takes its ticket
   }
   __syncthreads();
   if (tid == 0) {
