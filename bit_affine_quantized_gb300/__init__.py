@@ -15,7 +15,8 @@ from .build import LIB_PATH, build as build_library
 __all__ = [
     "MoeError", "Dims", "QMat", "BlobLayout", "LayerWeights", "Moe", "load_library", "header_symbols",
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_BAD_EXPERT_ID",
-    "MOE_ERR_TIMEOUT", "MOE_ERR_NONFINITE", "MOE_ERR_WORKSPACE", "build_library",
+    "MOE_ERR_TIMEOUT", "MOE_ERR_NONFINITE", "MOE_ERR_WORKSPACE", "build_library", "static_get_error",
+    "layer_forward_static",
 ]
 
 MOE_OK = 0
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH):
         "moe_selftest_wait_timeout": (I, [V, ctypes.c_ulonglong, V]),
         "moe_set_trace": (I, [V, V, I]),
         "moe_layer_forward_static": (I, [V, P(LayerWeights), V, V, V, V, V]),
+        "moe_static_get_error": (I, [P(I)]),
+        "moe_selftest_skip_arrival": (I, [V, I, ctypes.c_ulonglong]),
         "moe_layer_forward_stack": (I, [V, V, I, P(LayerWeights), V, Z, V]),
         "moe_get_error": (I, [V, P(I)]),
         "moe_head_forward": (I, [V, V, I, P(HeadWeights), ctypes.c_float, V, V, V]),
@@ -167,6 +170,16 @@ def layer_forward_static(x, w: LayerWeights, y, ids_out=None, logits_out=None, w
                                                  _ptr(weights_out), _stream(stream))
     if st != MOE_OK:
         raise MoeError(st, "moe_layer_forward_static")
+
+
+def static_get_error() -> int:
+    """moe_static_get_error: the device-side status of the static calls on the
+    current device since the last read (waits for the device; clears it)."""
+    st = ctypes.c_int(0)
+    rc = load_library().moe_static_get_error(ctypes.byref(st))
+    if rc != MOE_OK:
+        raise MoeError(rc, "moe_static_get_error")
+    return st.value
 
 
 class Moe:
@@ -255,6 +268,11 @@ class Moe:
 
     def selftest_wait_timeout(self, limit_ns: int, stream=None):
         self._check(self.lib.moe_selftest_wait_timeout(self.h, limit_ns, _stream(stream)), "moe_selftest_wait_timeout")
+
+    def selftest_skip_arrival(self, block: int, limit_ns: int):
+        """Arms the next fused single-token launch: `block` withholds its
+        barrier arrival, every wait gives up after limit_ns (failure test)."""
+        self._check(self.lib.moe_selftest_skip_arrival(self.h, block, limit_ns), "moe_selftest_skip_arrival")
 
     def get_error(self) -> int:
         st = ctypes.c_int(0)

@@ -5,6 +5,7 @@
 
 #include <algorithm>
 
+#include "abi_internal.h"
 #include "kernels.h"
 #include "moe.h"
 
@@ -22,6 +23,9 @@ struct moe_handle {
   bool prefill;               // multi-token layer calls use the fused prefill kernel
   int prefill_key[4], prefill_ok;  // cached check (hidden, inter, n_experts, top_k) -> usable
   bool head_ready;            // the head kernel's attributes are set (first head call)
+  // failure-detection hook, consumed by the next fused single-token launch
+  int skip_block_next;                  // -1: none
+  unsigned long long wait_ns_next;      // 0: the default limit
 };
 
 namespace {
@@ -77,15 +81,6 @@ int check_dims(const moe_dims *d) {
 
 int check_tokens(int T) { return (T >= 1 && T <= moe::kMaxTokens) ? MOE_OK : MOE_ERR_INVALID_ARG; }
 
-size_t blob_extent(const moe_layer_weights &w) {
-  const size_t H = w.dims.hidden, I = w.dims.inter;
-  const size_t q = I * H / 2, sb = I * (H / 64) * 2;
-  const size_t ends[9] = {w.layout.gate_q + q, w.layout.gate_s + sb, w.layout.gate_b + sb,
-                          w.layout.up_q + q,   w.layout.up_s + sb,   w.layout.up_b + sb,
-                          w.layout.down_q + q, w.layout.down_s + sb, w.layout.down_b + sb};
-  return *std::max_element(ends, ends + 9);
-}
-
 struct WsLayout {
   size_t logits, ids, wts, counts, offsets, perm, pos, act_e, act_beg, act_cnt, n_act, xn, h, o, xq, hq, y, total;
 };
@@ -136,24 +131,17 @@ moe::Routing routing_in(uint8_t *ws, const WsLayout &L) {
   return r;
 }
 
-int check_weights_impl(const moe_layer_weights *w) {
-  if (!w) return MOE_ERR_INVALID_ARG;
-  int st = check_dims(&w->dims);
-  if (st) return st;
-  const void *ptrs[6] = {w->router.q, w->router.scales, w->router.biases, w->experts, w->shared, nullptr};
-  for (int i = 0; i < 5; ++i)
-    if (!ptrs[i] || !aligned(ptrs[i], 16)) return MOE_ERR_INVALID_ARG;
-  if (w->logit_bias && !aligned(w->logit_bias, 4)) return MOE_ERR_INVALID_ARG;
-  if (w->router_scale && !aligned(w->router_scale, 16)) return MOE_ERR_INVALID_ARG;
-  if (w->per_expert_scale && !aligned(w->per_expert_scale, 4)) return MOE_ERR_INVALID_ARG;
-  if (w->post_norm && !aligned(w->post_norm, 16)) return MOE_ERR_INVALID_ARG;
-  if (w->layer_scalar && !aligned(w->layer_scalar, 4)) return MOE_ERR_INVALID_ARG;
-  const size_t offs[9] = {w->layout.gate_q, w->layout.gate_s, w->layout.gate_b, w->layout.up_q, w->layout.up_s,
-                          w->layout.up_b,   w->layout.down_q, w->layout.down_s, w->layout.down_b};
-  for (size_t o : offs)
-    if (o % 256) return MOE_ERR_INVALID_ARG;
-  if (w->expert_stride % 256 || w->expert_stride < blob_extent(*w)) return MOE_ERR_INVALID_ARG;
-  return MOE_OK;
+}  // namespace
+
+namespace moe_abi {
+
+size_t blob_extent(const moe_layer_weights &w) {
+  const size_t H = w.dims.hidden, I = w.dims.inter;
+  const size_t q = I * H / 2, sb = I * (H / 64) * 2;
+  const size_t ends[9] = {w.layout.gate_q + q, w.layout.gate_s + sb, w.layout.gate_b + sb,
+                          w.layout.up_q + q,   w.layout.up_s + sb,   w.layout.up_b + sb,
+                          w.layout.down_q + q, w.layout.down_s + sb, w.layout.down_b + sb};
+  return *std::max_element(ends, ends + 9);
 }
 
 moe::LayerPtrs layer_ptrs(const moe_layer_weights &w) {
@@ -172,6 +160,39 @@ moe::LayerPtrs layer_ptrs(const moe_layer_weights &w) {
   p.expert_scale = w.per_expert_scale;
   return p;
 }
+
+int check_weights(const moe_layer_weights *w) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  int st = check_dims(&w->dims);
+  if (st) return st;
+  const void *ptrs[5] = {w->router.q, w->router.scales, w->router.biases, w->experts, w->shared};
+  for (const void *p : ptrs)
+    if (!p || !aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+  if (w->logit_bias && !aligned(w->logit_bias, 4)) return MOE_ERR_INVALID_ARG;
+  if (w->router_scale && !aligned(w->router_scale, 16)) return MOE_ERR_INVALID_ARG;
+  if (w->per_expert_scale && !aligned(w->per_expert_scale, 4)) return MOE_ERR_INVALID_ARG;
+  if (w->post_norm && !aligned(w->post_norm, 16)) return MOE_ERR_INVALID_ARG;
+  if (w->layer_scalar && !aligned(w->layer_scalar, 4)) return MOE_ERR_INVALID_ARG;
+  const size_t offs[9] = {w->layout.gate_q, w->layout.gate_s, w->layout.gate_b, w->layout.up_q, w->layout.up_s,
+                          w->layout.up_b,   w->layout.down_q, w->layout.down_s, w->layout.down_b};
+  for (size_t o : offs)
+    if (o % 256) return MOE_ERR_INVALID_ARG;
+  if (w->expert_stride % 256 || w->expert_stride < blob_extent(*w)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool decode_fused_supported(const moe_dims &d, int n_sm) {
+  if (d.n_experts > n_sm || n_sm > 1024) return false;
+  const moe::Dims dd = to_dims(d, 1);
+  return moe::fused_decode_smem(dd) <= kSmemCap && moe::decode_blocks_per_sm(dd) >= 1;
+}
+
+}  // namespace moe_abi
+
+namespace {
+using moe_abi::blob_extent;
+using moe_abi::layer_ptrs;
+int check_weights_impl(const moe_layer_weights *w) { return moe_abi::check_weights(w); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -216,11 +237,10 @@ int run_router(moe_handle *h, const moe_layer_weights *w, int T, const void *x, 
 // The fused single-token kernel needs one resident block per SM (grid
 // barriers) and one router row per block.
 bool use_fused(moe_handle *h, const moe_layer_weights *w, int T) {
-  if (!h->fused || T != 1 || w->dims.n_experts > h->n_sm || h->n_sm > 1024) return false;
+  if (!h->fused || T != 1) return false;
   const int key[3] = {w->dims.hidden, w->dims.inter, w->dims.top_k};
   if (key[0] != h->fused_key[0] || key[1] != h->fused_key[1] || key[2] != h->fused_key[2]) {
-    const moe::Dims d = to_dims(w->dims, 1);
-    h->fused_ok = moe::fused_decode_smem(d) <= kSmemCap && moe::decode_blocks_per_sm(d) >= 1;
+    h->fused_ok = moe_abi::decode_fused_supported(w->dims, h->n_sm);
     memcpy(h->fused_key, key, sizeof(key));
   }
   return h->fused_ok != 0;
@@ -245,6 +265,10 @@ int run_fused(moe_handle *h, const moe_layer_weights *w, const void *x, void *hr
   a.err = h->dwords;
   a.trace = take_trace(h, 1);
   a.normalize = normalize;
+  a.skip_block = h->skip_block_next;
+  a.wait_ns = h->wait_ns_next ? h->wait_ns_next : moe::kWaitLimitNs;
+  h->skip_block_next = -1;
+  h->wait_ns_next = 0;
   return cuda_status(moe::launch_decode_fused(a, h->n_sm, st, h->pdl));
 }
 
@@ -342,6 +366,7 @@ int moe_create(moe_handle **out) {
   if (!h) return MOE_ERR_CUDA;
   h->device = dev;
   h->n_sm = prop.multiProcessorCount;
+  h->skip_block_next = -1;
   const char *fz = getenv("MOE_DECODE_FUSED");
   h->fused = !(fz && fz[0] == '0');
   const char *pz = getenv("MOE_PREFILL_FUSED");
@@ -583,12 +608,25 @@ int moe_selftest_wait_timeout(moe_handle *h, unsigned long long limit_ns, moe_st
   return cuda_status(moe::launch_wait_timeout(h->dwords, limit_ns, (cudaStream_t)stream));
 }
 
+int moe_selftest_skip_arrival(moe_handle *h, int block, unsigned long long limit_ns) {
+  if (!h || block < 0 || block >= h->n_sm || limit_ns == 0 || limit_ns > moe::kWaitLimitNs)
+    return MOE_ERR_INVALID_ARG;
+  h->skip_block_next = block;
+  h->wait_ns_next = limit_ns;
+  return MOE_OK;
+}
+
 int moe_get_error(moe_handle *h, int *status) {
   if (!h || !status) return MOE_ERR_INVALID_ARG;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   unsigned bits = 0;
   if (cudaMemcpy(&bits, h->dwords, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemset(h->dwords, 0, sizeof(unsigned)) != cudaSuccess) return MOE_ERR_CUDA;
+  // After a timeout a launch may have left its grid-barrier counter short of
+  // a whole number of grids (a block that never arrived), which would give
+  // the next launch a stale epoch: with the device idle, every counter,
+  // ticket and mailbox goes back to its initial zero state.
+  const size_t clear = (bits & moe::kErrTimeout) ? device_words(h->n_sm) * sizeof(unsigned) : sizeof(unsigned);
+  if (cudaMemset(h->dwords, 0, clear) != cudaSuccess) return MOE_ERR_CUDA;
   if (bits & moe::kErrTimeout)
     *status = MOE_ERR_TIMEOUT;
   else if (bits & moe::kErrBadId)

@@ -178,6 +178,13 @@ __host__ __device__ inline int quad_tile_bytes(int H) { return 8 * quad_pitch(H)
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+// The tanh form of GELU (Hendrycks & Gimpel 2016), the gate activation of
+// the GeGLU experts: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))).
+__device__ __forceinline__ float gelu_tanh(float z) {
+  const float c0 = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * z * (1.0f + tanhf(c0 * fmaf(0.044715f * z, z * z, z)));
+}
+
 // bf16 pair -> fp16 pair (exact in fp16's normal range).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

@@ -101,13 +101,14 @@ __device__ __forceinline__ void grid_arrive(unsigned long long *count) {
   cons_sync();  // the block's writes happen-before thread 0's release below
   if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
 }
-__device__ bool grid_wait(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag) {
+__device__ bool grid_wait(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag,
+                          unsigned long long limit_ns) {
   if (threadIdx.x == 0) {
     bool ok = true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 0;; ++it) {
       if (ld_acquire64(count) >= target) break;
-      if ((it & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) {
+      if ((it & 15u) == 15u && global_ns() - t0 > limit_ns) {
         ok = false;
         break;
       }
@@ -118,9 +119,11 @@ __device__ bool grid_wait(unsigned long long *count, unsigned long long target, 
   cons_sync();
   return *s_flag != 0;
 }
-__device__ bool grid_sync(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag) {
-  grid_arrive(count);
-  return grid_wait(count, target, err, s_flag);
+// arrive = false withholds this block's arrival (the failure-detection hook)
+__device__ bool grid_sync(unsigned long long *count, unsigned long long target, unsigned *err, int *s_flag,
+                          unsigned long long limit_ns, bool arrive = true) {
+  if (arrive) grid_arrive(count);
+  return grid_wait(count, target, err, s_flag, limit_ns);
 }
 
 // Orderable 32-bit key of a float (larger float -> larger key).
@@ -130,11 +133,6 @@ __device__ __forceinline__ unsigned ord_key(float f) {
 }
 __device__ __forceinline__ float key_value(unsigned k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-__device__ __forceinline__ float gelu_tanh_f(float z) {
-  const float c0 = 0.7978845608028654f;  // sqrt(2/pi)
-  return 0.5f * z * (1.0f + tanhf(c0 * fmaf(0.044715f * z, z * z, z)));
 }
 
 // One 64-wide group of a gate/up unit: mma rows r, r+8 (tile rows quad_row(r),
@@ -282,7 +280,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     int issued = 0;
     for (int it = 0; it < n_units && ok; ++it) {
       const int slot = it % kSlots;
-      if (it >= kSlots) ok = mbar_wait_idle(&empty[slot], ((it / kSlots) - 1) & 1);
+      if (it >= kSlots) ok = mbar_wait_idle(&empty[slot], ((it / kSlots) - 1) & 1, 64, a.wait_ns);
       if (!ok) break;
       uint8_t *dst = ring + slot * L.slot_bytes;
       const bool is_gu = it < n_gu_mine;
@@ -301,7 +299,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         gslot = 0;
       }
       if ((!is_gu || gslot > 0) && !routed) {
-        ok = mbar_wait_idle(route, 0, 32) && *reinterpret_cast<volatile int *>(&s_flag[2]) == 0;
+        ok = mbar_wait_idle(route, 0, 32, a.wait_ns) && *reinterpret_cast<volatile int *>(&s_flag[2]) == 0;
         routed = true;
         if (!ok) break;
       }
@@ -349,7 +347,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
     if (lane == 0) {
       if (!ok) set_error(a.err, kErrTimeout);
       for (int it = issued - kSlots > 0 ? issued - kSlots : 0; it < issued; ++it)
-        mbar_wait_idle(&full[it % kSlots], (it / kSlots) & 1);
+        mbar_wait_idle(&full[it % kSlots], (it / kSlots) & 1, 64, a.wait_ns);
     }
     return;
   }
@@ -513,7 +511,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
       gslot = 1 + r / L.nrt;
       rt = r - (gslot - 1) * L.nrt;
     }
-    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) return false;
+    if (!mbar_wait(&full[slot], (it / kSlots) & 1, a.wait_ns)) return false;
     const uint8_t *tile = ring + slot * L.slot_bytes;
     // groups warp, warp + kCons, ...; two groups in flight per iteration
     float tg0a = 0.f, tg2a = 0.f, tu0a = 0.f, tu2a = 0.f, tg0b = 0.f, tg2b = 0.f, tu0b = 0.f, tu2b = 0.f;
@@ -543,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         gs += rd[w * 64 + lane];
         us += rd[w * 64 + 16 + lane];
       }
-      const float hv = gelu_tanh_f(gs) * us;
+      const float hv = gelu_tanh(gs) * us;
       if (!(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
       a.hbuf[(size_t)gslot * I + rt * kRowsU + quad_row(lane)] = __float2half_rn(hv);  // lane: mma row
     }
@@ -572,7 +570,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
         for (int i = 0; i < 4; ++i)
           if (4 * lane + i < E && (mv[i] & 0xFFFFFFFF00000000ull) != tag) mine = false;
         if (__all_sync(0xffffffffu, mine)) break;
-        if ((pi & 7u) == 7u && __any_sync(0xffffffffu, global_ns() - t0 > kWaitLimitNs)) {
+        if ((pi & 7u) == 7u && __any_sync(0xffffffffu, global_ns() - t0 > a.wait_ns)) {
           got = false;
           break;
         }
@@ -679,7 +677,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   if (!ok) set_error(a.err, kErrTimeout);
 
   // ---- phase 4: grid barrier (all of h written), then the down units
-  if (!grid_sync(bar_count, base + nb, a.err, &s_flag[1]) || !ok) return;
+  if (!grid_sync(bar_count, base + nb, a.err, &s_flag[1], a.wait_ns, c != a.skip_block) || !ok) return;
   // stage every expert's h row (permuted fp16) one 16-wide quarter per
   // thread (all loads in one round), then the group sums in quarter order
   {
@@ -716,7 +714,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_layer_kernel(const Decode
   for (int jd = 0; jd < n_dn_mine; ++jd, ++it) {
     const int slot = it % kSlots;
     const int n0 = (c_dn + nb * jd) * kRowsU;
-    if (!mbar_wait(&full[slot], (it / kSlots) & 1)) {
+    if (!mbar_wait(&full[slot], (it / kSlots) & 1, a.wait_ns)) {
       set_error(a.err, kErrTimeout);
       return;
     }

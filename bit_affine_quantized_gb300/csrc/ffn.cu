@@ -105,12 +105,6 @@ __host__ __device__ inline DownLayout down_layout(int I, int nslot, int rows, in
   return L;
 }
 
-__device__ __forceinline__ float gelu_tanh(float z) {
-  // 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
-  const float c0 = 0.7978845608028654f;
-  return 0.5f * z * (1.0f + tanhf(c0 * fmaf(0.044715f * z, z * z, z)));
-}
-
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float lo_f16(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }

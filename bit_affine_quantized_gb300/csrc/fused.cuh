@@ -135,10 +135,5 @@ __device__ __forceinline__ void warp_topk(const float *logits, int E, int k, int
     }
 }
 
-__device__ __forceinline__ float gelu_tanh(float z) {
-  const float c0 = 0.7978845608028654f;  // sqrt(2/pi)
-  return 0.5f * z * (1.0f + tanhf(c0 * fmaf(0.044715f * z, z * z, z)));
-}
-
 }  // namespace fused
 }  // namespace moe

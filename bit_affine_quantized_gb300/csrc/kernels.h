@@ -68,6 +68,10 @@ struct DecodeArgs {
   unsigned *err;
   unsigned long long *trace;
   int normalize;
+  // failure-detection hook: every bounded wait of the launch gives up after
+  // wait_ns; block skip_block (-1: none) withholds its barrier-2 arrival
+  int skip_block;
+  unsigned long long wait_ns;
 };
 
 // Fused multi-token layer (prefill.cu): one persistent block per SM, 2 <= T <= 128.

@@ -9,16 +9,17 @@
 // expert activations h, the logits when the caller passes none, the grid
 // barrier counter, the logit mailboxes and the device error word) in
 // file-scope device arrays and calls no cudaMalloc, cudaFree or allocating
-// library routine.
+// library routine.  moe_static_get_error reads (and clears) its error word.
 #include <mutex>
 
+#include "abi_internal.h"
 #include "kernels.h"
 #include "moe.h"
 
 namespace {
 
 // Scratch shared by every call on a device (it lives until the process exits):
-//   [0, 256)      device error word (cleared by every call, not reported)
+//   [0, 256)      device error word (accumulates until moe_static_get_error)
 //   [256, 512)    grid-barrier arrival counter (zero at load; it only grows:
 //                 its value gives each launch the epoch that tags its logits)
 //   [512, 1024)   logits when the caller passes none: fp32 [E], E <= 128
@@ -28,18 +29,19 @@ constexpr size_t kScratchBytes = 16 * 1024;
 constexpr size_t kErrOff = 0, kBarOff = 256, kLogitsOff = 512, kHOff = 1024;
 __device__ __align__(256) unsigned char g_static_scratch[kScratchBytes];
 // logit mailboxes of the fused kernel: [grid][128] epoch-tagged 64-bit words
+// (160 KiB: devices with up to 160 multiprocessors)
 constexpr int kMaxStaticSm = 160;
 __device__ __align__(256) unsigned long long g_static_mbox[kMaxStaticSm * moe::kMaxExperts];
 
-// The array's name is a host-side stand-in in host code: its device address
-// is looked up once per device, with that device current.
+// The arrays' names are host-side stand-ins in host code: their device
+// addresses are looked up once per device, with that device current.
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 unsigned char *g_scratch_ptr[kMaxDevices];
 unsigned long long *g_mbox_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 
-int setup_device(int dev, unsigned char **ptr, int *n_sm) {
+int setup_device(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mu);
   if (!g_scratch_ptr[dev]) {
@@ -53,25 +55,12 @@ int setup_device(int dev, unsigned char **ptr, int *n_sm) {
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
     void *mb = nullptr;
     if (cudaGetSymbolAddress(&mb, g_static_mbox) != cudaSuccess || !mb) return MOE_ERR_CUDA;
-    g_mbox_ptr[dev] = static_cast<unsigned long long *>(mb);
     if (moe::decode_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+    g_mbox_ptr[dev] = static_cast<unsigned long long *>(mb);
     g_sm_count[dev] = sms;
     g_scratch_ptr[dev] = static_cast<unsigned char *>(p);
   }
-  *ptr = g_scratch_ptr[dev];
-  *n_sm = g_sm_count[dev];
   return MOE_OK;
-}
-
-size_t extent(const moe_layer_weights &w) {
-  const size_t H = w.dims.hidden, I = w.dims.inter;
-  const size_t q = I * H / 2, sb = I * (H / 64) * 2;
-  const size_t e[9] = {w.layout.gate_q + q, w.layout.gate_s + sb, w.layout.gate_b + sb,
-                       w.layout.up_q + q,   w.layout.up_s + sb,   w.layout.up_b + sb,
-                       w.layout.down_q + q, w.layout.down_s + sb, w.layout.down_b + sb};
-  size_t m = 0;
-  for (size_t v : e) m = v > m ? v : m;
-  return m;
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -81,7 +70,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 extern "C" int moe_layer_forward_static(const void *x, const moe_layer_weights *w, void *y, int32_t *ids_out,
                                         float *logits_out, float *weights_out, moe_stream_t stream) {
   if (!x || !y || !w) return MOE_ERR_INVALID_ARG;
-  int st = moe_check_weights(w);
+  int st = moe_abi::check_weights(w);
   if (st != MOE_OK) return st;
   if (!aligned16(x) || !aligned16(y) || (logits_out && !aligned16(logits_out))) return MOE_ERR_INVALID_ARG;
   // sizes beyond the static scratch are rejected
@@ -90,33 +79,16 @@ extern "C" int moe_layer_forward_static(const void *x, const moe_layer_weights *
     return MOE_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  unsigned char *scratch = nullptr;
-  int n_sm = 0;
-  if ((st = setup_device(dev, &scratch, &n_sm)) != MOE_OK) return st;
-  const moe::Dims d{w->dims.hidden, w->dims.inter, w->dims.n_experts, w->dims.top_k, 1};
-  // the fused kernel's own limits: one router row per block, one block per SM
-  if (w->dims.n_experts > n_sm || n_sm > kMaxStaticSm || moe::fused_decode_smem(d) > 227 * 1024 ||
-      moe::decode_blocks_per_sm(d) < 1)
-    return MOE_ERR_UNSUPPORTED;
-
-  // the error word starts at zero for every call
-  if (cudaMemsetAsync(scratch + kErrOff, 0, kBarOff - kErrOff, (cudaStream_t)stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if ((st = setup_device(dev)) != MOE_OK) return st;
+  const int n_sm = g_sm_count[dev];
+  unsigned char *scratch = g_scratch_ptr[dev];
+  // the fused kernel's own limits (one router row per block, one block per
+  // SM) and the size of the mailbox array
+  if (n_sm > kMaxStaticSm || !moe_abi::decode_fused_supported(w->dims, n_sm)) return MOE_ERR_UNSUPPORTED;
 
   moe::DecodeArgs a;
-  a.w.router_q = (const uint8_t *)w->router.q;
-  a.w.router_s = (const uint16_t *)w->router.scales;
-  a.w.router_b = (const uint16_t *)w->router.biases;
-  a.w.experts = (const uint8_t *)w->experts;
-  a.w.stride = w->expert_stride;
-  a.w.shared = (const uint8_t *)w->shared;
-  a.w.off = moe::Blob{w->layout.gate_q, w->layout.gate_s, w->layout.gate_b, w->layout.up_q,  w->layout.up_s,
-                      w->layout.up_b,   w->layout.down_q, w->layout.down_s, w->layout.down_b};
-  a.w.blob_bytes = extent(*w);
-  a.w.logit_bias = w->logit_bias;
-  a.w.router_scale = (const uint16_t *)w->router_scale;
-  a.w.expert_scale = w->per_expert_scale;
-  a.d = d;
+  a.w = moe_abi::layer_ptrs(*w);
+  a.d = moe::Dims{w->dims.hidden, w->dims.inter, w->dims.n_experts, w->dims.top_k, 1};
   a.x = (const uint16_t *)x;
   a.hres = nullptr;
   a.xn_user = nullptr;
@@ -130,5 +102,39 @@ extern "C" int moe_layer_forward_static(const void *x, const moe_layer_weights *
   a.err = reinterpret_cast<unsigned *>(scratch + kErrOff);
   a.trace = nullptr;
   a.normalize = 0;
+  a.skip_block = -1;
+  a.wait_ns = moe::kWaitLimitNs;
   return moe::launch_decode_fused(a, n_sm, (cudaStream_t)stream, true) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_static_get_error(int *status) {
+  if (!status) return MOE_ERR_INVALID_ARG;
+  *status = MOE_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  unsigned char *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    scratch = g_scratch_ptr[dev];
+  }
+  if (!scratch) return MOE_OK;  // no static call has run on this device
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpy(&bits, scratch + kErrOff, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(scratch + kErrOff, 0, sizeof(unsigned)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (bits & moe::kErrTimeout) {
+    // a launch that timed out may have left the barrier counter short of a
+    // whole grid: with the device idle, counter and mailboxes go back to zero
+    if (cudaMemset(scratch + kBarOff, 0, kLogitsOff - kBarOff) != cudaSuccess ||
+        cudaMemset(g_mbox_ptr[dev], 0, sizeof(g_static_mbox)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    *status = MOE_ERR_TIMEOUT;
+  } else if (bits & moe::kErrBadId) {
+    *status = MOE_ERR_BAD_EXPERT_ID;
+  } else if (bits & moe::kErrNonFinite) {
+    *status = MOE_ERR_NONFINITE;
+  }
+  return MOE_OK;
 }

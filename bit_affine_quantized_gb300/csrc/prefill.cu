@@ -887,7 +887,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
             us += red_g[w * 256 + (idx + 4) * 32 + ln];
           }
           const int m = (ln >> 2) + 8 * (idx >> 1), n = 2 * (ln & 3) + (idx & 1);  // mma row, token
-          const float hv = fused::gelu_tanh(gs * kCodeScale) * (us * kCodeScale);
+          const float hv = gelu_tanh(gs * kCodeScale) * (us * kCodeScale);
           if (n < nt && !(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
           s_hst_g[n * 16 + quad_row(m)] = __float2half_rn(hv);
         }

@@ -52,6 +52,16 @@
  *     back by moe_get_error.
  *   - A handle may be used from one stream at a time (it owns the device
  *     error word and the router's completion counter).
+ *   - The layer calls run one persistent launch per layer (one block per
+ *     SM, blocks that wait for one another at grid barriers).  Their blocks
+ *     must all be resident at once: while such a call runs, no other work
+ *     may hold SMs of the device (a kernel on another stream, another
+ *     process under MPS, a green context).  Otherwise blocks wait at a
+ *     barrier until the bounded wait (2 s) gives up, the call records
+ *     MOE_ERR_TIMEOUT and its outputs are not valid; moe_get_error then
+ *     reports the timeout and restores the barrier state for the next call.
+ *     Handles created with MOE_DECODE_FUSED=0 / MOE_PREFILL_FUSED=0 in the
+ *     environment run separate launches that never wait for one another.
  */
 #ifndef MOE_AFFINE_H
 #define MOE_AFFINE_H
@@ -226,25 +236,36 @@ int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe
  * e.g. a program whose own pool owns the whole device, or a per-token loop
  * where an allocation would stall the device and cannot be captured).
  * Same computation as moe_layer_forward with n_tokens = 1 on the fused
- * single-token kernel, but with no handle and no workspace: its scratch
- * (h, logits when logits_out is NULL, the grid-barrier counter and the
- * device error word) is one 16 KiB static device array that every GPU
- * loading this library holds until the process exits.
+ * single-token kernel, but with no handle and no workspace.  Its scratch
+ * lives in two static device arrays that every GPU loading this library
+ * holds until the process exits:
+ *   - 16 KiB: h, the logits when logits_out is NULL, the grid-barrier
+ *     counter and the device error word;
+ *   - 160 KiB: the logit mailboxes, 128 64-bit words per block of the grid
+ *     (one block per SM, so devices with at most 160 SMs).
  *   x    bf16 [H] in;  y bf16 [H] out;  ids_out int32 [k], logits_out
  *        fp32 [E], weights_out fp32 [k] nullable.
  * Limits: (top_k + 1) * inter * 2 <= 15 KiB (top-8 of inter 704 uses
- * 12,672 B) and the fused kernel's
- * conditions (n_experts <= SM count, its shared memory fits); otherwise
+ * 12,672 B), at most 160 SMs, and the fused kernel's conditions
+ * (n_experts <= SM count, its shared memory fits); otherwise
  * MOE_ERR_UNSUPPORTED and nothing is launched.  The first call on a device
- * looks up the array's device address and sets kernel attributes, so make
- * it before any stream capture.  Every call clears the error word, then
- * launches; the grid-barrier counter only grows (its value gives each launch
- * the epoch that tags its logits); the array keeps the last call's contents.  Calls
- * that overlap on the GPU (different streams, or the same array from two
- * threads) race on the shared scratch.  Device-side error flags of this
- * call (bounded-wait timeouts, non-finite logits) are not reported. */
+ * looks up the arrays' device addresses and sets kernel attributes, so make
+ * it before any stream capture.  The grid-barrier counter only grows (its
+ * value gives each launch the epoch that tags its logits); the arrays keep
+ * the last call's contents.  Calls that overlap on the GPU (different
+ * streams, or the same arrays from two threads) race on the shared scratch.
+ * Device-side errors (bounded-wait timeouts, non-finite values) accumulate
+ * in the static error word until moe_static_get_error reads them. */
 int moe_layer_forward_static(const void *x, const moe_layer_weights *w, void *y, int32_t *ids_out,
                              float *logits_out, float *weights_out, moe_stream_t stream);
+
+/* The error word of moe_layer_forward_static on the current device: waits
+ * for all work on the device, returns (in *status) the first device-side
+ * error recorded since the last read (MOE_OK if none, or if no static call
+ * ran on this device) and clears it.  After a timeout it also puts the
+ * static grid-barrier counter and mailboxes back to zero, so the next static
+ * call starts from a consistent state.  Allocates nothing. */
+int moe_static_get_error(int *status);
 
 /* ---- The tied 4-bit head and embedding (section "Why the runtime has this
  * shape": the embedding and the language-model head share one 4-bit affine
@@ -297,9 +318,22 @@ int moe_set_trace(moe_handle *h, unsigned long long *buffer, int n_launches);
  * reports.  Every wait in the kernels above uses the same bounded wait. */
 int moe_selftest_wait_timeout(moe_handle *h, unsigned long long limit_ns, moe_stream_t stream);
 
+/* Self-test of a grid barrier that never completes (failure detection
+ * without a GPU fault): arms the handle's next fused single-token launch so
+ * that block `block` (0 <= block < SM count) withholds its arrival at the
+ * barrier between the gate/up and down phases, and every bounded wait of
+ * that launch gives up after limit_ns (1 .. 2e9 ns) of device time.  The
+ * blocks then record MOE_ERR_TIMEOUT and leave (the launch's outputs are not
+ * valid); moe_get_error reports it and restores the barrier state, so the
+ * next call is correct again.  Host-side only: launches nothing itself. */
+int moe_selftest_skip_arrival(moe_handle *h, int block, unsigned long long limit_ns);
+
 /* Waits for all work on the device, then returns (in *status) the first
  * device-side error recorded since the last call (MOE_OK if none) and
- * clears it.  The return value reports failures of the call itself. */
+ * clears it.  After a timeout it also resets the handle's grid-barrier
+ * counters, tickets and logit mailboxes (a launch whose blocks did not all
+ * arrive leaves its counter out of step).  The return value reports
+ * failures of the call itself. */
 int moe_get_error(moe_handle *h, int *status);
 
 #ifdef __cplusplus

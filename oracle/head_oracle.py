@@ -13,7 +13,7 @@ Sources (page "TurboFieldfare - System design"):
     argmax token directly (pure-greedy configuration) or writes the full
     logits vector for the sampler.
 
-Readings where the pages are silent (listed again in the design notes):
+Readings where the pages are silent:
   * the softcap is cap * tanh(z / cap) with cap = 30 (the usual form of a
     logit softcap);
   * the head takes its input rows as given (any final norm is the caller's);

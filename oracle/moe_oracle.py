@@ -37,7 +37,7 @@ Sources (page "TurboFieldfare - System design", by section):
     grouped per expert; the grouping is a stable counting sort of the pair
     index t*k + j by expert id.
 
-Readings where the pages are silent (listed again in the design notes):
+Readings where the pages are silent:
   * top-k ties go to the lower expert id, and the k ids are returned in
     order of descending logit (ties: ascending id);
   * the softmax weights are computed in float64 (the pages return FP16);

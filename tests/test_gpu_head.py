@@ -1,7 +1,4 @@
-"""(Not collected: named pending_* until these tests have passed once on a
-GPU; then it becomes test_gpu_head.py.)
-
-The tied 4-bit head and embedding on a GB300, through the C ABI, against
+"""The tied 4-bit head and embedding on a GB300, through the C ABI, against
 the float64 oracle (page "TurboFieldfare - System design": the embedding and
 the head share one 4-bit affine matrix; a final logit softcap of 30; the head
 returns the argmax token or the full logits).
