@@ -42,9 +42,13 @@ CSRC = os.path.join(ROOT, "bit_affine_quantized_gb300", "csrc")
 # per-launch DRAM traffic of the fused kernels, from committed ncu summaries:
 # (summary file, sources that define the kernel)
 TRAFFIC = {
-    1: ("decode_layer_kernel_T1.md", ("decode.cu", "common.cuh", "kernels.h")),
-    128: ("prefill_layer_kernel_T128.md", ("prefill.cu", "fused.cuh", "common.cuh", "kernels.h")),
+    1: ("decode_layer_kernel_T1.md", ("decode.cu", "common.cuh")),
+    128: ("prefill_layer_kernel_T128.md", ("prefill.cu", "fused.cuh", "common.cuh")),
 }
+
+
+# steps of each workload when it is timed as a sub-record of the default line
+SUB_STEPS = {"layer1": 64, "batch64": 32, "prefill128": 32, "prefill30": 8}
 
 
 def layer_bytes(n_tokens: int, distinct_routed: int) -> int:
@@ -176,24 +180,47 @@ def barrier(world: int):
 
 
 # ---------------------------------------------------------------- our arm
-def build_layers(spec, device):
-    from synth.device import DeviceLayer
-    return [DeviceLayer(l, H, I, E, device=device, zipf=spec["zipf"]) for l in range(spec["layers"])]
+class Layers:
+    """The 30 synthetic layers (seed = layer index), resident in HBM, with the
+    Zipf logit offsets of each layer as a separate small tensor: workloads
+    with Zipf-skewed routing use the same weights plus that offset."""
+
+    def __init__(self, device, n_layers=N_LAYERS):
+        import torch
+        import bit_affine_quantized_gb300 as bq
+        from synth import gen
+        from synth.device import DeviceLayer
+        self.layers = [DeviceLayer(l, H, I, E, device=device) for l in range(n_layers)]
+        self.bias = [torch.from_numpy(gen.zipf_logit_bias(l, E)).to(device) for l in range(n_layers)]
+        dims = bq.make_dims(H, I, E, K)
+        self.plain = [bq.layer_weights_from(dims, L.addresses()) for L in self.layers]
+        self.zipf = []
+        for L, b in zip(self.layers, self.bias):
+            addr = dict(L.addresses())
+            addr["logit_bias"] = b.data_ptr()
+            self.zipf.append(bq.layer_weights_from(dims, addr))
+
+    def weights(self, spec):
+        w = self.zipf if spec["zipf"] else self.plain
+        return w[:spec["layers"]]
 
 
-def run_ours(args, spec, rank, world, device):
+def time_workload(moe, spec, weights, steps, warmup, rank, device, e2e=False, clocks=False):
+    """Times `steps` steps of a workload after `warmup` untimed ones.
+
+    A step is one pass of the hot path over one batch of synthetic input:
+    for residual workloads every layer of the stack on one chunk (one CUDA
+    graph), otherwise one layer call on one chunk, the layer copies rotated
+    across steps so that L2 never holds the next step's weights.  Returns
+    the step time (CUDA events on the launching stream around the whole
+    timed region), the summed duration of the layer calls (events around
+    each graph replay), the distinct experts touched, and optionally the
+    end-to-end time with host buffers and the clocks sampled meanwhile."""
     import torch
-    import bit_affine_quantized_gb300 as bq
     from synth import gen
 
-    bq.build_library()
-    moe = bq.Moe()
-    dims = bq.make_dims(H, I, E, K)
-    layers = build_layers(spec, device)
-    weights = [bq.layer_weights_from(dims, L.addresses()) for L in layers]
     T = spec["tokens"]
-    steps_total = args.warmup + args.steps
-    # per-step inputs, resident in HBM before the timed region
+    steps_total = warmup + steps
     chunk_seed = 1000 + 7919 * rank
     host_in = np.stack([gen.hidden_states(chunk_seed, s, T, H, rms_normalize=spec["rms"])
                         for s in range(steps_total)])                       # [S, T, H] bf16 bits
@@ -201,60 +228,51 @@ def run_ours(args, spec, rank, world, device):
     outputs = torch.empty_like(inputs)
     h = torch.empty((T, H), dtype=torch.int16, device=device)
     y = torch.empty_like(h)
-    ws = torch.empty(moe.workspace_bytes(dims, T), dtype=torch.uint8, device=device)
+    ws = torch.empty(moe.workspace_bytes(weights[0].dims, T), dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device=device)
-    ids = torch.empty((spec["layers"], T, K), dtype=torch.int32, device=device)
+    ids = torch.empty((len(weights), T, K), dtype=torch.int32, device=device)
 
-    def step_body():
-        # the graph body: all layers of one step on `h`
-        for l, w in enumerate(weights):
-            li = l % len(weights)
-            if spec["residual"]:
-                moe.layer_forward_residual(h, T, weights[li], ws, ids_out=ids[li], stream=stream)
-            else:
-                moe.layer_forward(h, T, weights[li], y, ws, ids_out=ids[li], stream=stream)
-            if not spec["residual"]:
-                break
+    def call(li):
+        if spec["residual"]:
+            moe.layer_forward_residual(h, T, weights[li], ws, ids_out=ids[li], stream=stream)
+        else:
+            moe.layer_forward(h, T, weights[li], y, ws, ids_out=ids[li], stream=stream)
 
-    # non-residual workloads rotate layer copies across steps (cold L2)
     graphs = []
     h.copy_(inputs[0])
     torch.cuda.synchronize(device)
     with torch.cuda.stream(stream):
         if spec["residual"]:
+            for li in range(len(weights)):
+                call(li)  # warm the code path once outside capture
             g = torch.cuda.CUDAGraph()
-            step_body()  # warm the code path once outside capture
             with torch.cuda.graph(g, stream=stream):
-                step_body()
+                for li in range(len(weights)):
+                    call(li)
             graphs.append(g)
         else:
-            for li, w in enumerate(weights):
+            for li in range(len(weights)):
+                call(li)
                 g = torch.cuda.CUDAGraph()
-                moe.layer_forward(h, T, w, y, ws, ids_out=ids[li], stream=stream)
                 with torch.cuda.graph(g, stream=stream):
-                    moe.layer_forward(h, T, w, y, ws, ids_out=ids[li], stream=stream)
+                    call(li)
                 graphs.append(g)
     torch.cuda.synchronize(device)
     st = moe.get_error()
-    if st != bq.MOE_OK:
+    if st != 0:
         raise RuntimeError(f"device error status {st} during warm-up")
-
     out_src = h if spec["residual"] else y
 
     # launches per layer call, read from the trace slots the kernels stamp
     trace = torch.zeros(4 * 8, dtype=torch.int64, device=device)
     moe.set_trace(trace, 8)
     with torch.cuda.stream(stream):
-        if spec["residual"]:
-            moe.layer_forward_residual(h, T, weights[0], ws, stream=stream)
-        else:
-            moe.layer_forward(h, T, weights[0], y, ws, stream=stream)
+        call(0)
     torch.cuda.synchronize(device)
     moe.set_trace(None, 0)
     launches_per_call = int((trace.view(8, 4) != 0).any(dim=1).sum())
-    calls_per_step = spec["layers"] if spec["residual"] else 1
+    calls_per_step = len(weights) if spec["residual"] else 1
 
-    # the kernels' own time: events around each graph replay, on its stream
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps_total)]
 
     def one_step(s):
@@ -265,92 +283,133 @@ def run_ours(args, spec, rank, world, device):
         outputs[s].copy_(out_src, non_blocking=True)
 
     with torch.cuda.stream(stream):
-        for s in range(args.warmup):
+        for s in range(warmup):
             one_step(s)
     torch.cuda.synchronize(device)
-    sampler = ClockSampler(torch.cuda.current_device() if device is None else torch.device(device).index or 0)
-    barrier(world)
-    torch.cuda.synchronize(device)
-    sampler.start()
-    time.sleep(0.3)
+    sampler = None
+    if clocks:
+        sampler = ClockSampler(torch.device(device).index or 0)
+        sampler.start()
+        time.sleep(0.3)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for s in range(args.warmup, steps_total):
+        for s in range(warmup, steps_total):
             one_step(s)
         ev1.record(stream)
     torch.cuda.synchronize(device)
-    elapsed_ms = ev0.elapsed_time(ev1)
-    kernel_ms = sum(a.elapsed_time(b) for a, b in kev[args.warmup:steps_total])
-    clocks = sampler.stop()
-    barrier(world)
+    res = {"elapsed_ms": ev0.elapsed_time(ev1),
+           "kernel_ms": sum(a.elapsed_time(b) for a, b in kev[warmup:steps_total]),
+           "launches_per_call": launches_per_call, "calls_per_step": calls_per_step}
+    if sampler is not None:
+        res["clocks"] = sampler.stop()
     st = moe.get_error()
-    if st != bq.MOE_OK:
+    if st != 0:
         raise RuntimeError(f"device error status {st} during the timed region")
-
-    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
-    ms_per_step = elapsed_ms / args.steps
-    units_per_step = T  # tokens (rows) per step per rank
-    value = world * units_per_step * args.steps / (elapsed_ms / 1e3)
 
     # algorithmic bytes: distinct experts actually touched per layer call
     ids_np = ids.cpu().numpy()
     if spec["residual"]:
-        n_calls = spec["layers"]
-        distinct = [len(np.unique(ids_np[l])) for l in range(n_calls)]
+        distinct = [len(np.unique(ids_np[l])) for l in range(len(weights))]
     else:
-        n_calls = 1
         distinct = [len(np.unique(ids_np[(steps_total - 1) % len(graphs)]))]
-    bytes_per_step = sum(layer_bytes(T, d) for d in distinct)
-    bytes_per_call = bytes_per_step / n_calls
+    res["distinct"] = distinct
+    res["bytes_per_call"] = sum(layer_bytes(T, d) for d in distinct) / len(distinct)
+    res["bytes_per_step"] = res["bytes_per_call"] * calls_per_step
+
+    if e2e:
+        # end to end through the public API with host buffers: pinned H2D of
+        # the step's input, the layer calls, D2H of the result, every step
+        pin_in = torch.from_numpy(host_in.view(np.int16)).pin_memory()
+        pin_out = torch.empty_like(pin_in).pin_memory()
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for s in range(steps):
+                h.copy_(pin_in[s], non_blocking=True)
+                graphs[s % len(graphs)].replay()
+                pin_out[s].copy_(out_src, non_blocking=True)
+                stream.synchronize()
+        res["e2e_s"] = time.perf_counter() - t0
+    return res
+
+
+def summary(spec, res, steps, world, hbm):
+    """Throughput, per-call time and roofline fraction of one timed workload."""
+    T = spec["tokens"]
+    call_us = res["kernel_ms"] * 1e3 / (steps * res["calls_per_step"])
+    achieved = res["bytes_per_call"] / (call_us / 1e6) / 1e9
+    return {"value": world * T * steps / (res["elapsed_ms"] / 1e3), "ms_per_step": res["elapsed_ms"] / steps,
+            "call_us": call_us, "achieved": achieved, "frac": achieved / hbm}
+
+
+def kernel_name(spec, res):
+    if res["launches_per_call"] != 1:
+        return "router + gate/up + down launches (MOE_*_FUSED=0)"
+    return "decode_layer_kernel" if spec["tokens"] == 1 else "prefill_layer_kernel"
+
+
+def run_ours(args, spec, rank, world, device):
+    import bit_affine_quantized_gb300 as bq
+
+    bq.build_library()
+    moe = bq.Moe()
+    layers = Layers(device)
     hbm, peak_kind = peaks()
-    # one layer call is one launch of the fused kernel (the dominant and only
-    # kernel of the step); its average duration over the timed region
-    call_us = max_over_ranks(kernel_ms, world, device) * 1e3 / (args.steps * calls_per_step)
-    achieved = bytes_per_call / (call_us / 1e6) / 1e9
-    fused = launches_per_call == 1
-    traffic, traffic_src = traffic_per_launch(T) if fused else (None, "chained launches")
-
-    # end to end through the public API with host buffers: pinned H2D of the
-    # step's input, the layer calls, D2H of the result, every step
-    pin_in = torch.from_numpy(host_in.view(np.int16)).pin_memory()
-    pin_out = torch.empty_like(pin_in).pin_memory()
-    e2e_steps = args.steps
-    torch.cuda.synchronize(device)
+    T = spec["tokens"]
     barrier(world)
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for s in range(e2e_steps):
-            h.copy_(pin_in[s], non_blocking=True)
-            graphs[s % len(graphs)].replay()
-            pin_out[s].copy_(out_src, non_blocking=True)
-            stream.synchronize()
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world, device)
-    e2e_value = world * units_per_step * e2e_steps / e2e_s
-
-    kernel_name = ("decode_layer_kernel" if T == 1 else "prefill_layer_kernel") if fused else \
-        "router + gate/up + down launches (MOE_*_FUSED=0)"
+    res = time_workload(moe, spec, layers.weights(spec), args.steps, args.warmup, rank, device, e2e=True,
+                        clocks=True)
+    for key in ("elapsed_ms", "kernel_ms", "e2e_s"):
+        res[key] = max_over_ranks(res[key], world, device)
+    barrier(world)
+    sm = summary(spec, res, args.steps, world, hbm)
+    fused = res["launches_per_call"] == 1
+    traffic, traffic_src = traffic_per_launch(T) if fused else (None, "chained launches")
     line = {
-        "metric": args.metric, "value": round(value, 3), "unit": args.unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "metric": args.metric, "value": round(sm["value"], 3), "unit": args.unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sm["ms_per_step"], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": spec["desc"], "layers": spec["layers"], "tokens_per_step": T, "hidden": H,
                    "inter": I, "experts": E, "top_k": K, "group": 64,
                    "l2": "inputs larger than L2: %.0f MB of touched weights per step (L2 129 MB)%s" % (
-                       bytes_per_step / 1e6, "" if spec["residual"] else "; 8 layer copies rotated"),
+                       res["bytes_per_step"] / 1e6, "" if spec["residual"] else "; 8 layer copies rotated"),
                    "cuda_graph": True, "pdl": os.environ.get("MOE_PDL", "1") != "0",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": kernel_name,
-                     "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": traffic, "traffic_source": traffic_src,
-                     "algorithmic_bytes_per_launch": round(bytes_per_call), "launch_us": round(call_us, 3),
-                     "launches_timed": args.steps * calls_per_step},
-        "e2e": {"value": round(e2e_value, 3), "unit": args.unit, "h2d_bytes_per_step": T * H * 2,
-                "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
-        "gpu_launches": launches_per_call * calls_per_step * args.steps,
-        "clocks": clocks,
+        "roofline": {"bound": "hbm", "kernel": kernel_name(spec, res),
+                     "achieved": round(sm["achieved"], 1), "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(sm["frac"], 4), "traffic": traffic, "traffic_source": traffic_src,
+                     "algorithmic_bytes_per_launch": round(res["bytes_per_call"]),
+                     "launch_us": round(sm["call_us"], 3), "launches_timed": args.steps * res["calls_per_step"]},
+        "e2e": {"value": round(world * T * args.steps / res["e2e_s"], 3), "unit": args.unit,
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2, "steps": args.steps},
+        "gpu_launches": res["launches_per_call"] * res["calls_per_step"] * args.steps,
+        "clocks": res["clocks"],
     }
+    # the metric's other workloads, each timed on its own region after the main one
+    if not args.no_workloads:
+        subs = {}
+        name = [k for k, v in WORKLOADS.items() if v is spec][0]
+        for other, steps in SUB_STEPS.items():
+            if other == name:
+                continue
+            ospec = WORKLOADS[other]
+            r = time_workload(moe, ospec, layers.weights(ospec), steps, 3, rank, device)
+            for key in ("elapsed_ms", "kernel_ms"):
+                r[key] = max_over_ranks(r[key], world, device)
+            o = summary(ospec, r, steps, world, hbm)
+            otraffic = traffic_per_launch(ospec["tokens"])[0] if r["launches_per_call"] == 1 else None
+            subs[other] = {"workload": ospec["desc"], "value": round(o["value"], 3),
+                           "unit": "rows/s" if ospec["zipf"] else "tok/s", "steps": steps, "warmup": 3,
+                           "ms_per_step": round(o["ms_per_step"], 5), "kernel": kernel_name(ospec, r),
+                           "launch_us": round(o["call_us"], 3),
+                           "algorithmic_bytes_per_launch": round(r["bytes_per_call"]),
+                           "distinct_experts_per_call": round(float(np.mean(r["distinct"])), 2),
+                           "achieved_gbs": round(o["achieved"], 1), "frac": round(o["frac"], 4),
+                           "traffic": otraffic,
+                           "gpu_launches": r["launches_per_call"] * r["calls_per_step"] * steps}
+        line["workloads"] = subs
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
     moe.close()
@@ -358,15 +417,15 @@ def run_ours(args, spec, rank, world, device):
 
 
 # ---------------------------------------------------------------- oracle arm
-def _oracle_sample(spec, seconds: float, layer_cap: int = 30):
+def _oracle_sample(spec, seconds: float, chunk: int, layer_cap: int = 30):
     """Times the float64 oracle on a bounded sample of the workload: one
-    token-chunk through consecutive layers until `seconds` of oracle time.
-    Returns (seconds per (layer, chunk), layers timed)."""
+    token-chunk (input `chunk`) through consecutive layers until `seconds` of
+    oracle time.  Returns (seconds per (layer, chunk), layers timed)."""
     from oracle import moe_oracle as O
     from synth import gen
 
     T = spec["tokens"]
-    h = gen.hidden_states(1000, 0, T, H, rms_normalize=spec["rms"])
+    h = gen.hidden_states(1000, chunk, T, H, rms_normalize=spec["rms"])
     spent, timed = 0.0, 0
     for l in range(min(layer_cap, spec["layers"])):
         router = gen.router_weights(l, E, H)
@@ -388,26 +447,16 @@ def _oracle_sample(spec, seconds: float, layer_cap: int = 30):
     return spent / timed, timed
 
 
-def _oracle_child(name: str, seconds: float, steps: int = 0):
-    """Runs the oracle sample in a child process pinned to one BLAS thread."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", name, "--cpu-seconds", str(seconds),
-           "--oracle-steps", str(steps)]
-    res = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
-    if res.returncode != 0:
-        raise RuntimeError(res.stderr[-800:])
-    return json.loads(res.stdout.strip().splitlines()[-1])
-
-
-def _oracle_steps(spec, steps: int):
-    """Per-step oracle time of layer 0 on fresh inputs (reference arm)."""
+def _oracle_steps(spec, steps):
+    """Oracle time of layer 0 of the stack on the inputs of the given steps
+    (one bounded sample per step of the reference arm)."""
     from oracle import moe_oracle as O
     from synth import gen
     router = gen.router_weights(0, E, H)
     bias = gen.zipf_logit_bias(0, E) if spec["zipf"] else None
     shared = gen.expert_weights(0, gen.SHARED_ID, H, I)
     out = []
-    for s in range(steps):
+    for s in steps:
         h = gen.hidden_states(1000, s, spec["tokens"], H, rms_normalize=spec["rms"])
         x = O.rmsnorm_no_scale(h) if spec["residual"] else h
         ids = O.select_top_k(O.router_logits(x, router, bias), K)
@@ -421,39 +470,91 @@ def _oracle_steps(spec, steps: int):
     return out
 
 
-def cpu_baseline(spec, seconds: float) -> dict:
-    """Oracle on the host in a child process pinned to one BLAS thread."""
-    name = [k for k, v in WORKLOADS.items() if v is spec][0]
+def oracle_cores() -> int:
+    """Host cores available to the oracle's worker processes."""
     try:
-        per_layer, timed = _oracle_child(name, seconds)
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _oracle_pool(name: str, jobs):
+    """Runs one child process per job (a list of extra arguments) at once,
+    each on one BLAS thread: every host core runs whole layer calls of its
+    own, the processes split the work by input chunk or step, and no result
+    depends on how many there are.  Returns the children's results in job
+    order."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    procs = []
+    for extra in jobs:
+        cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", name, *extra]
+        procs.append(subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env))
+    out = []
+    for p in procs:
+        o, e = p.communicate(timeout=1800)
+        if p.returncode != 0:
+            raise RuntimeError(e[-800:])
+        out.append(json.loads(o.strip().splitlines()[-1]))
+    return out
+
+
+def cpu_baseline(spec, seconds: float) -> dict:
+    """The float64 oracle on all host cores: one process per core, each
+    timing whole layer calls on its own input chunk for about `seconds`."""
+    name = [k for k, v in WORKLOADS.items() if v is spec][0]
+    cores = oracle_cores()
+    try:
+        t0 = time.perf_counter()
+        res = _oracle_pool(name, [["--cpu-seconds", str(seconds), "--oracle-chunk", str(c)] for c in range(cores)])
+        wall = time.perf_counter() - t0
     except Exception as exc:  # reported, never fatal for the GPU number
         return {"value": None, "error": str(exc)[-400:]}
     T = spec["tokens"]
-    value = T / (per_layer * (spec["layers"] if spec["residual"] else 1))
-    return {"value": round(value, 6), "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": f"{timed} layer call(s) of {T} token(s) timed ({per_layer:.2f} s each), scaled to "
-                      f"{spec['layers'] if spec['residual'] else 1} layer(s) per step; numpy float64, one thread"}
+    layers = spec["layers"] if spec["residual"] else 1
+    per_core = [T / (per_layer * layers) for per_layer, _ in res]
+    calls = sum(n for _, n in res)
+    mean_call = float(np.mean([p for p, _ in res]))
+    return {"value": round(sum(per_core), 6), "unit": "rows/s" if spec["zipf"] else "tok/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{cores} processes, one per host core, each timing whole layer calls of {T} token(s) on its "
+                      f"own input chunk for about {seconds:.0f} s ({calls} calls in all, {mean_call:.2f} s each); "
+                      f"per-core throughput = tokens / (seconds per call x {layers} layer(s) per step), summed "
+                      f"over the cores; numpy float64, one BLAS thread per process; {wall:.1f} s wall"}
 
 
 def run_reference(args, spec, rank, world):
     if rank != 0:
         return None
     name = [k for k, v in WORKLOADS.items() if v is spec][0]
-    times = _oracle_child(name, 0.0, steps=args.warmup + args.steps)
-    timed = times[args.warmup:]
+    cores = oracle_cores()
+    steps = list(range(args.warmup + args.steps))
+    per = [p for p in (steps[i::cores] for i in range(cores)) if p]
+    t0 = time.perf_counter()
+    res = _oracle_pool(name, [["--oracle-steps", ",".join(map(str, p))] for p in per])
+    wall = time.perf_counter() - t0
+    times = {}
+    for p, r in zip(per, res):
+        times.update(zip(p, r))
+    timed = [times[s] for s in steps[args.warmup:]]
     per_layer = sum(timed) / len(timed)
     layers = spec["layers"] if spec["residual"] else 1
     T = spec["tokens"]
-    value = T / (per_layer * layers)
+    used = len(per)
+    value = used * T / (per_layer * layers)
+    unit = "rows/s" if spec["zipf"] else "tok/s"
     return {
-        "impl": "reference", "metric": args.metric, "value": round(value, 6), "unit": args.unit, "n_gpus": world,
+        "impl": "reference", "metric": args.metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_layer * layers * 1e3, 3),
+        "ms_per_step_kind": f"extrapolated: layer 0 timed on each step's input ({per_layer * 1e3:.1f} ms), "
+                            f"x {layers} layer(s)",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": spec["desc"], "layers": spec["layers"], "tokens_per_step": T},
-        "cpu_baseline": {"value": round(value, 6), "unit": args.unit, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": used, "kind": "oracle",
                          "sample": f"each step: layer 0 of the stack for {T} token(s) in the float64 oracle, "
-                                   f"scaled to {layers} layer(s)"},
-        "e2e": {"value": round(value, 6), "unit": args.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                                   f"scaled to {layers} layer(s); the {len(steps)} steps spread over {used} "
+                                   f"processes (one per host core, one BLAS thread each), throughput summed over "
+                                   f"them; {wall:.1f} s wall"},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
@@ -468,14 +569,17 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--oracle-steps", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-steps", default="", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-chunk", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the selected workload (no sub-records of the other four)")
     args = ap.parse_args(argv)
     if args.oracle_sample:
         spec = WORKLOADS[args.oracle_sample]
-        if args.oracle_steps > 0:
-            print(json.dumps(_oracle_steps(spec, args.oracle_steps)))
+        if args.oracle_steps:
+            print(json.dumps(_oracle_steps(spec, [int(v) for v in args.oracle_steps.split(",")])))
         else:
-            print(json.dumps(_oracle_sample(spec, args.cpu_seconds)))
+            print(json.dumps(_oracle_sample(spec, args.cpu_seconds, args.oracle_chunk)))
         return 0
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
