@@ -96,6 +96,7 @@ def load_library(path: str = LIB_PATH):
         "moe_get_error": (I, [V, P(I)]),
         "moe_head_forward": (I, [V, V, I, P(HeadWeights), ctypes.c_float, V, V, V]),
         "moe_embed": (I, [V, V, I, P(HeadWeights), V, V]),
+        "moe_dense_forward": (I, [V, V, I, P(HeadWeights), V, V, V]),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
@@ -256,6 +257,12 @@ class Moe:
         and/or greedy tokens (int32 [T])."""
         self._check(self.lib.moe_head_forward(self.h, _ptr(x), n_tokens, ctypes.byref(hw), ctypes.c_float(softcap),
                                               _ptr(logits), _ptr(tokens), _stream(stream)), "moe_head_forward")
+
+    def dense_forward(self, x, n_tokens, w: HeadWeights, y=None, y32=None, stream=None):
+        """A dense 4-bit affine projection y = W x on n_tokens (<= 8) rows:
+        bf16 [T, N] and/or fp32 [T, N] outputs."""
+        self._check(self.lib.moe_dense_forward(self.h, _ptr(x), n_tokens, ctypes.byref(w), _ptr(y), _ptr(y32),
+                                               _stream(stream)), "moe_dense_forward")
 
     def embed(self, ids, n, hw: HeadWeights, out, stream=None):
         """Tied embedding rows (bf16 [n, H]) of int32 token ids on the device."""

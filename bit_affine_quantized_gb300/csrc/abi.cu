@@ -565,10 +565,46 @@ int moe_head_forward(moe_handle *h, const void *x, int n_tokens, const moe_head_
   a.s = (const uint16_t *)w->w.scales;
   a.b = (const uint16_t *)w->w.biases;
   a.logits = logits;
+  a.out_bf16 = nullptr;
   a.tokens = tokens;
   a.best = reinterpret_cast<unsigned long long *>(h->dwords + kHeadStateOffset);
   a.counter = h->dwords + kHeadStateOffset + 2 * moe::kHeadMaxTokens;
   a.softcap = softcap;
+  a.T = n_tokens;
+  a.V = w->vocab;
+  a.H = w->hidden;
+  a.err = h->dwords;
+  a.trace = take_trace(h, 1);
+  return cuda_status(moe::launch_head(a, (int)((warps + 7) / 8), (cudaStream_t)stream, h->pdl));
+}
+
+int moe_dense_forward(moe_handle *h, const void *x, int n_tokens, const moe_head_weights *w, void *y, float *y32,
+                      moe_stream_t stream) {
+  if (!h || !x || (!y && !y32)) return MOE_ERR_INVALID_ARG;
+  int st = check_head(w);
+  if (st) return st;
+  if (n_tokens < 1 || n_tokens > moe::kHeadMaxTokens) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (y && !aligned(y, 2)) || (y32 && !aligned(y32, 4))) return MOE_ERR_INVALID_ARG;
+  if (!h->head_ready) {
+    if (moe::head_set_attributes() != cudaSuccess) return MOE_ERR_CUDA;
+    h->head_ready = true;
+  }
+  const int per_sm = moe::head_blocks_per_sm(w->hidden, n_tokens);
+  if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
+  const long long n_units = w->vocab / 16, max_warps = (long long)h->n_sm * per_sm * 8;
+  const long long per_warp = (n_units + max_warps - 1) / max_warps;
+  const long long warps = (n_units + per_warp - 1) / per_warp;
+  moe::HeadArgs a;
+  a.x = (const uint16_t *)x;
+  a.q = (const uint32_t *)w->w.q;
+  a.s = (const uint16_t *)w->w.scales;
+  a.b = (const uint16_t *)w->w.biases;
+  a.logits = y32;
+  a.out_bf16 = (uint16_t *)y;
+  a.tokens = nullptr;  // no argmax: the greedy state is neither read nor written
+  a.best = reinterpret_cast<unsigned long long *>(h->dwords + kHeadStateOffset);
+  a.counter = h->dwords + kHeadStateOffset + 2 * moe::kHeadMaxTokens;
+  a.softcap = 0.0f;
   a.T = n_tokens;
   a.V = w->vocab;
   a.H = w->hidden;

@@ -5,7 +5,9 @@
 // a pure-greedy configuration, else the full logits).
 //
 // head_kernel: logits[t, v] = cap * tanh(sum_k w[v, k] x[t, k] / cap) for up
-// to 8 tokens, w = q * s + b per 64-wide group.  An HBM-bound GEMV over the
+// to 8 tokens, w = q * s + b per 64-wide group; with no cap and no argmax it
+// is the plain dense 4-bit projection (the attention's Q/K/V and output
+// projections use the same format).  An HBM-bound GEMV over the
 // whole vocabulary: every warp streams 16-row units straight from global
 // memory (per row pair and group each lane loads 8 bytes of codes, so the
 // 4 lanes of a quad cover one 32-byte sector of a row), the products run on
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const HeadArgs a) {
       float v = cap > 0.f ? cap * tanhf(t[i] / cap) : t[i];
       if (tok < T) {
         if (a.logits) a.logits[(size_t)tok * V + row] = v;
+        if (a.out_bf16) a.out_bf16[(size_t)tok * V + row] = float_to_bf16_bits(v);
         if (!isfinite(v)) {
           bad = true;
           v = -INFINITY;

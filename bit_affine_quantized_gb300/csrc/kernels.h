@@ -115,6 +115,7 @@ struct HeadArgs {
   const uint32_t *q;          // [V, H/8] packed 4-bit codes
   const uint16_t *s, *b;      // bf16 [V, H/64]
   float *logits;              // nullable fp32 [T, V]
+  uint16_t *out_bf16;         // nullable bf16 [T, V]: the same values rounded to bf16
   int32_t *tokens;            // nullable [T]: greedy token ids
   unsigned long long *best;   // [8] packed (logit, id) maxima: zero between launches
   unsigned *counter;          // finished-block ticket: zero between launches

@@ -291,6 +291,22 @@ typedef struct {
 int moe_head_forward(moe_handle *h, const void *x, int n_tokens, const moe_head_weights *w, float softcap,
                      float *logits, int32_t *tokens, moe_stream_t stream);
 
+/* A dense 4-bit affine projection in the same matrix format (section ".gturbo
+ * directory": the production manifest stores the attention weights 4-bit
+ * affine, group 64, like the embedding; section "Metal execution": single-
+ * token decode runs projections as custom GEMV kernels), e.g. the
+ * attention's Q/K/V and output projections:
+ *   y[t, n] = sum_k W[n, k] x[t, k]
+ *   w        W [N, K] as moe_head_weights (vocab = N rows, a multiple of 16;
+ *            hidden = K columns, 64 .. 4096, a multiple of 64)
+ *   x        bf16 [T, K], 16-byte aligned, T in [1, 8]
+ *   y        nullable bf16 [T, N] (the fp32 sum rounded to nearest even)
+ *   y32      nullable fp32 [T, N]; not both null
+ * One launch of the head kernel with no softcap and no argmax, graph-
+ * capturable; it does not touch the head's greedy state. */
+int moe_dense_forward(moe_handle *h, const void *x, int n_tokens, const moe_head_weights *w, void *y, float *y32,
+                      moe_stream_t stream);
+
 /* The tied embedding: out[i] = bf16(q[ids[i], :] * scale + bias), the
  * dequantised row rounded once to bf16 (no scale factor).
  *   ids int32 [n] on the device, n >= 1;  out bf16 [n, H], 16-byte aligned.

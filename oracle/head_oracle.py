@@ -53,6 +53,20 @@ def head_logits(x_bits, head: dict, cap: float = SOFTCAP, rows=None) -> np.ndarr
     return out
 
 
+def dense(x_bits, w: dict) -> np.ndarray:
+    """y[t, n] = (W x_t)[n] for a dense 4-bit affine matrix W [N, K] (dict
+    q/s/b, the format of the head and of the attention projections: page
+    "TurboFieldfare - System design", section ".gturbo directory", stores the
+    attention weights 4-bit affine, group 64, like the embedding); float64
+    [T, N]."""
+    x = bf16_to_f64(x_bits)
+    out = np.full((x.shape[0], w["q"].shape[0]), np.nan)  # a row block left out stays visible
+    for b0 in range(0, out.shape[1], ROW_BLOCK):
+        sel = slice(b0, min(out.shape[1], b0 + ROW_BLOCK))
+        out[:, sel] = x @ dequantize(w["q"][sel], w["s"][sel], w["b"][sel], 4).T
+    return out
+
+
 def greedy_token(logits) -> np.ndarray:
     """Index of the largest logit per row, the lowest index among equal
     maxima; int64 [T]."""

@@ -12,6 +12,10 @@ against a copy with a planted mistake.
                      (the dequantisation fixtures)
   pin_greedy         argmax with ties to the lower id, -inf entries
   pin_embed          tied embedding = dequantised row (hand-worked fixtures)
+  pin_dense_exact    the dense projection on unit scales, zero biases and
+                     small integer inputs equals the exact int64 product
+  pin_dense_brute    the dense projection of a tiny matrix against the
+                     plain-Python scalar brute force, row blocking included
 """
 from __future__ import annotations
 
@@ -131,4 +135,37 @@ def pin_embed(h):
         assert np.array_equal(got[i], want)
 
 
-ALL_HEAD_PINS = [pin_softcap, pin_head_brute, pin_head_rows, pin_head_onehot, pin_greedy, pin_embed]
+def pin_dense_exact(h):
+    rng = np.random.default_rng(7)
+    n, k, t = 48, 192, 3
+    codes = rng.integers(0, 16, size=(n, k))
+    q = np.zeros((n, k // 8), dtype=np.uint32)
+    for i in range(8):
+        q |= (codes[:, i::8].astype(np.uint32) << np.uint32(4 * i))
+    one = _bf16(1.0)
+    w = {"q": q, "s": np.full((n, k // 64), one, dtype=np.uint16), "b": np.zeros((n, k // 64), dtype=np.uint16)}
+    xi = rng.integers(-8, 9, size=(t, k))
+    x = gen.to_bf16_bits(xi.astype(np.float64))
+    want = xi.astype(np.int64) @ codes.astype(np.int64).T
+    assert np.array_equal(h.dense(x, w), want.astype(np.float64))
+
+
+def pin_dense_brute(h):
+    n, k, t = 24, 128, 2
+    w = gen.head_weights(4, n, k)
+    x = gen.hidden_states(4, 0, t, k, rms_normalize=True)
+    rows = {"q": w["q"].tolist(), "s": w["s"].tolist(), "b": w["b"].tolist()}
+    old = h.ROW_BLOCK
+    try:
+        for block in (old, 5):
+            h.ROW_BLOCK = block
+            got = h.dense(x, w)
+            for ti in range(t):
+                want = np.array(_brute.matvec(rows, 4, [_brute.bf16(v) for v in x[ti].tolist()]))
+                assert np.max(np.abs(got[ti] - want)) <= 1e-13 * max(1.0, np.max(np.abs(want)))
+    finally:
+        h.ROW_BLOCK = old
+
+
+ALL_HEAD_PINS = [pin_softcap, pin_head_brute, pin_head_rows, pin_head_onehot, pin_greedy, pin_embed,
+                 pin_dense_exact, pin_dense_brute]

@@ -144,3 +144,38 @@ def test_head_then_embed_chained(moe):
     assert moe.get_error() == bq.MOE_OK
     tk = tokens.cpu().numpy()
     assert np.array_equal(from_dev_bf16(out), HO.embed(np.arange(T), head.host_rows(tk)))
+
+
+@pytest.mark.parametrize("N,K,T", [(4096, 2816, 1), (2816, 4096, 4), (1024, 256, 8), (16, 64, 3)])
+def test_dense_projection(moe, N, K, T):
+    """The dense 4-bit projection (Q/K/V- and O-like shapes; the pages give the
+    format, not the attention's sizes): fp32 and bf16 outputs against the
+    float64 oracle, and each output alone gives the same values."""
+    w = DeviceHead(21, N, K)
+    x = _x(22, T, K, 1.0)
+    y32 = torch.empty((T, N), dtype=torch.float32, device="cuda")
+    y16 = torch.empty((T, N), dtype=torch.int16, device="cuda")
+    moe.dense_forward(to_dev_bf16(x), T, _hw(w), y=y16, y32=y32)
+    torch.cuda.synchronize()
+    assert moe.get_error() == bq.MOE_OK
+    ref = HO.dense(x, w.host_rows())
+    got32 = y32.cpu().numpy().astype(np.float64)
+    assert_close(got32, ref, "dense fp32")
+    got16 = from_dev_bf16(y16)
+    assert np.array_equal(got16, gen.to_bf16_bits(got32.astype(np.float32).astype(np.float64)))
+    only16 = torch.empty_like(y16)
+    moe.dense_forward(to_dev_bf16(x), T, _hw(w), y=only16)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev_bf16(only16), got16)
+
+
+def test_dense_projection_leaves_greedy_state(moe):
+    """A projection between two head calls must not disturb the head's argmax state."""
+    head = DeviceHead(23, 1024, 256)
+    x = _x(24, 2, 256, 30.0)
+    _, t0 = _run(moe, head, x)
+    w = DeviceHead(25, 512, 256)
+    y = torch.empty((2, 512), dtype=torch.float32, device="cuda")
+    moe.dense_forward(to_dev_bf16(_x(26, 2, 256, 1.0)), 2, _hw(w), y32=y)
+    _, t1 = _run(moe, head, x)
+    assert np.array_equal(t0, t1)

@@ -74,6 +74,10 @@ HEAD_MUTATIONS = {
     "greedy_ties_to_higher": ("out[t] = int(np.flatnonzero(lg[t] == m)[0])", "out[t] = int(np.flatnonzero(lg[t] == m)[-1])"),
     "greedy_argmin": ("m = lg[t].max()", "m = lg[t].min()"),
     "row_block_short": ("sel = idx[b0:b0 + ROW_BLOCK]", "sel = idx[b0:b0 + ROW_BLOCK - 1]"),
+    "dense_block_short": ("sel = slice(b0, min(out.shape[1], b0 + ROW_BLOCK))",
+                          "sel = slice(b0, min(out.shape[1], b0 + ROW_BLOCK - 1))"),
+    "dense_scale_for_bias": ("w[\"s\"][sel], w[\"b\"][sel], 4).T", "w[\"s\"][sel], w[\"s\"][sel], 4).T"),
+    "dense_rows_reversed": ("out[:, sel] = x @ dequantize", "out[:, sel][:, ::-1] = x @ dequantize"),
     "embed_unrounded_rows_shifted": ("w = dequantize(head[\"q\"][ids], head[\"s\"][ids], head[\"b\"][ids], 4)",
                                      "w = dequantize(head[\"q\"][ids], head[\"s\"][ids[::-1]], head[\"b\"][ids], 4)"),
 }
