@@ -23,6 +23,7 @@ struct moe_handle {
   bool prefill;               // multi-token layer calls use the fused prefill kernel
   int prefill_key[4], prefill_ok;  // cached check (hidden, inter, n_experts, top_k) -> usable
   bool head_ready;            // the head kernel's attributes are set (first head call)
+  bool prefill_dense;         // multi-token calls may run dense slots on the tensor cores (tcgen05)
   // failure-detection hook, consumed by the next fused single-token launch
   int skip_block_next;                  // -1: none
   unsigned long long wait_ns_next;      // 0: the default limit
@@ -307,7 +308,7 @@ int run_prefill(moe_handle *h, const moe_layer_weights *w, int T, const void *x,
   a.err = h->dwords;
   a.trace = take_trace(h, 1);
   a.normalize = normalize;
-  return cuda_status(moe::launch_prefill_fused(a, h->n_sm, st, h->pdl));
+  return cuda_status(moe::launch_prefill_fused(a, h->n_sm, st, h->pdl, h->prefill_dense));
 }
 
 int run_ffn(moe_handle *h, const moe_layer_weights *w, int T, const void *x, const moe::Routing &r, int include_shared,
@@ -371,6 +372,11 @@ int moe_create(moe_handle **out) {
   h->fused = !(fz && fz[0] == '0');
   const char *pz = getenv("MOE_PREFILL_FUSED");
   h->prefill = !(pz && pz[0] == '0');
+  // the tcgen05 instance of the multi-token kernel for dense slots: opt-in
+  // (MOE_PREFILL_DENSE=1); on the target workloads it is not yet faster than
+  // the default instance
+  const char *dz = getenv("MOE_PREFILL_DENSE");
+  h->prefill_dense = dz && dz[0] == '1';
   if (cudaMalloc(&h->dwords, device_words(h->n_sm) * sizeof(unsigned)) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;

@@ -13,6 +13,17 @@ constexpr int kConsThreads = kCons * 32;     // 512
 constexpr int kThreads = kConsThreads + 32;  // + producer warp
 
 __device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsThreads) : "memory"); }
+// Barrier of the consumer warps that also ANDs a predicate over them (so a
+// bounded wait that ran out in some threads only is seen by all).
+__device__ __forceinline__ bool cons_sync_and(bool v) {
+  uint32_t res;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(res)
+      : "r"((uint32_t)v), "n"(kConsThreads)
+      : "memory");
+  return res != 0;
+}
 
 __device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long *p) {
   unsigned long long v;

@@ -141,7 +141,8 @@ cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t st, bool pdl);
 size_t prefill_fused_smem(const Dims &d);  // 0: shape not supported
 int prefill_blocks_per_sm(const Dims &d);
 cudaError_t prefill_set_attributes();
-cudaError_t launch_prefill_fused(const PrefillArgs &a, int n_blocks, cudaStream_t st, bool pdl);
+// allow_dense: slots with many rows in the chunk may take the tcgen05 path
+cudaError_t launch_prefill_fused(const PrefillArgs &a, int n_blocks, cudaStream_t st, bool pdl, bool allow_dense);
 
 size_t fused_decode_smem(const Dims &d);
 int decode_blocks_per_sm(const Dims &d);

@@ -30,7 +30,9 @@
 // nibbles come out * 16 and meet activations stored / 16), per-group
 // correction (scale * 2^24) * acc + bias * sum(x).
 #include <math.h>
+#include <string.h>
 
+#include "dense.cuh"
 #include "fused.cuh"
 #include "kernels.h"
 
@@ -49,9 +51,14 @@ constexpr int kNBar = 3;     // grid barriers per launch
 constexpr int kRedBytes = kCons * 256 * 4;
 
 // misc: s_flag int[16] | s_hst fp16[8][16] (group 0) | s_logit float[128] | s_part float[16] |
-// mbarriers [10] | s_wt float[8] (group 0) | s_hst (group 1) | s_wt (group 1)
+// mbarriers [10] | s_wt float[8] (group 0) | s_hst (group 1) | s_wt (group 1) | dense-path mbarriers [14] |
+// tensor-memory address
 constexpr int kMiscHst = 64, kMiscLogit = 320, kMiscPart = 832, kMiscBar = 896, kMiscWt = 976, kMiscHst1 = 1024,
-              kMiscWt1 = 1280, kMiscBytes = 1536;
+              kMiscWt1 = 1280, kMiscDBar = 1320, kMiscTmem = 1432, kMiscBytes = 1536;
+constexpr int kMmaWarp = kCons + 1;             // issues the tcgen05.mma of dense blocks
+constexpr int kThreadsP = fused::kThreads + 32;  // consumers + producer + MMA warp
+constexpr int kMaxDense = 64;  // dense slots of a chunk (at most T*k / dense::kMinRows + 1)
+static_assert(kMaxTokens * kMaxTopK / dense::kMinRows + 1 <= kMaxDense, "every dense slot has a list entry");
 
 __host__ __device__ inline int pw8(int w) { return w + ((8 - (w % 16)) + 16) % 16; }
 __host__ __device__ inline int al16(int v) { return (v + 15) & ~15; }
@@ -78,7 +85,7 @@ struct PL {
 // fragment loads (8 mod 32 words for the 8-byte gate/up loads, 64 mod 128
 // bytes for the 16-byte router loads); down codes keep a row pitch of 8 mod
 // 16 words; operand rows 4 mod 8 words; quarter sums: see qsum_pitch.
-__host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) {
+__host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T, bool dense = false) {
   PL L;
   L.G = H / kGroup;
   L.GI = I / kGroup;
@@ -109,8 +116,12 @@ __host__ __device__ inline PL prefill_layout(int H, int I, int E, int k, int T) 
   o += L.xbuf;
   L.red = o;  // cross-warp reductions, grouping temporaries
   o += imax(kRedBytes, (1 + kCons) * E * 4);
-  L.grp = o;  // chunk0 int32 [E+2], perm/pos int16 [T*k], act_e/beg/cnt int16 [E+1]
-  o = al16(o + (E + 2) * 4 + 2 * T * k * 2 + 3 * (E + 1) * 2);
+  // the dense instance reuses ring, X and red (from L.ring, aligned up to 1 KB) for its own plan
+  if (dense) o = imax(o, L.ring + dense::plan(L.G).total + 1024);
+  L.grp = o;  // chunk0 int32 [E+2], perm/pos int16 [T*k], act_e/beg/cnt int16 [E+1], dense slots int16
+              // [kMaxDense], token -> position int16 [kMaxTokens], position weights float [kMaxTokens]
+  o = al16(o + (E + 2) * 4 + 2 * T * k * 2 + 3 * (E + 1) * 2 + kMaxDense * 2 + kMaxTokens * 2);
+  o = al16(o + kMaxTokens * 4);
   L.misc = o;
   o = al16(o + kMiscBytes);
   L.total = o;
@@ -322,6 +333,11 @@ __device__ __forceinline__ Unit decode_unit(int u, int per, const int *chunk0, i
 }
 }  // namespace
 
+size_t prefill_dense_smem(const Dims &d) {
+  const PL L = prefill_layout(d.H, d.I, d.E, d.k, d.T, true);
+  return L.total <= 227 * 1024 ? (size_t)L.total : 0;
+}
+
 size_t prefill_fused_smem(const Dims &d) {
   const PL L = prefill_layout(d.H, d.I, d.E, d.k, d.T);
   return L.total <= 227 * 1024 ? (size_t)L.total : 0;
@@ -331,15 +347,20 @@ namespace {
 // Kernel parameters: the arguments and the shared-memory layout (computed on
 // the host, so its fields are read from the parameter bank, not registers).
 struct PrefillParams {
+  dense::Maps dm;  // tensor maps of the dense path (64-byte aligned: first)
   PrefillArgs a;
   PL L;
+  int dense_on;    // slots with at least dense::kMinRows rows take the tcgen05 path
 };
 }  // namespace
 
 // kScales: the layer has learned router scales (the router-scale code is
 // compiled out of the plain instance).
-template <bool kScales>
-__global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const PrefillParams prm) {
+// kDense: the instance with the tcgen05 path for dense slots (one more warp,
+// the MMA warp); the plain instance compiles the light path alone.
+template <bool kScales, bool kDense>
+__global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
+    prefill_layer_kernel(const __grid_constant__ PrefillParams prm) {
   extern __shared__ __align__(128) uint8_t smem[];
   const PrefillArgs &a = prm.a;
   const PL &L = prm.L;
@@ -357,6 +378,22 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   int16_t *g_act_e = g_pos + npairs;                                    // [E+1]
   int16_t *g_act_beg = g_act_e + (E + 1);                               // [E+1]
   int16_t *g_act_cnt = g_act_beg + (E + 1);                             // [E+1]
+  int16_t *g_dense = g_act_cnt + (E + 1);                               // [kMaxDense] dense active slots
+  int16_t *g_tpos = g_dense + kMaxDense;                                // [kMaxTokens] token -> position (dense unit)
+  float *g_wpos = reinterpret_cast<float *>(smem + L.grp + ((((E + 2) * 4 + 2 * npairs * 2 + 3 * (E + 1) * 2 +
+                                                               kMaxDense * 2 + kMaxTokens * 2) + 15) & ~15));
+  // the dense path: its plan on a 1 KB boundary inside ring + X + red, its barriers, tensor memory
+  uint8_t *dbase = smem + L.ring + ((1024u - (smem_addr(smem + L.ring) & 1023u)) & 1023u);
+  const dense::Plan DP = dense::plan(G);
+  uint64_t *ddfull = reinterpret_cast<uint64_t *>(smem + L.misc + kMiscDBar);  // [kStages] TMA landed
+  uint64_t *ddempty = ddfull + dense::kStages;                                  // [kStages] MMAs done with a stage
+  uint64_t *dadone = ddempty + dense::kStages;                                  // [2] MMAs done with an A buffer
+  uint64_t *dsfull = dadone + 2;                                                // scales of the unit landed
+  uint64_t *dsempty = dsfull + 1;                                               // scales consumed (every warp)
+  uint64_t *dafull = dsempty + 1;                                               // [2] A buffer written (every warp)
+  uint64_t *dtfree = dafull + 2;                                                // epilogue done with tensor memory
+  uint64_t *dtready = dtfree + 1;                                               // tensor memory allocated
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + L.misc + kMiscTmem);
   int *s_flag = reinterpret_cast<int *>(smem + L.misc);
   float *s_logit = reinterpret_cast<float *>(smem + L.misc + kMiscLogit);
   float *s_part = reinterpret_cast<float *>(smem + L.misc + kMiscPart);
@@ -384,6 +421,18 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     mbar_init(xempty, 2);  // one arrival per consumer group
     mbar_init(route, 1);
     mbar_init(hready, 1);
+    for (int i = 0; i < dense::kStages; ++i) {
+      mbar_init(&ddfull[i], 1);
+      mbar_init(&ddempty[i], 1);
+    }
+    mbar_init(&dadone[0], 1);
+    mbar_init(&dadone[1], 1);
+    mbar_init(dsfull, 1);
+    mbar_init(dsempty, kCons);
+    mbar_init(&dafull[0], kCons);
+    mbar_init(&dafull[1], kCons);
+    mbar_init(dtfree, 1);
+    mbar_init(dtready, 1);
     fence_mbar_init();
     s_flag[8] = 0;  // abort
   }
@@ -415,14 +464,90 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     }
     if (ok) ok = mbar_wait_idle(route, 0, 32) && *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
     fused::fence_proxy_async_global();  // operand rows written by other blocks before barrier 1
-    if (ok) {
+    const int nbl = (kDense && ok) ? s_flag[11] : nb;  // light blocks; the rest take the dense slots
+    int dgi = 0, du = 0;                   // dense path: K groups issued, units whose scales went out
+    if (kDense && ok && c >= nbl) {
+     if constexpr (kDense) {
+      // ---- dense block: per unit the scales and biases (one bulk copy per
+      // array), then per K group the operand rows (2-D TMA, 128-byte swizzle)
+      // and the codes of 128 weight rows (3-D TMA) into a kStages ring
+      const int nd = s_flag[10], nblk = nb - nbl, db = c - nbl;
+      auto dense_loads = [&](bool down) {
+        const int ntile = ((down ? H : I) + dense::kRows - 1) / dense::kRows;
+        const int kg = down ? GI : G;
+        for (int u = db; u < nd * ntile && ok; u += nblk) {
+          const int ds = u / ntile, rt = u - ds * ntile, sa = g_dense[ds];
+          const int e = g_act_e[sa];
+          const int sh = e < 0 ? 1 : 0;
+          const uint8_t *blob = sh ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
+          const int r0 = rt * dense::kRows, nrows = min(dense::kRows, (down ? H : I) - r0);
+          if (du >= 1) ok = __all_sync(0xffffffffu, mbar_wait_idle(dsempty, (du - 1) & 1, 32));
+          if (!ok) break;
+          const int nf = down ? 2 : 4;
+          if (lane == 0) mbar_arrive_expect_tx(dsfull, (uint32_t)(nf * nrows * kg * 2));
+          __syncwarp();
+          if (lane < nf) {
+            const size_t off = down ? (lane == 0 ? a.w.off.down_s : a.w.off.down_b)
+                                    : (lane == 0 ? a.w.off.gate_s
+                                                 : lane == 1 ? a.w.off.gate_b : lane == 2 ? a.w.off.up_s : a.w.off.up_b);
+            bulk_g2s(dbase + DP.s + lane * dense::kRows * kg * 2, blob + off + (size_t)r0 * kg * 2,
+                     (uint32_t)(nrows * kg * 2), dsfull);
+          }
+          ++du;
+          const int by = down ? g_act_beg[sa] : 0;  // first operand row: the slot's positions, or token 0
+          // the first groups' codes into L2 (later groups: kAhead ahead of their TMA below)
+          if (lane == 0)
+            for (int g = 0; g < kg && g < dense::kAhead; ++g) {
+              if (down) {
+                dense::tma_prefetch_3d(&prm.dm.dq[sh], 32 * g, r0, sh ? 0 : e);
+              } else {
+                dense::tma_prefetch_3d(&prm.dm.gq[sh], 32 * g, r0, sh ? 0 : e);
+                dense::tma_prefetch_3d(&prm.dm.uq[sh], 32 * g, r0, sh ? 0 : e);
+              }
+            }
+          for (int g = 0; g < kg && ok; ++g, ++dgi) {
+            const int st = dgi % dense::kStages;
+            if (dgi >= dense::kStages)
+              ok = __all_sync(0xffffffffu, mbar_wait_idle(&ddempty[st], ((dgi / dense::kStages) - 1) & 1, 32));
+            if (!ok) break;
+            if (lane == 0) {
+              const int gp = g + dense::kAhead;
+              if (gp < kg) {
+                if (down) {
+                  dense::tma_prefetch_3d(&prm.dm.dq[sh], 32 * gp, r0, sh ? 0 : e);
+                } else {
+                  dense::tma_prefetch_3d(&prm.dm.gq[sh], 32 * gp, r0, sh ? 0 : e);
+                  dense::tma_prefetch_3d(&prm.dm.uq[sh], 32 * gp, r0, sh ? 0 : e);
+                }
+              }
+              mbar_arrive_expect_tx(&ddfull[st], (uint32_t)(dense::kRows * 128 + (down ? 1 : 2) * dense::kRows * 32));
+              dense::tma_load_2d(dbase + DP.b[st], down ? &prm.dm.h : &prm.dm.x, 64 * g, by, &ddfull[st]);
+              if (down) {
+                dense::tma_load_3d(dbase + DP.c[st], &prm.dm.dq[sh], 32 * g, r0, sh ? 0 : e, &ddfull[st]);
+              } else {
+                dense::tma_load_3d(dbase + DP.c[st], &prm.dm.gq[sh], 32 * g, r0, sh ? 0 : e, &ddfull[st]);
+                dense::tma_load_3d(dbase + DP.c[st] + dense::kRows * 32, &prm.dm.uq[sh], 32 * g, r0, sh ? 0 : e,
+                                   &ddfull[st]);
+              }
+            }
+            __syncwarp();
+          }
+        }
+      };
+      dense_loads(false);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_idle(hready, 0, 32)) &&
+                   *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
+      fused::fence_proxy_async_global();  // h rows written by other blocks before barrier 2
+      if (ok) dense_loads(true);
+     }
+    } else if (ok) {
       const int nact = s_flag[9];
       const int nchunks = chunk0[nact];
       const int n_gu = nchunks * L.nrt, n_dn = nchunks * L.nrt_dn;
       int cur = -1;
       // gate/up: weight tile, then the chunk's operand rows when the chunk changes
       const uint8_t *blob = nullptr;  // weights of the current chunk's slot
-      for (int u = c * n_gu / nb; u < (c + 1) * n_gu / nb && ok; ++u) {
+      for (int u = c * n_gu / nbl; u < (c + 1) * n_gu / nbl && ok; ++u) {
         const int chg = u / L.nrt, tile = u - chg * L.nrt;
         Unit x;
         if (chg != cur) {
@@ -467,7 +592,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       // h rows of a chunk once every block has written them
       bool hr = false;
       cur = -1;
-      for (int u = c * n_dn / nb; u < (c + 1) * n_dn / nb && ok; ++u) {
+      for (int u = c * n_dn / nbl; u < (c + 1) * n_dn / nbl && ok; ++u) {
         const int chg = u / L.nrt_dn, tile = u - chg * L.nrt_dn;
         Unit x;
         if (chg != cur) {
@@ -523,7 +648,73 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       if (!ok) set_error(a.err, kErrTimeout);
       for (int j = it - kWSlots > 0 ? it - kWSlots : 0; j < it; ++j) mbar_wait_idle(&full[j % kWSlots], (j / kWSlots) & 1);
       if (xk >= 1) mbar_wait_idle(xfull, (xk - 1) & 1);
+      for (int j = dgi - dense::kStages > 0 ? dgi - dense::kStages : 0; j < dgi; ++j)
+        mbar_wait_idle(&ddfull[j % dense::kStages], (j / dense::kStages) & 1);
+      if (du >= 1) mbar_wait_idle(dsfull, (du - 1) & 1);
     }
+    return;
+  }
+
+  // ============================================================ MMA warp
+  // Dense blocks only: owns the tensor memory (256 columns: gate, up) and
+  // issues each K group's tcgen05.mma once the consumers have written its A
+  // tile, so the dequantisation of the next group overlaps the MMAs.
+  if constexpr (kDense) if (warp == kMmaWarp) {
+    const bool okr = __all_sync(0xffffffffu, mbar_wait_idle(route, 0, 64)) &&
+                     *reinterpret_cast<volatile int *>(&s_flag[8]) == 0;
+    const int nbl = okr ? s_flag[11] : nb;
+    if (!okr || c < nbl) return;
+    dense::tc_alloc(s_tmem, 256);
+    dense::tc_fence_before();
+    __syncwarp();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
+    if (lane == 0) mbar_arrive_expect_tx(dtready, 0);
+    const int nd = s_flag[10], nblk = nb - nbl;
+    int dgi = 0, du = 0;
+    bool ok = true;
+    auto mma_units = [&](bool down) {
+      const int ntile = ((down ? H : I) + dense::kRows - 1) / dense::kRows;
+      const int kg = down ? GI : G;
+      const int nm = down ? 1 : 2;
+      for (int u = c - nbl; u < nd * ntile && ok; u += nblk) {
+        const int sa = g_dense[u / ntile];
+        const int N = ((down ? (int)g_act_cnt[sa] : T) + 15) & ~15;
+        const uint32_t idesc = dense::idesc_f16(dense::kRows, N);
+        if (du >= 1) ok = __all_sync(0xffffffffu, mbar_wait_idle(dtfree, (du - 1) & 1, 32));  // TMEM read out
+        ++du;
+        dense::tc_fence_after();
+        for (int g = 0; g < kg && ok; ++g) {
+          const int st = dgi % dense::kStages, ab = dgi & 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&ddfull[st], (dgi / dense::kStages) & 1) &&
+                                           mbar_wait(&dafull[ab], (dgi >> 1) & 1));
+          if (!ok) break;
+          dense::tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t bd = dense::sdesc(smem_addr(dbase + DP.b[st]) + ks * 32, 16, 1024, 2);
+              for (int m = 0; m < nm; ++m) {
+                const uint64_t ad =
+                    dense::sdesc(smem_addr(dbase + DP.a[ab] + m * dense::kRows * 128) + ks * 32, 16, 1024, 2);
+                dense::tc_mma(tmem + m * 128, ad, bd, idesc, (g > 0 || ks > 0) ? 1u : 0u);
+              }
+            }
+            dense::tc_commit(&ddempty[st]);  // the TMA stage may be refilled
+            dense::tc_commit(&dadone[ab]);   // the A buffer may be rewritten; after the last group: unit done
+          }
+          __syncwarp();
+          ++dgi;
+        }
+      }
+    };
+    mma_units(false);
+    if (ok) mma_units(true);
+    // tensor memory back once the last MMAs completed and the last epilogue read them (bounded waits)
+    if (dgi > 0) mbar_wait(&dadone[(dgi - 1) & 1], ((dgi - 1) >> 1) & 1);
+    if (du > 0) mbar_wait_idle(dtfree, (du - 1) & 1, 64);
+    dense::tc_fence_after();
+    __syncwarp();
+    dense::tc_dealloc(tmem, 256);
     return;
   }
 
@@ -742,7 +933,8 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
     cons_sync();
     if (warp == 0) {
       // exclusive scan of counts -> fill positions; active slots (shared first); chunk prefix
-      int run = 0, nact = 1, chunks = (T + kTC - 1) / kTC;
+      const bool don = kDense && prm.dense_on != 0;
+      int run = 0, nact = 1, chunks = (don && T >= dense::kMinRows) ? 0 : (T + kTC - 1) / kTC;
       if (lane == 0) {
         g_act_e[0] = -1;
         g_act_beg[0] = (int16_t)npairs;
@@ -758,7 +950,7 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
           const int v = __shfl_up_sync(0xffffffffu, incl, off);
           if (lane >= off) incl += v;
         }
-        const int nch = (ce + kTC - 1) / kTC;
+        const int nch = (don && ce >= dense::kMinRows) ? 0 : (ce + kTC - 1) / kTC;
         int incl_ch = nch;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -781,6 +973,37 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
       if (lane == 0) {
         chunk0[nact] = chunks;
         s_flag[9] = nact;
+      }
+      __syncwarp();
+      // dense slots in active-slot order; the blocks that take them: the
+      // last n_db blocks, as many as the cost of their gate/up units asks
+      // for against the light ones (a dense unit ~ dense::kGuCost light units)
+      int nd = 0;
+      for (int a0 = 0; a0 < nact; a0 += 32) {
+        const int sa = a0 + lane;
+        const bool dn = don && sa < nact && g_act_cnt[sa] >= dense::kMinRows;
+        const unsigned bal = __ballot_sync(0xffffffffu, dn);
+        if (dn && nd + __popc(bal & lanemask_lt()) < kMaxDense) g_dense[nd + __popc(bal & lanemask_lt())] = (int16_t)sa;
+        nd += __popc(bal);
+      }
+      if (lane == 0) {
+        nd = nd < kMaxDense ? nd : kMaxDense;
+        const int n_dg = nd * ((I + dense::kRows - 1) / dense::kRows);
+        const int n_dd = nd * ((H + dense::kRows - 1) / dense::kRows);
+        const float dc = (float)n_dg * dense::kGuCost + (float)n_dd * dense::kDnCost;
+        const float lc = (float)chunks * ((float)L.nrt + (float)L.nrt_dn);
+        // at least one dense block per gate/up unit while they are few: a
+        // second unit on one block would hold every block at barrier 2
+        int ndb = 0;
+        if (n_dg > 0) {
+          ndb = lc > 0.f ? (int)rintf((float)nb * dc / (dc + lc)) : nb;
+          if (n_dg <= nb / 4 && ndb < n_dg) ndb = n_dg;
+          ndb = ndb < 1 ? 1 : ndb;
+          ndb = ndb > n_dg ? n_dg : ndb;
+          if (lc > 0.f && ndb > nb - 1) ndb = nb - 1;
+        }
+        s_flag[10] = nd;
+        s_flag[11] = nb - ndb;  // light blocks [0, nbl), dense blocks [nbl, nb)
       }
     }
     cons_sync();
@@ -819,14 +1042,154 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
 
   const int nact = aborted ? 0 : s_flag[9];
   const int nchunks = aborted ? 0 : chunk0[nact];
+  const int nbl = (kDense && !aborted) ? s_flag[11] : nb;  // light blocks [0, nbl); dense blocks [nbl, nb)
+  const bool dense_blk = kDense && !aborted && c >= nbl;
+
+  // ---- dense blocks: the MMA warp owns the tensor memory of the
+  // accumulators (gate in columns 0..127, up in 128..255; down uses the
+  // first 128); its address once the allocation is done
+  uint32_t tmem = 0;
+  bool have_tmem = false;
+  int dgi = 0, du = 0;  // K groups consumed, units whose scales were consumed
+  // The dense units of this block: (dense slot, 128 weight rows) for u = c -
+  // nbl, c - nbl + (nb - nbl), ...  Gate/up: A = 128 rows of gate and of up,
+  // B = the chunk's operand rows (every token; the epilogue keeps those
+  // routed to the slot).  Down: A = 128 rows of W_down, B = h of the slot's
+  // sorted positions.  Per K group every consumer thread dequantises one
+  // quarter (down: one eighth) of the A tiles and each warp signals the MMA
+  // warp, which issues the K = 64 step as four tcgen05.mma per matrix.
+  auto dense_units = [&](bool down) {
+    const int nd = s_flag[10], nblk = nb - nbl;
+    const int ntile = ((down ? H : I) + dense::kRows - 1) / dense::kRows;
+    const int kg = down ? GI : G;
+    const uint16_t *sb = reinterpret_cast<const uint16_t *>(dbase + DP.s);
+    for (int u = c - nbl; u < nd * ntile && !aborted; u += nblk) {
+      const int ds = u / ntile, rt = u - ds * ntile, sa = g_dense[ds];
+      const int e = g_act_e[sa], beg = g_act_beg[sa], cnt = g_act_cnt[sa];
+      const int r0 = rt * dense::kRows, nrows = min(dense::kRows, (down ? H : I) - r0);
+      const int N = ((down ? cnt : T) + 15) & ~15;  // MMA N: operand rows, padded to 16
+      if (!down) {
+        for (int t = tid; t < T; t += kConsThreads) {  // token -> its position in this slot, or -1
+          int pos = -1;
+          if (e < 0) {
+            pos = npairs + t;
+          } else {
+            for (int j = 0; j < k; ++j)
+              if (__ldcg(a.r.ids + t * k + j) == e) pos = g_pos[t * k + j];
+          }
+          g_tpos[t] = (int16_t)pos;
+        }
+      } else {
+        for (int n = tid; n < cnt; n += kConsThreads) g_wpos[n] = e < 0 ? 1.0f : __ldcg(a.r.wts + g_perm[beg + n]);
+      }
+      cons_sync();  // the tables are complete before any warp's epilogue reads them
+      bool okd = mbar_wait(dsfull, du & 1);
+      ++du;
+      for (int g = 0; g < kg; ++g, ++dgi) {
+        const int st = dgi % dense::kStages, ab = dgi & 1;
+        okd = okd && mbar_wait(&ddfull[st], (dgi / dense::kStages) & 1);
+        if (dgi >= 2) okd = okd && mbar_wait(&dadone[ab], ((dgi >> 1) - 1) & 1);
+        if (okd) {
+          const uint8_t *cb = dbase + DP.c[st];
+          uint8_t *ab_ = dbase + DP.a[ab];
+          const int rr = tid & 127;
+          if (!down) {
+            const int m = tid >> 8, hh = (tid >> 7) & 1;  // matrix (gate, up), half of the group
+            const uint4 cw = *reinterpret_cast<const uint4 *>(cb + m * dense::kRows * 32 + rr * 32 + hh * 16);
+            const float sf = bf16_bits_to_float(sb[(2 * m) * dense::kRows * kg + rr * kg + g]);
+            const float bf = bf16_bits_to_float(sb[(2 * m + 1) * dense::kRows * kg + rr * kg + g]);
+            const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
+            // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
+            uint8_t *row = ab_ + m * dense::kRows * 128 + rr * 128;
+            const int sw = rr & 7, j0 = 4 * hh;
+            *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
+            *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
+            *reinterpret_cast<uint4 *>(row + ((j0 + 2) ^ sw) * 16) = dense::dequant_word(cw.z, s2, b2, b16);
+            *reinterpret_cast<uint4 *>(row + ((j0 + 3) ^ sw) * 16) = dense::dequant_word(cw.w, s2, b2, b16);
+          } else {
+            const int qq = tid >> 7;  // quarter of the group
+            const uint2 cw = *reinterpret_cast<const uint2 *>(cb + rr * 32 + qq * 8);
+            const float sf = bf16_bits_to_float(sb[rr * kg + g]);
+            const float bf = bf16_bits_to_float(sb[dense::kRows * kg + rr * kg + g]);
+            const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
+            uint8_t *row = ab_ + rr * 128;
+            const int sw = rr & 7, j0 = 2 * qq;
+            *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
+            *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
+          }
+        }
+        dense::fence_async_smem();  // the A tiles, written by threads, are read by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&dafull[ab], 0);  // this warp's part of the A tile is in place
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(dsempty, 0);  // this warp is done with the unit's scales
+      okd = okd && mbar_wait(&dadone[(dgi - 1) & 1], ((dgi - 1) >> 1) & 1);  // every MMA of the unit done
+      if (!have_tmem) {
+        okd = okd && mbar_wait(dtready, 0);
+        tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
+        have_tmem = true;
+      }
+      okd = __all_sync(0xffffffffu, okd);  // tcgen05.ld below is warp-collective
+      dense::tc_fence_after();
+      // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (weight
+      // rows) and columns 32 (w / 4) .. +31 (operand rows)
+      const int w4 = warp & 3, cbk = warp >> 2, rr = 32 * w4 + lane;
+      if (okd && 32 * cbk < N) {
+        const uint32_t ta = tmem + ((uint32_t)(32 * w4) << 16) + 32 * cbk;
+        bool odd = false;
+        const int i = r0 + rr;
+        const int slot = dense::operand_slot(i & 63, odd);
+        for (int hf = 0; hf < 2; ++hf) {  // 16 columns at a time
+          if (!down) {
+            float gv[16], uv[16];
+            dense::tc_ld16(ta + 16 * hf, gv);
+            dense::tc_ld16(ta + 128 + 16 * hf, uv);
+            if (rr < nrows) {
+              __half *dst = a.hperm + (i & ~63) + slot;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int t = 32 * cbk + 16 * hf + j;
+                const int pos = t < T ? g_tpos[t] : -1;
+                if (pos >= 0) {
+                  const float hv = gelu_tanh(gv[j]) * uv[j];
+                  if (!(fabsf(hv) <= 65504.0f)) set_error(a.err, kErrNonFinite);
+                  dst[(size_t)pos * I] = __float2half_rn(odd ? hv * 0.0625f : hv);  // odd words / 16
+                }
+              }
+            }
+          } else {
+            float dv[16];
+            dense::tc_ld16(ta + 16 * hf, dv);
+            if (rr < nrows) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int n = 32 * cbk + 16 * hf + j;
+                if (n < cnt) a.obuf[(size_t)(beg + n) * H + r0 + rr] = g_wpos[n] * dv[j];
+              }
+            }
+          }
+        }
+      }
+      dense::tc_fence_before();
+      if (!fused::cons_sync_and(okd)) {
+        aborted = true;
+        set_error(a.err, kErrTimeout);
+        break;
+      }
+      if (tid == 0) mbar_arrive_expect_tx(dtfree, 0);  // the MMA warp may overwrite the accumulators
+    }
+  };
 
   // ---- G: gate/up units [c * n_gu / nb, (c + 1) * n_gu / nb).  Steps of two
   // consecutive units of one chunk (group 0 takes the first, group 1 the
   // second) or one unit at a chunk's end; both groups walk every step so they
   // leave each X phase (chunk) together.
-  {
+  if (dense_blk) {
+    if constexpr (kDense) dense_units(false);
+  } else {
     const int n_gu = nchunks * L.nrt;
-    const int lo = c * n_gu / nb, hi = (c + 1) * n_gu / nb;
+    const int lo = c * n_gu / nbl, hi = (c + 1) * n_gu / nbl;
     int u = lo, itu = it, ph = -1, xp = xk - 1, p0 = 0, nt = 0;
     while (u < hi && !aborted) {
       const int chg = u / L.nrt;
@@ -933,9 +1296,11 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   // ---- D: down units [c * n_dn / nb, (c + 1) * n_dn / nb) -> weighted outputs,
   // in the same two-group steps.  A group's warp w owns rows 16w..16w+15 of its
   // 128-row unit over the whole K, so its results leave straight from registers.
-  {
+  if (dense_blk) {
+    if constexpr (kDense) dense_units(true);
+  } else {
     const int n_dn = nchunks * L.nrt_dn;
-    const int lo = c * n_dn / nb, hi = (c + 1) * n_dn / nb;
+    const int lo = c * n_dn / nbl, hi = (c + 1) * n_dn / nbl;
     int u = lo, itu = it, ph = -1, xp = xk - 1, p0 = 0, nt = 0;
     while (u < hi && !aborted) {
       const int chg = u / L.nrt_dn;
@@ -1051,27 +1416,112 @@ __global__ void __launch_bounds__(fused::kThreads, 1) prefill_layer_kernel(const
   if (tid == 0) trace_max(a.trace, kTrExit);
 }
 
-cudaError_t launch_prefill_fused(const PrefillArgs &a, int n_blocks, cudaStream_t st, bool pdl) {
-  const PrefillParams prm{a, prefill_layout(a.d.H, a.d.I, a.d.E, a.d.k, a.d.T)};
+namespace {
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry
+// point (no link against the driver library)
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// A tensor map over a row-major tensor of `rank` dims (dims[0] innermost),
+// byte strides of dims 1.. in `strides`; out-of-range elements read as zero.
+bool encode(EncodeTiledFn f, CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
+            const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw,
+            CUtensorMapL2promotion l2) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return f(m, dt, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           sw, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The dense path's maps: operand rows of x and of h (fp16, boxes of 64
+// elements x 128 rows with the 128-byte swizzle the tensor cores read), and
+// the 4-bit codes of gate, up and down (boxes of 32 bytes x 128 rows of one
+// expert), for the routed experts (3-D over the fixed-stride blobs) and the
+// shared expert.
+bool dense_maps(const PrefillArgs &a, dense::Maps &dm) {
+  const EncodeTiledFn f = encode_fn();
+  if (!f) return false;
+  const cuuint64_t H = a.d.H, I = a.d.I, E = a.d.E, T = a.d.T, npos = (cuuint64_t)a.d.T * (a.d.k + 1);
+  const cuuint32_t bx[2] = {64, dense::kRows};
+  bool ok = true;
+  {
+    const cuuint64_t dims[2] = {H, T}, str[1] = {H * 2};
+    ok = ok && encode(f, &dm.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.xperm, dims, str, bx, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  }
+  {
+    const cuuint64_t dims[2] = {I, npos}, str[1] = {I * 2};
+    ok = ok && encode(f, &dm.h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.hperm, dims, str, bx, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  }
+  const cuuint32_t bq[3] = {32, dense::kRows, 1};
+  auto codes = [&](CUtensorMap *m, size_t off, cuuint64_t row_bytes, cuuint64_t rows) {
+    const cuuint64_t dr[3] = {row_bytes, rows, E}, sr[2] = {row_bytes, a.w.stride};
+    const cuuint64_t ds[3] = {row_bytes, rows, 1}, ss[2] = {row_bytes, row_bytes * rows};
+    return encode(f, &m[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w.experts + off, dr, sr, bq, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
+           encode(f, &m[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w.shared + off, ds, ss, bq, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  };
+  ok = ok && codes(dm.gq, a.w.off.gate_q, H / 2, I) && codes(dm.uq, a.w.off.up_q, H / 2, I) &&
+       codes(dm.dq, a.w.off.down_q, I / 2, H);
+  return ok;
+}
+}  // namespace
+
+cudaError_t launch_prefill_fused(const PrefillArgs &a, int n_blocks, cudaStream_t st, bool pdl, bool allow_dense) {
+  PrefillParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.a = a;
   const bool scales = a.w.router_scale != nullptr || a.w.expert_scale != nullptr;
-  return launch_k(scales ? prefill_layer_kernel<true> : prefill_layer_kernel<false>, dim3(n_blocks),
+  // the tcgen05 instance: only when asked for, the chunk can hold a dense
+  // slot, its shared memory fits one block per SM, and the maps encode
+  const size_t dsmem = allow_dense && a.d.T >= dense::kMinRows ? prefill_dense_smem(a.d) : 0;
+  bool dense_on = dsmem != 0;
+  if (dense_on) {
+    int n = 0;
+    dense_on = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                   &n, scales ? prefill_layer_kernel<true, true> : prefill_layer_kernel<false, true>, kThreadsP,
+                   dsmem) == cudaSuccess &&
+               n >= 1 && dense_maps(a, prm.dm);
+  }
+  prm.dense_on = dense_on ? 1 : 0;
+  prm.L = prefill_layout(a.d.H, a.d.I, a.d.E, a.d.k, a.d.T, dense_on);
+  if (dense_on)
+    return launch_k(scales ? prefill_layer_kernel<true, true> : prefill_layer_kernel<false, true>, dim3(n_blocks),
+                    dim3(kThreadsP), dsmem, st, pdl, prm);
+  return launch_k(scales ? prefill_layer_kernel<true, false> : prefill_layer_kernel<false, false>, dim3(n_blocks),
                   dim3(fused::kThreads), prefill_fused_smem(a.d), st, pdl, prm);
 }
 
 cudaError_t prefill_set_attributes() {
-  const cudaError_t e =
-      cudaFuncSetAttribute(prefill_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefill_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  const void *ks[4] = {(const void *)prefill_layer_kernel<false, false>, (const void *)prefill_layer_kernel<true, false>,
+                       (const void *)prefill_layer_kernel<false, true>, (const void *)prefill_layer_kernel<true, true>};
+  for (const void *kf : ks) {
+    const cudaError_t e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 int prefill_blocks_per_sm(const Dims &d) {
   const size_t smem = prefill_fused_smem(d);
   if (smem == 0) return 0;
   int n = 0, n2 = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_layer_kernel<false>, fused::kThreads, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_layer_kernel<false, false>, fused::kThreads, smem) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n2, prefill_layer_kernel<true>, fused::kThreads, smem) !=
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n2, prefill_layer_kernel<true, false>, fused::kThreads, smem) !=
           cudaSuccess)
     return 0;
   return n < n2 ? n : n2;

@@ -340,3 +340,39 @@ def test_bounded_wait_reports_timeout(moe):
     moe.selftest_wait_timeout(5_000_000)
     assert moe.get_error() == bq.MOE_ERR_TIMEOUT
     assert moe.get_error() == bq.MOE_OK     # cleared by the read
+
+
+@pytest.mark.parametrize("n_tokens,zipf", [(100, False), (100, True), (128, False), (128, True)],
+                         ids=["T100-uniform", "ragged100-zipf", "prefill128-uniform", "prefill128-zipf"])
+def test_prefill_dense_slots(layer0, layer0_zipf, n_tokens, zipf):
+    """Slots with at least 96 rows in the chunk (the shared expert; the heaviest
+    experts of a Zipf-skewed chunk) run on the tcgen05 path: weight tiles
+    dequantised once to fp16 in shared memory, tcgen05.mma into tensor memory.
+    Both paths must meet the oracle; their outputs differ in some bits (the
+    tcgen05 path rounds each weight to fp16), which shows the path ran.  The
+    routing is computed before the experts, so the ids are identical."""
+    import os
+    layer = layer0_zipf if zipf else layer0
+    x = hidden(77, n_tokens, n_tokens)
+    outs = {}
+    for dense in ("1", "0"):
+        old = os.environ.get("MOE_PREFILL_DENSE")
+        os.environ["MOE_PREFILL_DENSE"] = dense
+        try:
+            m = bq.Moe()
+        finally:
+            if old is None:
+                del os.environ["MOE_PREFILL_DENSE"]
+            else:
+                os.environ["MOE_PREFILL_DENSE"] = old
+        try:
+            out = run_layer(m, layer, x)
+        finally:
+            m.close()
+        assert out["status"] == bq.MOE_OK
+        _check_routing(out, layer, x, K)
+        ref = oracle_layer(layer, x, K, out["ids"])
+        assert_close(bf16_bits_to_f64(out["y"]), ref["y"], f"y (T={n_tokens}, dense={dense})")
+        outs[dense] = out
+    assert np.array_equal(outs["1"]["ids"], outs["0"]["ids"])
+    assert not np.array_equal(outs["1"]["y"], outs["0"]["y"]), "the tcgen05 path did not run"
