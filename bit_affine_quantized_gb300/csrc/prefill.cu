@@ -1306,14 +1306,16 @@ __global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
       const int chg = u / L.nrt_dn;
       const bool pair = u + 1 < hi && (u + 1) / L.nrt_dn == chg;
       if (chg != ph) {
+        // a down unit ends without a group barrier: only after this one has
+        // every warp of the group left the old chunk's h rows (and its
+        // routing weights), so only then may the producer refill them
+        gsync();
         if (ph >= 0 && gt == 0) fused::mbar_arrive_cnt(xempty, 1);
         ph = chg;
         ++xp;
         const Unit x = decode_unit(u, L.nrt_dn, chunk0, nact, g_act_e, g_act_beg, g_act_cnt);
         p0 = x.beg + kTC * x.ch;
         nt = x.nt;
-        // the chunk's routing weights for this group (after its last readers)
-        gsync();
         if (gt < nt) {
           const int pos = p0 + gt;
           s_wt_g[gt] = pos >= npairs ? 1.0f : __ldcg(a.r.wts + g_perm[pos]);
