@@ -55,6 +55,7 @@ constexpr int kRedBytes = kCons * 256 * 4;
 // tensor-memory address
 constexpr int kMiscHst = 64, kMiscLogit = 320, kMiscPart = 832, kMiscBar = 896, kMiscWt = 976, kMiscHst1 = 1024,
               kMiscWt1 = 1280, kMiscDBar = 1320, kMiscTmem = 1432, kMiscBytes = 1536;
+constexpr int kMiscLand = 1008;  // int [kWSlots]: last ring use seen landed per slot
 constexpr int kMmaWarp = kCons + 1;             // issues the tcgen05.mma of dense blocks
 constexpr int kThreadsP = fused::kThreads + 32;  // consumers + producer + MMA warp
 constexpr int kMaxDense = 64;  // dense slots of a chunk (at most T*k / dense::kMinRows + 1)
@@ -402,6 +403,13 @@ __global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
   uint64_t *xfull = empty + kWSlots;
   uint64_t *xempty = xfull + 1;
   uint64_t *route = xempty + 1;   // grouping ready
+  // The two consumer groups share the ring but each consumes only its own
+  // units, so a group can reach slot s for use j while use j - kWSlots (the
+  // other group's, in the same slot) has not landed yet: a parity wait then
+  // sees the older phase's parity and passes early.  Every consumer records
+  // here the use it saw land in each slot, and waits for use j only once
+  // use j - kWSlots is recorded.
+  volatile int *s_land = reinterpret_cast<volatile int *>(smem + L.misc + kMiscLand);
   uint64_t *hready = route + 1;   // all h written (barrier 2 passed)
   // per consumer group: h staging of a gate/up unit, routing weights of the current down chunk
   const int gi = (warp >> 3) & 1, wl = warp & 7, gt = tid & 255;
@@ -421,6 +429,7 @@ __global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
     mbar_init(xempty, 2);  // one arrival per consumer group
     mbar_init(route, 1);
     mbar_init(hready, 1);
+    for (int i = 0; i < kWSlots; ++i) s_land[i] = -1;
     for (int i = 0; i < dense::kStages; ++i) {
       mbar_init(&ddfull[i], 1);
       mbar_init(&ddempty[i], 1);
@@ -761,6 +770,19 @@ __global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
     if (lane == 0) fused::mbar_arrive_cnt(&empty[slot], 2);
   };
   auto gsync = [&]() { asm volatile("bar.sync %0, 256;" ::"r"(2 + gi) : "memory"); };
+  // ring use j of a group: wait until use j - kWSlots of its slot has landed
+  // (bounded), then for use j's own phase; record it
+  auto wait_use = [&](int j) -> bool {
+    const int slot = j % kWSlots;
+    if (j >= kWSlots && s_land[slot] < j - kWSlots) {
+      const unsigned long long t0 = global_ns();
+      while (s_land[slot] < j - kWSlots)
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    if (!mbar_wait(&full[slot], (j / kWSlots) & 1)) return false;
+    if (gt == 0) s_land[slot] = j;
+    return true;
+  };
   const uint16_t *src = a.hres ? a.hres : a.x;
   const int nquart = H / 16;
   const int r = lane >> 2, cq = lane & 3;
@@ -879,6 +901,7 @@ __global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
           aborted = true;
           set_error(a.err, kErrTimeout);
         } else {
+          if (tid == 0) s_land[slot] = it;  // every warp consumes router tiles, in order
           const uint8_t *tile = ring + slot * L.wslot;
           const uint16_t *rs = rsb + m * kRtRows * G, *rb = rsb + rsb_n + m * kRtRows * G;
           for (int g = warp; g < G; g += kCons)
@@ -1213,7 +1236,7 @@ __global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
       const int mine = gi == 0 ? u : (pair ? u + 1 : -1);
       if (mine >= 0) {
         const int myit = itu + gi, slot = myit % kWSlots, tile = mine - chg * L.nrt;
-        if (!mbar_wait(&full[slot], (myit / kWSlots) & 1)) {
+        if (!wait_use(myit)) {
           aborted = true;
           set_error(a.err, kErrTimeout);
           break;
@@ -1345,7 +1368,7 @@ __global__ void __launch_bounds__(kDense ? kThreadsP : fused::kThreads, 1)
       const int mine = gi == 0 ? u : (pair ? u + 1 : -1);
       if (mine >= 0) {
         const int myit = itu + gi, slot = myit % kWSlots, tile = mine - chg * L.nrt_dn;
-        if (!mbar_wait(&full[slot], (myit / kWSlots) & 1)) {
+        if (!wait_use(myit)) {
           aborted = true;
           set_error(a.err, kErrTimeout);
           break;
