@@ -49,6 +49,9 @@ TRAFFIC = {
 
 # steps of each workload when it is timed as a sub-record of the default line
 SUB_STEPS = {"layer1": 64, "batch64": 32, "prefill128": 32, "prefill30": 8}
+# the tied 4-bit head (vocabulary 262,144 x hidden 2816, group-64 affine) on one
+# decoded token: greedy token only, softcap 30
+HEAD_V, HEAD_STEPS, HEAD_SOFTCAP = 262144, 32, 30.0
 
 
 def layer_bytes(n_tokens: int, distinct_routed: int) -> int:
@@ -409,11 +412,49 @@ def run_ours(args, spec, rank, world, device):
                            "achieved_gbs": round(o["achieved"], 1), "frac": round(o["frac"], 4),
                            "traffic": otraffic,
                            "gpu_launches": r["launches_per_call"] * r["calls_per_step"] * steps}
+        subs["head"] = time_head(moe, device, hbm, world)
         line["workloads"] = subs
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
     moe.close()
     return line
+
+
+def time_head(moe, device, hbm, world):
+    """The tied head, one token per call (greedy token), CUDA events over
+    HEAD_STEPS calls on one stream after 3 warm-up calls; its 415 MB of codes,
+    scales and biases stream from HBM on every call (larger than L2)."""
+    import torch
+    import bit_affine_quantized_gb300 as bq
+    from synth import gen
+    from synth.device import DeviceHead
+
+    head = DeviceHead(11, HEAD_V, H, device=device)
+    hw = bq.make_head_weights(head.vocab, head.hidden, *head.addresses())
+    x = torch.from_numpy(gen.hidden_states(2026, 0, 1, H, True).view(np.int16)).to(device)
+    tok = torch.empty(1, dtype=torch.int32, device=device)
+    st = torch.cuda.Stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            moe.head_forward(x, 1, hw, HEAD_SOFTCAP, tokens=tok, stream=st)
+        torch.cuda.synchronize(device)
+        e0.record(st)
+        for _ in range(HEAD_STEPS):
+            moe.head_forward(x, 1, hw, HEAD_SOFTCAP, tokens=tok, stream=st)
+        e1.record(st)
+    torch.cuda.synchronize(device)
+    assert moe.get_error() == 0, "head call reported an error"
+    call_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device) / HEAD_STEPS
+    nbytes = HEAD_V * H // 2 + HEAD_V * (H // 64) * 4 + H * 2 + 4  # codes, bf16 scales + biases, x, token
+    achieved = nbytes / call_s / 1e9
+    del head
+    return {"workload": "tied 4-bit head, vocabulary %d x hidden %d, one token per call, greedy token, softcap %g"
+                        % (HEAD_V, H, HEAD_SOFTCAP),
+            "value": round(world / call_s, 3), "unit": "tok/s", "steps": HEAD_STEPS, "warmup": 3,
+            "kernel": "head_kernel", "launch_us": round(call_s * 1e6, 3), "algorithmic_bytes_per_launch": nbytes,
+            "achieved_gbs": round(achieved, 1), "frac": round(achieved / hbm, 4), "traffic": None,
+            "gpu_launches": HEAD_STEPS}
 
 
 # ---------------------------------------------------------------- oracle arm
