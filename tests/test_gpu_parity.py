@@ -200,6 +200,31 @@ def test_deterministic(moe, layer0_zipf, n_tokens):
     assert np.array_equal(a["logits"].view(np.uint32), b["logits"].view(np.uint32))
 
 
+@pytest.mark.parametrize("n_tokens", [37, 100])
+def test_repeated_calls_bit_identical(moe, layer0, n_tokens):
+    """Sixteen residual calls of the multi-token kernel on the same input all
+    bit-identical (fixed-order reductions): a ring or buffer race in the
+    kernel (a consumer group reading a slot before its copy landed, a buffer
+    released while still read) shows up here as a call that differs."""
+    w = weights_of(layer0)
+    x_bits = hidden(2024, 0, n_tokens, rms=False)
+    ws = workspace(moe, w, n_tokens)
+    first = None
+    for rep in range(16):
+        h = to_dev_bf16(x_bits)
+        y = torch.empty_like(h)
+        ids = torch.empty((n_tokens, K), dtype=torch.int32, device="cuda")
+        moe.layer_forward_residual(h, n_tokens, w, ws, y_out=y, ids_out=ids)
+        torch.cuda.synchronize()
+        assert moe.get_error() == bq.MOE_OK
+        out = (from_dev_bf16(y), from_dev_bf16(h), ids.cpu().numpy())
+        if first is None:
+            first = out
+            continue
+        for got, want, what in zip(out, first, ("y", "residual stream", "ids")):
+            assert np.array_equal(got, want), f"call {rep}: {what} differs from the first call"
+
+
 @pytest.mark.parametrize("hidden_dim,inter,n_experts,k,n_tokens", [
     (128, 64, 8, 2, 1), (128, 64, 8, 2, 33), (256, 128, 4, 4, 5), (192, 128, 16, 8, 17), (64, 64, 1, 1, 3),
 ])
