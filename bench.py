@@ -52,6 +52,10 @@ SUB_STEPS = {"layer1": 64, "batch64": 32, "prefill128": 32, "prefill30": 8}
 # the tied 4-bit head (vocabulary 262,144 x hidden 2816, group-64 affine) on one
 # decoded token: greedy token only, softcap 30
 HEAD_V, HEAD_STEPS, HEAD_SOFTCAP = 262144, 32, 30.0
+# expert offload: a 4-layer decode stack (Zipf-skewed routing, the pages'
+# premise) with each layer's routed experts in pinned host memory behind 16
+# device slots per layer
+OFFLOAD_LAYERS, OFFLOAD_SLOTS, OFFLOAD_WARM, OFFLOAD_STEPS = 4, 16, 16, 48
 
 
 def layer_bytes(n_tokens: int, distinct_routed: int) -> int:
@@ -413,6 +417,7 @@ def run_ours(args, spec, rank, world, device):
                            "traffic": otraffic,
                            "gpu_launches": r["launches_per_call"] * r["calls_per_step"] * steps}
         subs["head"] = time_head(moe, device, hbm, world)
+        subs["offload"] = time_offload(moe, device, world)
         line["workloads"] = subs
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
@@ -455,6 +460,71 @@ def time_head(moe, device, hbm, world):
             "kernel": "head_kernel", "launch_us": round(call_s * 1e6, 3), "algorithmic_bytes_per_launch": nbytes,
             "achieved_gbs": round(achieved, 1), "frac": round(achieved / hbm, 4), "traffic": None,
             "gpu_launches": HEAD_STEPS}
+
+
+def time_offload(moe, device, world):
+    """Decode through OFFLOAD_LAYERS layers with moe_layer_forward_offload:
+    the router on the device, the ids to the host, the LFU slot cache, one
+    host-to-device copy per missing expert, the block on the slots.  Each call
+    waits on the stream (the CPU handoff), so the time is host wall clock over
+    OFFLOAD_STEPS steps after OFFLOAD_WARM warm-up steps that fill the caches."""
+    import torch
+    import bit_affine_quantized_gb300 as bq
+    from synth import gen
+    from synth.device import DeviceLayer
+
+    dims = bq.make_dims(H, I, E, K)
+    layers, hosts, ws_off, slots = [], [], [], []
+    for l in range(OFFLOAD_LAYERS):
+        L = DeviceLayer(100 + l, H, I, E, device=device, zipf=True)
+        n = E * L.stride
+        host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        host.copy_(L.buf[L.experts_off:L.experts_off + n])
+        addr = dict(L.addresses())
+        addr["experts"] = host.data_ptr()
+        layers.append(L)
+        hosts.append(host)
+        ws_off.append(bq.layer_weights_from(dims, addr))
+        slots.append(torch.empty(OFFLOAD_SLOTS * L.stride, dtype=torch.uint8, device=device))
+    stride = layers[0].stride
+    blob = ws_off[0].layout.down_b + (H * (I // 64) * 2)  # extent of one blob's sub-tensors
+    cache = bq.ExpertCache(OFFLOAD_LAYERS, OFFLOAD_SLOTS)
+    ws = torch.empty(moe.workspace_bytes(dims, 1), dtype=torch.uint8, device=device)
+    h = torch.empty((1, H), dtype=torch.int16, device=device)
+    st = torch.cuda.Stream(device)
+    inputs = [torch.from_numpy(gen.hidden_states(3000, s, 1, H, False).view(np.int16)).to(device)
+              for s in range(OFFLOAD_WARM + OFFLOAD_STEPS)]
+
+    def step(s):
+        with torch.cuda.stream(st):
+            h.copy_(inputs[s])
+            for l in range(OFFLOAD_LAYERS):
+                moe.layer_forward_offload(h, cache, l, ws_off[l], slots[l], ws, stream=st)
+        torch.cuda.synchronize(device)
+
+    for s in range(OFFLOAD_WARM):
+        step(s)
+    before = [cache.stats(l) for l in range(OFFLOAD_LAYERS)]
+    t0 = time.perf_counter()
+    for s in range(OFFLOAD_WARM, OFFLOAD_WARM + OFFLOAD_STEPS):
+        step(s)
+    elapsed = max_over_ranks(time.perf_counter() - t0, world, device)
+    assert moe.get_error() == 0, "offload call reported an error"
+    after = [cache.stats(l) for l in range(OFFLOAD_LAYERS)]
+    hits = sum(a[0] - b[0] for a, b in zip(after, before))
+    misses = sum(a[1] - b[1] for a, b in zip(after, before))
+    cache.close()
+    per_layer_us = elapsed / (OFFLOAD_STEPS * OFFLOAD_LAYERS) * 1e6
+    h2d = misses * blob / OFFLOAD_STEPS
+    del layers, hosts, slots
+    return {"workload": "decode, %d-layer MoE stack with routed experts in pinned host memory, %d device slots per "
+                        "layer, least-frequently-used eviction (recency breaks ties), Zipf(1.1) logit offsets"
+                        % (OFFLOAD_LAYERS, OFFLOAD_SLOTS),
+            "value": round(world * OFFLOAD_STEPS / elapsed, 3), "unit": "tok/s", "steps": OFFLOAD_STEPS,
+            "warmup": OFFLOAD_WARM, "timing": "host wall clock (each call waits on the stream for the ids)",
+            "layers": OFFLOAD_LAYERS, "layer_us": round(per_layer_us, 2),
+            "hit_rate": round(hits / max(1, hits + misses), 4), "expert_loads_per_step": round(misses / OFFLOAD_STEPS, 2),
+            "h2d_bytes_per_step": round(h2d), "gpu_launches": None}
 
 
 # ---------------------------------------------------------------- oracle arm

@@ -16,7 +16,7 @@ __all__ = [
     "MoeError", "Dims", "QMat", "BlobLayout", "LayerWeights", "Moe", "load_library", "header_symbols",
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_CUDA", "MOE_ERR_BAD_EXPERT_ID",
     "MOE_ERR_TIMEOUT", "MOE_ERR_NONFINITE", "MOE_ERR_WORKSPACE", "build_library", "static_get_error",
-    "layer_forward_static",
+    "layer_forward_static", "ExpertCache",
 ]
 
 MOE_OK = 0
@@ -97,6 +97,13 @@ def load_library(path: str = LIB_PATH):
         "moe_head_forward": (I, [V, V, I, P(HeadWeights), ctypes.c_float, V, V, V]),
         "moe_embed": (I, [V, V, I, P(HeadWeights), V, V]),
         "moe_dense_forward": (I, [V, V, I, P(HeadWeights), V, V, V]),
+        "moe_cache_create": (I, [I, I, P(V)]),
+        "moe_cache_destroy": (None, [V]),
+        "moe_cache_lookup": (I, [V, I, V, I, V, V, V, P(I)]),
+        "moe_cache_stats": (I, [V, I, P(ctypes.c_longlong), P(ctypes.c_longlong)]),
+        "moe_cache_slot_expert": (I, [V, I, I]),
+        "moe_cache_slots": (I, [V]),
+        "moe_layer_forward_offload": (I, [V, V, I, V, P(LayerWeights), V, V, Z, V]),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
@@ -183,6 +190,53 @@ def static_get_error() -> int:
     return st.value
 
 
+class ExpertCache:
+    """Host-side slot policy of the expert offload (moe_cache_*): n_layers
+    layers of n_slots slots, least frequently used eviction, recency breaking
+    ties."""
+
+    def __init__(self, n_layers: int, n_slots: int = 16):
+        self.lib = load_library()
+        self.c = ctypes.c_void_p()
+        st = self.lib.moe_cache_create(n_layers, n_slots, ctypes.byref(self.c))
+        if st:
+            raise MoeError(st, "moe_cache_create")
+        self.n_layers, self.n_slots = n_layers, n_slots
+
+    def lookup(self, layer: int, ids):
+        """One step for a sequence of selected expert ids: (slots, [(slot,
+        expert) loads])."""
+        n = len(ids)
+        a = (ctypes.c_int32 * n)(*ids)
+        sl, ls, li = (ctypes.c_int32 * n)(), (ctypes.c_int32 * n)(), (ctypes.c_int32 * n)()
+        nl = ctypes.c_int()
+        st = self.lib.moe_cache_lookup(self.c, layer, a, n, sl, ls, li, ctypes.byref(nl))
+        if st:
+            raise MoeError(st, "moe_cache_lookup")
+        return list(sl), [(ls[i], li[i]) for i in range(nl.value)]
+
+    def stats(self, layer: int):
+        h, m = ctypes.c_longlong(), ctypes.c_longlong()
+        st = self.lib.moe_cache_stats(self.c, layer, ctypes.byref(h), ctypes.byref(m))
+        if st:
+            raise MoeError(st, "moe_cache_stats")
+        return h.value, m.value
+
+    def slot_expert(self, layer: int, slot: int) -> int:
+        return self.lib.moe_cache_slot_expert(self.c, layer, slot)
+
+    def close(self):
+        if self.c:
+            self.lib.moe_cache_destroy(self.c)
+            self.c = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class Moe:
     """One library handle (device error word + router counter) on the current device."""
 
@@ -250,6 +304,15 @@ class Moe:
         self._check(self.lib.moe_layer_forward_stack(self.h, _ptr(hidden), len(layers), arr, _ptr(ws),
                                                      ws.numel() * ws.element_size(), _stream(stream)),
                     "moe_layer_forward_stack")
+
+    def layer_forward_offload(self, hidden, cache: "ExpertCache", layer: int, w: LayerWeights, slots, ws,
+                              stream=None):
+        """One single-token residual layer with its routed experts in host
+        memory (w.experts: pinned host memory), filling the layer's device
+        `slots` through `cache` (moe_layer_forward_offload)."""
+        self._check(self.lib.moe_layer_forward_offload(self.h, cache.c, layer, _ptr(hidden), ctypes.byref(w),
+                                                       _ptr(slots), _ptr(ws), ws.numel() * ws.element_size(),
+                                                       _stream(stream)), "moe_layer_forward_offload")
 
     def head_forward(self, x, n_tokens, hw: HeadWeights, softcap: float = 30.0, logits=None, tokens=None,
                      stream=None):

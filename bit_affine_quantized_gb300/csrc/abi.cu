@@ -546,6 +546,59 @@ int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe
   return MOE_OK;
 }
 
+int moe_layer_forward_offload(moe_handle *h, moe_expert_cache *c, int layer, void *hidden,
+                              const moe_layer_weights *w, void *slots, void *ws, size_t ws_bytes,
+                              moe_stream_t stream) {
+  if (!h || !c || !hidden || !w || !slots || !ws) return MOE_ERR_INVALID_ARG;
+  int st = check_weights_impl(w);
+  if (st) return st;
+  if (w->post_norm || w->layer_scalar) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(hidden, 16) || !aligned(slots, 256)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(w->dims, 1, ws, ws_bytes))) return st;
+  if (moe_cache_slot_expert(c, layer, 0) < -1) return MOE_ERR_INVALID_ARG;  // no such layer in the cache
+  const int k = w->dims.top_k;
+  if (k > moe::kMaxTopK || moe_cache_slots(c) < k || moe_cache_slots(c) > w->dims.n_experts) return MOE_ERR_UNSUPPORTED;
+  uint8_t *wsb = (uint8_t *)ws;
+  const WsLayout L = ws_layout(w->dims, 1);
+  const cudaStream_t s = (cudaStream_t)stream;
+  // cb1: rmsnorm + router + top-k (ids and weights into the workspace)
+  if ((st = run_router(h, w, 1, nullptr, hidden, nullptr, nullptr, nullptr, nullptr, wsb, s, true))) return st;
+  // the handoff: the ids to the host
+  int32_t ids[moe::kMaxTopK], sl[moe::kMaxTopK], load_slots[moe::kMaxTopK], load_ids[moe::kMaxTopK];
+  if (cudaMemcpyAsync(ids, wsb + L.ids, k * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int n_loads = 0;
+  if ((st = moe_cache_lookup(c, layer, ids, k, sl, load_slots, load_ids, &n_loads))) return st;
+  // io: one copy per missing expert into its slot
+  const size_t blob = blob_extent(*w);
+  for (int i = 0; i < n_loads; ++i) {
+    if (load_ids[i] >= w->dims.n_experts) return MOE_ERR_BAD_EXPERT_ID;
+    if (cudaMemcpyAsync((uint8_t *)slots + (size_t)load_slots[i] * w->expert_stride,
+                        (const uint8_t *)w->experts + (size_t)load_ids[i] * w->expert_stride, blob,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  // cb2: the ids relabelled by slot (the copy reads host memory that stays
+  // valid: cudaMemcpyAsync from pageable memory returns once the data is staged)
+  if (cudaMemcpyAsync(wsb + L.ids, sl, k * sizeof(int32_t), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_layer_weights wl = *w;
+  wl.experts = slots;  // expert id = slot index from here on
+  moe::Routing r = routing_in(wsb, L);
+  moe::SortArgs sa;
+  sa.ids = r.ids;
+  sa.T = 1;
+  sa.k = k;
+  sa.E = w->dims.n_experts;
+  sa.r = r;
+  sa.include_shared = 1;
+  sa.err = h->dwords;
+  sa.trace = take_trace(h, 1);
+  if (moe::launch_sort(sa, s, h->pdl) != cudaSuccess) return MOE_ERR_CUDA;
+  return run_ffn(h, &wl, 1, wsb + L.xn, r, 1, nullptr, hidden, wsb, s);
+}
+
 int moe_head_forward(moe_handle *h, const void *x, int n_tokens, const moe_head_weights *w, float softcap,
                      float *logits, int32_t *tokens, moe_stream_t stream) {
   if (!h || !x || (!logits && !tokens)) return MOE_ERR_INVALID_ARG;

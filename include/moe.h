@@ -231,6 +231,57 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
 int moe_layer_forward_stack(moe_handle *h, void *hidden, int n_layers, const moe_layer_weights *layers,
                             void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---- Expert offload (sections "Resource split", "Load and ownership" and
+ * "Decode": every opened layer owns 16 routed-expert slots; after the router
+ * (cb1) the host looks the selected experts up in the layer's cache, fills
+ * only the missing slots (io), then the routed branch runs on the slots
+ * (cb2); eviction is least frequently used, recency breaking ties).  Here
+ * the routed experts stay in pinned host memory and the slots are device
+ * memory, filled over the host link.
+ *
+ * moe_expert_cache is the host-side policy state of n_layers layers of
+ * n_slots slots each (n_slots <= MOE_CACHE_MAX_SLOTS); it owns no device
+ * memory.  Readings of the policy: an expert's use count starts at 1 when it
+ * enters a slot and grows by 1 at each step that selects it; recency is the
+ * step of its last selection; empty slots are taken first (lowest index);
+ * a step's own experts are never evicted by its misses; remaining ties go to
+ * the lower slot. */
+#define MOE_CACHE_MAX_SLOTS 64
+typedef struct moe_expert_cache moe_expert_cache;
+int moe_cache_create(int n_layers, int n_slots, moe_expert_cache **out);
+void moe_cache_destroy(moe_expert_cache *c);
+/* One step of the policy for `n` selected experts `ids` (host int32) of
+ * `layer`: slots[j] (host int32 [n]) = the slot holding ids[j] afterwards;
+ * load_slots / load_ids (nullable host int32 [n]) = the slots to fill and
+ * their experts, *n_loads of them.  MOE_ERR_UNSUPPORTED if the step has more
+ * distinct experts than slots, MOE_ERR_BAD_EXPERT_ID for a negative id. */
+int moe_cache_lookup(moe_expert_cache *c, int layer, const int32_t *ids, int n, int32_t *slots,
+                     int32_t *load_slots, int32_t *load_ids, int *n_loads);
+/* Hits and misses of a layer so far (a hit: a selected expert already in a slot). */
+int moe_cache_stats(const moe_expert_cache *c, int layer, long long *hits, long long *misses);
+/* The expert in a slot (-1: empty; -2: bad arguments). */
+int moe_cache_slot_expert(const moe_expert_cache *c, int layer, int slot);
+int moe_cache_slots(const moe_expert_cache *c);
+
+/* One single-token layer of a residual stack with its routed experts in host
+ * memory: the router on the device (rmsnorm of hidden, logits, top-k), the
+ * ids copied to the host (one stream synchronisation: the CPU handoff of the
+ * pages), moe_cache_lookup, one host-to-device copy per missing expert into
+ * its slot, then the block (shared expert + the routed experts on their
+ * slots) with hidden <- bf16(hidden + y) in place.  Results equal those of
+ * moe_layer_forward_residual on resident experts with the chained launches
+ * (the same kernels, the experts relabelled by slot).
+ *   w        the layer: router and shared expert in device memory; w->experts
+ *            pinned host memory of the E expert blobs (w->expert_stride apart)
+ *   slots    device memory of this layer's slots: moe_cache_slots(c) blobs at
+ *            w->expert_stride bytes each, 256-byte aligned, owned by the caller
+ *   ws       workspace of moe_workspace_bytes(dims, 1)
+ * No layer tail (MOE_ERR_UNSUPPORTED); not capturable in a CUDA graph (it
+ * waits on the stream). */
+int moe_layer_forward_offload(moe_handle *h, moe_expert_cache *c, int layer, void *hidden,
+                              const moe_layer_weights *w, void *slots, void *ws, size_t ws_bytes,
+                              moe_stream_t stream);
+
 /* Single-token layer call that allocates nothing (the pages have no
  * counterpart: it exists for hosts that cannot allocate device memory,
  * e.g. a program whose own pool owns the whole device, or a per-token loop
