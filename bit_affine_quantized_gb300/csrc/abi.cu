@@ -27,6 +27,12 @@ struct moe_handle {
   // failure-detection hook, consumed by the next fused single-token launch
   int skip_block_next;                  // -1: none
   unsigned long long wait_ns_next;      // 0: the default limit
+  // expert offload: streams that fill missing slots in parallel (created on
+  // the first offload call), an event per stream the layer's stream waits on
+  static constexpr int kCopyStreams = 4;
+  cudaStream_t copy_st[kCopyStreams];
+  cudaEvent_t copy_ev[kCopyStreams];
+  bool copy_ready;
 };
 
 namespace {
@@ -396,6 +402,11 @@ int moe_create(moe_handle **out) {
 
 int moe_destroy(moe_handle *h) {
   if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->copy_ready)
+    for (int i = 0; i < moe_handle::kCopyStreams; ++i) {
+      cudaStreamDestroy(h->copy_st[i]);
+      cudaEventDestroy(h->copy_ev[i]);
+    }
   const cudaError_t e = cudaFree(h->dwords);
   free(h);
   return cuda_status(e);
@@ -570,14 +581,46 @@ int moe_layer_forward_offload(moe_handle *h, moe_expert_cache *c, int layer, voi
     return MOE_ERR_CUDA;
   int n_loads = 0;
   if ((st = moe_cache_lookup(c, layer, ids, k, sl, load_slots, load_ids, &n_loads))) return st;
-  // io: one copy per missing expert into its slot
+  // io: one copy per missing expert into its slot, spread over the copy
+  // streams so distinct misses move in parallel ("no two reads write the
+  // same slot": each slot appears once per step).  The layer's stream is idle
+  // here (synchronised above), so no earlier work still reads these slots.
+  if (!h->copy_ready) {
+    for (int i = 0; i < moe_handle::kCopyStreams; ++i)
+      if (cudaStreamCreateWithFlags(&h->copy_st[i], cudaStreamNonBlocking) != cudaSuccess ||
+          cudaEventCreateWithFlags(&h->copy_ev[i], cudaEventDisableTiming) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    h->copy_ready = true;
+  }
   const size_t blob = blob_extent(*w);
-  for (int i = 0; i < n_loads; ++i) {
+  for (int i = 0; i < n_loads; ++i)
     if (load_ids[i] >= w->dims.n_experts) return MOE_ERR_BAD_EXPERT_ID;
-    if (cudaMemcpyAsync((uint8_t *)slots + (size_t)load_slots[i] * w->expert_stride,
-                        (const uint8_t *)w->experts + (size_t)load_ids[i] * w->expert_stride, blob,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return MOE_ERR_CUDA;
+  // Host memory the device can read (pinned and mapped): the GPU copies the
+  // blobs itself (one launch, every blob in parallel); otherwise the copy
+  // engines do, one copy per blob over the copy streams.
+  cudaPointerAttributes pa;
+  const bool mapped = (blob % 16) == 0 && cudaPointerGetAttributes(&pa, w->experts) == cudaSuccess &&
+                      pa.type == cudaMemoryTypeHost && pa.devicePointer != nullptr &&
+                      ((uintptr_t)pa.devicePointer % 16) == 0 && (w->expert_stride % 16) == 0;
+  if (n_loads > 0 && mapped) {
+    moe::FillArgs fa;
+    fa.n = n_loads;
+    fa.bytes = blob;
+    for (int i = 0; i < n_loads; ++i) {
+      fa.src[i] = (const uint8_t *)pa.devicePointer + (size_t)load_ids[i] * w->expert_stride;
+      fa.dst[i] = (uint8_t *)slots + (size_t)load_slots[i] * w->expert_stride;
+    }
+    if (moe::launch_fill_slots(fa, s) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    for (int i = 0; i < n_loads; ++i)
+      if (cudaMemcpyAsync((uint8_t *)slots + (size_t)load_slots[i] * w->expert_stride,
+                          (const uint8_t *)w->experts + (size_t)load_ids[i] * w->expert_stride, blob,
+                          cudaMemcpyHostToDevice, h->copy_st[i % moe_handle::kCopyStreams]) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    for (int i = 0; i < n_loads && i < moe_handle::kCopyStreams; ++i)
+      if (cudaEventRecord(h->copy_ev[i], h->copy_st[i]) != cudaSuccess ||
+          cudaStreamWaitEvent(s, h->copy_ev[i], 0) != cudaSuccess)
+        return MOE_ERR_CUDA;
   }
   // cb2: the ids relabelled by slot (the copy reads host memory that stays
   // valid: cudaMemcpyAsync from pageable memory returns once the data is staged)

@@ -149,6 +149,16 @@ int decode_blocks_per_sm(const Dims &d);
 cudaError_t decode_set_attributes();
 cudaError_t launch_decode_fused(const DecodeArgs &a, int n_blocks, cudaStream_t st, bool pdl);
 
+// Expert offload: copy whole blobs from device-mapped host memory into slots.
+constexpr int kMaxFill = 16;
+struct FillArgs {
+  const void *src[kMaxFill];  // device-side addresses of the host blobs (16-byte aligned)
+  void *dst[kMaxFill];        // slots
+  size_t bytes;               // per blob, a multiple of 16
+  int n;
+};
+cudaError_t launch_fill_slots(const FillArgs &a, cudaStream_t st);
+
 // smem budgets (bytes) for a given shape; 0 = shape not supported by that kernel
 size_t router_smem(const Dims &d, int tb);
 size_t gateup_smem(const Dims &d, int tt);

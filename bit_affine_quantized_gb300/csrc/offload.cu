@@ -3,9 +3,10 @@
 // opened layer owns 16 expert slots; a hit reuses the slot, a miss takes an
 // evictable slot and reads the expert into it; eviction is least frequently
 // used with recency as the tie-breaker).  Here the experts live in host
-// memory and the slots in device memory; this file is the policy alone (host
-// code, no device work): which slot each selected expert occupies after a
-// step and which slots must be filled.
+// memory and the slots in device memory.  This file holds the policy (host
+// code: which slot each selected expert occupies after a step and which slots
+// must be filled) and the kernel that fills slots from device-mapped host
+// memory.
 //
 // Readings (the pages leave these open): an expert's use count starts at 1
 // when it enters a slot, grows by 1 at every step that selects it, and is
@@ -18,6 +19,7 @@
 #include <new>
 #include <vector>
 
+#include "kernels.h"
 #include "moe.h"
 
 struct moe_expert_cache {
@@ -136,3 +138,40 @@ extern "C" int moe_cache_slot_expert(const moe_expert_cache *c, int layer, int s
 }
 
 extern "C" int moe_cache_slots(const moe_expert_cache *c) { return c ? c->n_slots : 0; }
+
+// ------------------------------------------------------------ slot fills
+// The missing experts of a step copied into their slots by the GPU itself:
+// every block streams one share of one blob from host memory (device-mapped
+// pinned memory, read over the host link) into the slot.  GPU-initiated
+// reads keep many more requests in flight than the copy engines do.
+namespace moe {
+namespace {
+constexpr int kFillThreads = 256;
+constexpr int kFillBlocksPerBlob = 48;
+
+__global__ void __launch_bounds__(kFillThreads) fill_slots_kernel(const FillArgs a) {
+  const int i = blockIdx.x / kFillBlocksPerBlob, part = blockIdx.x - i * kFillBlocksPerBlob;
+  if (i >= a.n) return;
+  const uint4 *src = reinterpret_cast<const uint4 *>(a.src[i]);
+  uint4 *dst = reinterpret_cast<uint4 *>(a.dst[i]);
+  const size_t n16 = a.bytes / 16, per = (n16 + kFillBlocksPerBlob - 1) / kFillBlocksPerBlob;
+  const size_t b0 = (size_t)part * per, b1 = b0 + per < n16 ? b0 + per : n16;
+  // four 16-byte loads in flight per thread
+  size_t j = b0 + threadIdx.x;
+  for (; j + 3 * kFillThreads < b1; j += 4 * kFillThreads) {
+    const uint4 v0 = src[j], v1 = src[j + kFillThreads], v2 = src[j + 2 * kFillThreads], v3 = src[j + 3 * kFillThreads];
+    dst[j] = v0;
+    dst[j + kFillThreads] = v1;
+    dst[j + 2 * kFillThreads] = v2;
+    dst[j + 3 * kFillThreads] = v3;
+  }
+  for (; j < b1; j += kFillThreads) dst[j] = src[j];
+}
+}  // namespace
+
+cudaError_t launch_fill_slots(const FillArgs &a, cudaStream_t st) {
+  if (a.n < 1 || a.n > kMaxFill || a.bytes % 16) return cudaErrorInvalidValue;
+  fill_slots_kernel<<<a.n * kFillBlocksPerBlob, kFillThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+}  // namespace moe
