@@ -27,6 +27,7 @@ MOE_ERR_BAD_EXPERT_ID = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_NONFINITE = 6
 MOE_ERR_WORKSPACE = 7
+MOE_PROMPT_MAX_ROWS = 4096
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
 
@@ -104,6 +105,8 @@ def load_library(path: str = LIB_PATH):
         "moe_cache_slot_expert": (I, [V, I, I]),
         "moe_cache_slots": (I, [V]),
         "moe_layer_forward_offload": (I, [V, V, I, V, P(LayerWeights), V, V, Z, V]),
+        "moe_prompt_workspace_bytes": (Z, [P(Dims), I]),
+        "moe_layer_forward_prompt": (I, [V, V, I, P(LayerWeights), V, V, V, V, V, Z, V]),
     }
     for name, (res, args) in proto.items():
         fn = getattr(lib, name)
@@ -296,6 +299,20 @@ class Moe:
                                                         _ptr(x_out), _ptr(ids_out), _ptr(logits_out), _ptr(ws),
                                                         ws.numel() * ws.element_size(), _stream(stream)),
                     "moe_layer_forward_residual")
+
+    def prompt_workspace_bytes(self, dims: Dims, n_rows: int) -> int:
+        return int(self.lib.moe_prompt_workspace_bytes(ctypes.byref(dims), n_rows))
+
+    def layer_forward_prompt(self, hidden, n_rows, w: LayerWeights, ws, y_out=None, x_out=None, ids_out=None,
+                             logits_out=None, stream=None):
+        """One residual layer on a whole prompt of up to 4096 rows
+        (moe_layer_forward_prompt): the same function as
+        layer_forward_residual, row by row, with the expert work grouped over
+        all rows; ws of prompt_workspace_bytes(dims, n_rows) bytes."""
+        self._check(self.lib.moe_layer_forward_prompt(self.h, _ptr(hidden), n_rows, ctypes.byref(w), _ptr(y_out),
+                                                      _ptr(x_out), _ptr(ids_out), _ptr(logits_out), _ptr(ws),
+                                                      ws.numel() * ws.element_size(), _stream(stream)),
+                    "moe_layer_forward_prompt")
 
     def layer_forward_stack(self, hidden, layers, ws, stream=None):
         """Single-token layers of a residual stack in one call (hidden bf16 [H]

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "moe")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_gb300.so")
-SOURCES = ["abi.cu", "router.cu", "ffn.cu", "decode.cu", "prefill.cu", "noalloc.cu", "tail.cu", "head.cu", "offload.cu"]
+SOURCES = ["abi.cu", "router.cu", "ffn.cu", "decode.cu", "prefill.cu", "noalloc.cu", "tail.cu", "head.cu", "offload.cu", "prompt.cu"]
 HEADERS = ["common.cuh", "fused.cuh", "kernels.h", "abi_internal.h", "dense.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -123,6 +123,42 @@ WsLayout ws_layout(const moe_dims &d, int T) {
   return L;
 }
 
+// Workspace of the whole-prompt layer (T rows, T*k + T sorted positions).
+struct PromptWs {
+  size_t logits, ids, wts, counts, offsets, perm, pos, ch_e, ch_beg, ch_cnt, n_ch, xn, xg, hg, o, y, total;
+};
+
+PromptWs prompt_ws(const moe_dims &d, int T) {
+  const size_t H = d.hidden, I = d.inter, E = d.n_experts, k = d.top_k;
+  const size_t npos = (size_t)T * (k + 1);
+  const size_t nch = (size_t)moe::prompt_max_chunks(T, (int)k, (int)E);
+  PromptWs L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.logits = take((size_t)T * E * 4);
+  L.ids = take((size_t)T * k * 4);
+  L.wts = take((size_t)T * k * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take((size_t)T * k * 4);
+  L.pos = take((size_t)T * k * 4);
+  L.ch_e = take(nch * 4);
+  L.ch_beg = take(nch * 4);
+  L.ch_cnt = take(nch * 4);
+  L.n_ch = take(4);
+  L.xn = take((size_t)T * H * 2);
+  L.xg = take(npos * H * 2);
+  L.hg = take(npos * I * 2);
+  L.o = take(npos * H * 4);
+  L.y = take((size_t)T * H * 2);  // block output ahead of a layer tail
+  L.total = off;
+  return L;
+}
+
 moe::Routing routing_in(uint8_t *ws, const WsLayout &L) {
   moe::Routing r;
   r.ids = (int32_t *)(ws + L.ids);
@@ -367,7 +403,8 @@ int moe_create(moe_handle **out) {
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (prop.major != 10 || prop.minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
   if (moe::router_set_attributes() != cudaSuccess || moe::ffn_set_attributes() != cudaSuccess ||
-      moe::decode_set_attributes() != cudaSuccess || moe::prefill_set_attributes() != cudaSuccess)
+      moe::decode_set_attributes() != cudaSuccess || moe::prefill_set_attributes() != cudaSuccess ||
+      moe::prompt_set_attributes() != cudaSuccess)
     return MOE_ERR_CUDA;
   moe_handle *h = (moe_handle *)calloc(1, sizeof(moe_handle));
   if (!h) return MOE_ERR_CUDA;
@@ -537,6 +574,69 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens, const 
   ta.post_norm = (const uint16_t *)w->post_norm;
   ta.layer_scalar = w->layer_scalar;
   ta.T = n_tokens;
+  ta.H = w->dims.hidden;
+  ta.trace = take_trace(h, 1);
+  return cuda_status(moe::launch_tail(ta, s, h->pdl));
+}
+
+size_t moe_prompt_workspace_bytes(const moe_dims *dims, int n_rows) {
+  if (check_dims(dims) != MOE_OK || n_rows < 1 || n_rows > moe::kPromptMaxRows) return 0;
+  if (!moe::prompt_supported(to_dims(*dims, n_rows))) return 0;
+  return prompt_ws(*dims, n_rows).total;
+}
+
+int moe_layer_forward_prompt(moe_handle *h, void *hidden, int n_rows, const moe_layer_weights *w, void *y_out,
+                             void *x_out, int32_t *ids_out, float *logits_out, void *ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  if (!h || !hidden) return MOE_ERR_INVALID_ARG;
+  int st = check_weights_impl(w);
+  if (st) return st;
+  if (n_rows < 1 || n_rows > moe::kPromptMaxRows) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || (y_out && !aligned(y_out, 16)) || (x_out && !aligned(x_out, 16)) ||
+      (logits_out && !aligned(logits_out, 16)))
+    return MOE_ERR_INVALID_ARG;
+  const moe::Dims d = to_dims(w->dims, n_rows);
+  if (!moe::prompt_supported(d)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  const PromptWs L = prompt_ws(w->dims, n_rows);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  uint8_t *wsb = (uint8_t *)ws;
+  const cudaStream_t s = (cudaStream_t)stream;
+  // With a layer tail the combine writes y and the tail launch updates hidden.
+  const bool tail = w->post_norm != nullptr || w->layer_scalar != nullptr;
+  moe::PromptArgs a;
+  memset(&a, 0, sizeof(a));
+  a.w = layer_ptrs(*w);
+  a.d = d;
+  a.hres = (uint16_t *)hidden;
+  a.xn = (uint16_t *)(wsb + L.xn);
+  a.xn_user = (uint16_t *)x_out;
+  a.logits = logits_out ? logits_out : (float *)(wsb + L.logits);
+  a.ids_user = ids_out;
+  a.r.ids = (int32_t *)(wsb + L.ids);
+  a.r.wts = (float *)(wsb + L.wts);
+  a.r.counts = (int32_t *)(wsb + L.counts);
+  a.r.offsets = (int32_t *)(wsb + L.offsets);
+  a.r.perm = (int32_t *)(wsb + L.perm);
+  a.r.pos = (int32_t *)(wsb + L.pos);
+  a.ch_e = (int32_t *)(wsb + L.ch_e);
+  a.ch_beg = (int32_t *)(wsb + L.ch_beg);
+  a.ch_cnt = (int32_t *)(wsb + L.ch_cnt);
+  a.n_ch = (int32_t *)(wsb + L.n_ch);
+  a.xg = (__half *)(wsb + L.xg);
+  a.hg = (__half *)(wsb + L.hg);
+  a.obuf = (float *)(wsb + L.o);
+  a.err = h->dwords;
+  a.trace = take_trace(h, 6);
+  void *yb = tail && !y_out ? (void *)(wsb + L.y) : y_out;
+  st = cuda_status(moe::launch_prompt(a, (uint16_t *)yb, !tail, h->n_sm, s, h->pdl));
+  if (st || !tail) return st;
+  moe::TailArgs ta;
+  ta.y = (const uint16_t *)yb;
+  ta.h = (uint16_t *)hidden;
+  ta.post_norm = (const uint16_t *)w->post_norm;
+  ta.layer_scalar = w->layer_scalar;
+  ta.T = n_rows;
   ta.H = w->dims.hidden;
   ta.trace = take_trace(h, 1);
   return cuda_status(moe::launch_tail(ta, s, h->pdl));

@@ -673,7 +673,11 @@ cudaError_t launch_down(const FfnArgs &a, cudaStream_t st, bool pdl) {
   if (e != cudaSuccess) return e;
   FfnArgs c = a;
   if (c.trace) c.trace += 4;  // the combine launch traces into the next slot group
-  return launch_k(combine_kernel, dim3(a.d.T), dim3(256), 0, st, pdl, c);
+  return launch_combine(c, st, pdl);
+}
+
+cudaError_t launch_combine(const FfnArgs &a, cudaStream_t st, bool pdl) {
+  return launch_k(combine_kernel, dim3(a.d.T), dim3(256), 0, st, pdl, a);
 }
 
 cudaError_t ffn_set_attributes() {

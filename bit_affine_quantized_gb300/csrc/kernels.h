@@ -159,6 +159,37 @@ struct FillArgs {
 };
 cudaError_t launch_fill_slots(const FillArgs &a, cudaStream_t st);
 
+// Whole-prompt layer (prompt.cu): up to kPromptMaxRows rows through one
+// layer; the expert work in chunks of at most kPromptChunk rows of one expert.
+constexpr int kPromptMaxRows = 4096;
+constexpr int kPromptChunk = 128;
+struct PromptArgs {
+  LayerPtrs w;
+  Dims d;                   // T = the prompt's rows
+  uint16_t *hres;           // bf16 [T, H] residual stream, updated in place
+  uint16_t *xn;             // bf16 [T, H] normalised rows
+  uint16_t *xn_user;        // nullable copy of xn
+  float *logits;            // fp32 [T, E] (user buffer or workspace)
+  int32_t *ids_user;        // nullable [T, k]
+  float *wts_user;          // nullable [T, k]
+  Routing r;                // ids, wts, counts, offsets, perm, pos
+  int32_t *ch_e;            // [prompt_max_chunks] expert of each chunk (kSharedSlot: shared)
+  int32_t *ch_beg;          // first sorted position of the chunk
+  int32_t *ch_cnt;          // rows of the chunk (1 .. kPromptChunk)
+  int32_t *n_ch;            // [1] chunks
+  __half *xg;               // fp16 [T*k + T, H] operand rows per sorted position
+  __half *hg;               // fp16 [T*k + T, I] h rows per sorted position (operand order)
+  float *obuf;              // fp32 [T*k + T, H] weighted expert outputs
+  unsigned *err;
+  unsigned long long *trace;  // nullable: 6 launches x 4 slots
+};
+int prompt_max_chunks(int T, int k, int E);
+bool prompt_supported(const Dims &d);
+cudaError_t prompt_set_attributes();
+// router, grouping, gather, gate/up GEMM, down GEMM, combine (6 launches);
+// the combine writes y (nullable) and, if add_residual, hres <- bf16(hres + y)
+cudaError_t launch_prompt(const PromptArgs &a, uint16_t *y, bool add_residual, int n_sm, cudaStream_t st, bool pdl);
+
 // smem budgets (bytes) for a given shape; 0 = shape not supported by that kernel
 size_t router_smem(const Dims &d, int tb);
 size_t gateup_smem(const Dims &d, int tt);
@@ -171,6 +202,8 @@ cudaError_t launch_router(const RouterArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_sort(const SortArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_gateup(const FfnArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_down(const FfnArgs &a, cudaStream_t st, bool pdl);
+// y[t] = sum of the token's weighted expert outputs (obuf) + the shared row; T blocks
+cudaError_t launch_combine(const FfnArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_wait_timeout(unsigned *err, unsigned long long limit_ns, cudaStream_t st);
 bool use_down_decode(const Dims &d);
 

@@ -1,0 +1,899 @@
+// Whole-prompt MoE layer, sm_103a: the rows of a prompt (up to 4096) through
+// one layer in six launches.
+//
+// Page "TurboFieldfare - System design", section "Prefill": execution is
+// layer-major; the router scores every row, the token/expert pairs are
+// grouped into bounded routed-MoE work, experts are streamed in tiles of at
+// most eight and the next tile is fetched while the current tile's work is
+// still queued, and the shared and routed branches are combined before the
+// layer tail.  Section "Metal execution": prefill projections dequantise one
+// bounded weight tile into FP16 on-chip memory and hand it to the matrix
+// units.
+//
+// Here the weights stay resident in HBM and the "cache" the tiles stream
+// through is the GPU's L2: every expert's weights are read once per layer for
+// all of the prompt's rows instead of once per 128-row chunk.
+//
+//   prompt_router_kernel  16 rows per block: rmsnorm, the 8-bit router on the
+//                         tensor cores (mma.m16n8k16, codes as exact fp16
+//                         integers, per-group affine correction in fp32),
+//                         top-k and softmax per row.
+//   prompt_sort_kernel    one block: stable counting sort of all pairs by
+//                         expert, then the bounded chunks (at most 128 rows
+//                         of one expert) in tile order: the shared expert,
+//                         then experts 0-7, 8-15, ...
+//   prompt_gather_kernel  the normalised rows at their sorted positions, in
+//                         the operand order of the dense dequantisation.
+//   prompt_gemm_kernel    persistent, one block per SM: units (chunk, 128
+//                         weight rows); per K group the producer warp loads
+//                         the chunk's operand rows and the 4-bit codes with
+//                         tensor TMA, 16 warps dequantise the codes into an
+//                         fp16 A tile, one thread issues tcgen05.mma (M = 128
+//                         weight rows, N = the chunk's rows) into tensor
+//                         memory; the epilogue applies GeGLU (gate/up) or the
+//                         routing weight (down).  Each block prefetches its
+//                         next unit's weights into L2 while the current unit
+//                         runs.
+//   combine_kernel        y[t] = sum of the token's weighted expert outputs
+//                         in selection order + the shared expert's, added to
+//                         the residual stream (ffn.cu).
+#include <cuda.h>
+#include <math.h>
+#include <string.h>
+
+#include "dense.cuh"
+#include "fused.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------------ router
+constexpr int kRtTok = 16;        // rows per router block (one m16 tile)
+constexpr int kRtThreads = 256;   // 8 warps, 16 experts (two n8 tiles) each
+constexpr int kRtGroups = 2;      // 64-wide K groups per code stage
+constexpr int kRtStages = 3;
+constexpr int kRtCodePitch = 64 * kRtGroups + 16;  // bytes per expert row of a stage: rows 4 banks apart
+
+struct RtLayout {
+  int xp, x, xs, sb, codes, total;
+};
+__host__ __device__ inline RtLayout rt_layout(int H, int E) {
+  const int G = H / kGroup;
+  RtLayout L;
+  L.xp = 2 * H + 16;  // fp16 row pitch: consecutive rows 4 banks apart
+  int o = 0;
+  L.x = o;
+  o += kRtTok * L.xp;
+  L.xs = o;
+  o += kRtTok * G * 4;
+  L.sb = o;
+  o = (o + 2 * E * G * 2 + 15) & ~15;
+  L.codes = o;
+  o += kRtStages * E * kRtCodePitch;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Two 8-bit codes (little-endian pair) as an exact fp16 pair: the byte goes
+// under the exponent of 1024, then 1024 is subtracted.
+__device__ __forceinline__ uint32_t codes8_f16x2(uint32_t pair) {
+  const uint32_t biased = __byte_perm(pair, 0x64646464u, 0x4140);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x64006400u));
+  return r;
+}
+
+__global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int H = a.d.H, E = a.d.E, T = a.d.T, k = a.d.k, G = H / kGroup;
+  const RtLayout L = rt_layout(H, E);
+  uint8_t *sx = smem + L.x;
+  float *sxs = reinterpret_cast<float *>(smem + L.xs);
+  uint16_t *ssb = reinterpret_cast<uint16_t *>(smem + L.sb);  // scales [E][G], then biases [E][G]
+  uint8_t *scodes = smem + L.codes;
+  float *slogit = reinterpret_cast<float *>(scodes);  // [kRtTok][E], after the K loop
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * kRtTok, tb = min(kRtTok, T - t0);
+  const int nst = (G + kRtGroups - 1) / kRtGroups;
+  if (blockIdx.x == 0 && tid == 0) trace_min(a.trace, kTrEntry);
+
+  // router weights never change: the first stages of codes and all scales
+  // and biases are requested before the dependency wait
+  auto load_stage = [&](int s) {
+    if (s < nst) {
+      const int g0 = s * kRtGroups, ng = min(kRtGroups, G - g0), per = 4 * ng;  // 16-byte pieces per row
+      uint8_t *dst = scodes + (s % kRtStages) * E * kRtCodePitch;
+      for (int i = tid; i < E * per; i += kRtThreads) {
+        const int e = i / per, j = i - e * per;
+        cp_async16(dst + e * kRtCodePitch + 16 * j, a.w.router_q + (size_t)e * H + 64 * g0 + 16 * j);
+      }
+    }
+    cp_async_commit();
+  };
+  for (int s = 0; s < kRtStages - 1; ++s) load_stage(s);
+  for (int i = tid; i < E * G; i += kRtThreads) {
+    ssb[i] = __ldg(a.w.router_s + i);
+    ssb[E * G + i] = __ldg(a.w.router_b + i);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && tid == 0) trace_min(a.trace, kTrWaited);
+
+  // rmsnorm of the block's rows (warp w: rows w, w + 8); normalised rows out
+  // (bf16), router operand rows (fp16, natural order) and their 64-group sums
+  const int nvec = H / 8;
+  for (int rl = warp; rl < kRtTok; rl += kRtThreads / 32) {
+    uint8_t *xrow = sx + rl * L.xp;
+    if (rl >= tb) {  // rows past the prompt: zero operand
+      for (int v = lane; v < nvec; v += 32) *reinterpret_cast<uint4 *>(xrow + 16 * v) = make_uint4(0u, 0u, 0u, 0u);
+      for (int g = lane; g < G; g += 32) sxs[rl * G + g] = 0.f;
+      continue;
+    }
+    const uint16_t *src = a.hres + (size_t)(t0 + rl) * H;
+    float ss = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(src) + v);
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv = 1.0f / sqrtf(ss / (float)H + 1e-6f);
+    const float isq = rsqrtf((float)H);
+    // lanes 8q .. 8q+7 hold the eight vectors of one 64-group (nvec is a multiple of 8)
+    for (int v0 = 0; v0 < nvec; v0 += 32) {
+      const int v = v0 + lane;
+      float gs = 0.f;
+      if (v < nvec) {
+        const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(src) + v);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+        uint32_t ob[4], oh[4];
+        uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+        if (a.w.router_scale) rv = __ldg(reinterpret_cast<const uint4 *>(a.w.router_scale) + v);
+        const uint32_t r4[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint16_t lb = float_to_bf16_bits(__uint_as_float(w4[q] << 16) * inv);
+          const uint16_t hb = float_to_bf16_bits(__uint_as_float(w4[q] & 0xFFFF0000u) * inv);
+          ob[q] = (uint32_t)lb | ((uint32_t)hb << 16);
+          __half2 hv;
+          if (a.w.router_scale)  // router input x * router_scale / sqrt(H), rounded once to fp16
+            hv = __floats2half2_rn(bf16_bits_to_float(lb) * (__uint_as_float(r4[q] << 16) * isq),
+                                   bf16_bits_to_float(hb) * (__uint_as_float(r4[q] & 0xFFFF0000u) * isq));
+          else
+            hv = __floats2half2_rn(bf16_bits_to_float(lb), bf16_bits_to_float(hb));
+          oh[q] = *reinterpret_cast<const uint32_t *>(&hv);
+          gs += __low2float(hv);
+          gs += __high2float(hv);
+        }
+        *reinterpret_cast<uint4 *>(a.xn + (size_t)(t0 + rl) * H + 8 * v) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        if (a.xn_user)
+          *reinterpret_cast<uint4 *>(a.xn_user + (size_t)(t0 + rl) * H + 8 * v) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        *reinterpret_cast<uint4 *>(xrow + 16 * v) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+      }
+      gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+      gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+      gs += __shfl_xor_sync(0xffffffffu, gs, 4);
+      if ((lane & 7) == 0 && v < nvec) sxs[rl * G + v / 8] = gs;
+    }
+  }
+
+  // logits: warp w owns experts 16w .. 16w+15 (two n8 tiles) for all 16 rows
+  const int r = lane >> 2, c = lane & 3;
+  const int n0 = 16 * warp;
+  float tot[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tot[nt][i] = 0.f;
+  for (int s = 0; s < nst; ++s) {
+    cp_async_wait<kRtStages - 2>();
+    __syncthreads();  // stage s landed for every thread; stage s - 1 fully consumed
+    load_stage(s + kRtStages - 1);
+    const uint8_t *cs = scodes + (s % kRtStages) * E * kRtCodePitch;
+    const int g0 = s * kRtGroups, ng = min(kRtGroups, G - g0);
+    if (n0 < E) {
+      for (int gl = 0; gl < ng; ++gl) {
+        const int g = g0 + gl;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const int kk = 64 * g + 16 * ks;
+          uint32_t A[4];
+          A[0] = *reinterpret_cast<const uint32_t *>(sx + r * L.xp + 2 * (kk + 2 * c));
+          A[1] = *reinterpret_cast<const uint32_t *>(sx + (r + 8) * L.xp + 2 * (kk + 2 * c));
+          A[2] = *reinterpret_cast<const uint32_t *>(sx + r * L.xp + 2 * (kk + 8 + 2 * c));
+          A[3] = *reinterpret_cast<const uint32_t *>(sx + (r + 8) * L.xp + 2 * (kk + 8 + 2 * c));
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            // experts past E (E not a multiple of 16) read expert E - 1: columns discarded below
+            const uint8_t *crow = cs + min(n0 + 8 * nt + r, E - 1) * kRtCodePitch + 64 * gl + 16 * ks + 2 * c;
+            const uint32_t b0 = codes8_f16x2(*reinterpret_cast<const uint16_t *>(crow));
+            const uint32_t b1 = codes8_f16x2(*reinterpret_cast<const uint16_t *>(crow + 8));
+            mma_f16(acc[nt], A, b0, b1);
+          }
+        }
+        const float x0 = sxs[r * G + g], x1 = sxs[(r + 8) * G + g];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e = n0 + 8 * nt + 2 * c + (i & 1);
+            const int ee = e < E ? e : E - 1;  // columns past E are discarded below
+            const float sc = bf16_bits_to_float(ssb[ee * G + g]), bi = bf16_bits_to_float(ssb[E * G + ee * G + g]);
+            tot[nt][i] = fmaf(bi, (i >> 1) ? x1 : x0, fmaf(sc, acc[nt][i], tot[nt][i]));
+          }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // the code stages become the logit table
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = n0 + 8 * nt + 2 * c + (i & 1), rl = r + 8 * (i >> 1);
+      if (e < E) {
+        const float v = tot[nt][i] + (a.w.logit_bias ? a.w.logit_bias[e] : 0.f);
+        slogit[rl * E + e] = v;
+        if (rl < tb) a.logits[(size_t)(t0 + rl) * E + e] = v;
+      }
+    }
+  __syncthreads();
+  for (int rl = warp; rl < tb; rl += kRtThreads / 32) {
+    const int t = t0 + rl;
+    bool bad = false;
+    fused::warp_topk(slogit + rl * E, E, k, a.r.ids + (size_t)t * k, a.r.wts + (size_t)t * k, a.w.expert_scale, &bad);
+    if (bad && lane == 0) set_error(a.err, kErrNonFinite);
+    __syncwarp();
+    if (lane < k) {
+      if (a.ids_user) a.ids_user[(size_t)t * k + lane] = a.r.ids[(size_t)t * k + lane];
+      if (a.wts_user) a.wts_user[(size_t)t * k + lane] = a.r.wts[(size_t)t * k + lane];
+    }
+  }
+  if (tid == 0) trace_max(a.trace, kTrExit);
+}
+
+// ------------------------------------------------------------------ grouping
+constexpr int kSortThreads = 1024;
+constexpr int kSortWarps = kSortThreads / 32;
+
+// Exclusive scan of v over the 32 lanes of one warp; returns the lane's
+// prefix and writes the total to *sum (every lane).
+__device__ __forceinline__ int warp_excl_scan(int v, int *sum) {
+  const int lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  *sum = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - v;
+}
+
+__global__ void __launch_bounds__(kSortThreads) prompt_sort_kernel(const PromptArgs a) {
+  __shared__ int s_hist[kSortWarps][kMaxExperts];  // pairs per (warp segment, expert), then segment bases
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_ch0[kMaxExperts + 1];           // first chunk of each expert
+  const int T = a.d.T, k = a.d.k, E = a.d.E, n = T * k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) trace_min(a.trace, kTrEntry);
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = tid; i < kSortWarps * kMaxExperts; i += kSortThreads) (&s_hist[0][0])[i] = 0;
+  __syncthreads();
+  // each warp owns one contiguous segment of the pairs, 32 at a time in order
+  const int seg = (n + kSortWarps - 1) / kSortWarps;
+  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+  bool bad = false;
+  for (int b = s0; b < s1; b += 32) {
+    const int p = b + lane;
+    const int e = p < s1 ? __ldcg(a.r.ids + p) : -1;
+    const bool ok = p < s1 && e >= 0 && e < E;
+    bad = bad || (p < s1 && !ok);
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : (1 << 30) + lane);
+    if (ok && (peers & lanemask_lt()) == 0) s_hist[warp][e] += __popc(peers);
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(a.err, kErrBadId);
+  __syncthreads();
+  // expert offsets (warp 0: four experts per lane)
+  if (warp == 0) {
+    int cnt[4], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * lane + i;
+      cnt[i] = 0;
+      if (e < E)
+        for (int w = 0; w < kSortWarps; ++w) cnt[i] += s_hist[w][e];
+      sum += cnt[i];
+    }
+    int total;
+    int base = warp_excl_scan(sum, &total);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * lane + i;
+      if (e < E) {
+        s_off[e] = base;
+        a.r.offsets[e] = base;
+        a.r.counts[e] = cnt[i];
+      }
+      base += cnt[i];
+    }
+    if (lane == 0) {
+      s_off[E] = total;
+      a.r.offsets[E] = total;
+    }
+  }
+  __syncthreads();
+  if (tid < E) {  // segment bases of expert tid, in segment order (stable)
+    int run = s_off[tid];
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int c = s_hist[w][tid];
+      s_hist[w][tid] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int b = s0; b < s1; b += 32) {
+    const int p = b + lane;
+    const int e = p < s1 ? __ldcg(a.r.ids + p) : -1;
+    const bool ok = p < s1 && e >= 0 && e < E;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : (1 << 30) + lane);
+    if (ok) {
+      const int q = s_hist[warp][e] + __popc(peers & lanemask_lt());
+      a.r.perm[q] = p;
+      a.r.pos[p] = q;
+    } else if (p < s1) {
+      a.r.pos[p] = -1;
+    }
+    __syncwarp();
+    if (ok && (peers & lanemask_lt()) == 0) s_hist[warp][e] += __popc(peers);
+    __syncwarp();
+  }
+  // bounded chunks: the shared expert's rows first, then every expert's
+  // sorted positions in runs of at most kPromptChunk, experts in ascending id
+  // (tiles of eight consecutive experts follow one another)
+  const int nsh = (T + kPromptChunk - 1) / kPromptChunk;
+  if (warp == 0) {
+    int nc[4], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * lane + i;
+      nc[i] = e < E ? (s_off[e + 1] - s_off[e] + kPromptChunk - 1) / kPromptChunk : 0;
+      sum += nc[i];
+    }
+    int total;
+    int base = nsh + warp_excl_scan(sum, &total);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * lane + i;
+      if (e < E) s_ch0[e] = base;
+      base += nc[i];
+    }
+    if (lane == 0) *a.n_ch = nsh + total;
+  }
+  __syncthreads();
+  for (int j = tid; j < nsh; j += kSortThreads) {
+    a.ch_e[j] = kSharedSlot;
+    a.ch_beg[j] = n + j * kPromptChunk;
+    a.ch_cnt[j] = min(kPromptChunk, T - j * kPromptChunk);
+  }
+  for (int e = warp; e < E; e += kSortWarps) {
+    const int beg = s_off[e], cnt = s_off[e + 1] - beg;
+    for (int j = lane; j * kPromptChunk < cnt; j += 32) {
+      a.ch_e[s_ch0[e] + j] = e;
+      a.ch_beg[s_ch0[e] + j] = beg + j * kPromptChunk;
+      a.ch_cnt[s_ch0[e] + j] = min(kPromptChunk, cnt - j * kPromptChunk);
+    }
+  }
+  if (tid == 0) trace_max(a.trace, kTrExit);
+}
+
+// ------------------------------------------------------------------ gather
+constexpr int kGatherThreads = 256;
+
+// One warp per sorted position: the normalised row of its token in the
+// operand order (fp16 pairs permuted within each 16-element quarter, odd
+// words divided by 16), the B operand of the dense gate/up units.
+__global__ void __launch_bounds__(kGatherThreads) prompt_gather_kernel(const PromptArgs a) {
+  const int T = a.d.T, k = a.d.k, H = a.d.H, E = a.d.E;
+  const int lane = threadIdx.x & 31;
+  const int pos = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5);
+  if (blockIdx.x == 0 && threadIdx.x == 0) trace_min(a.trace, kTrEntry);
+  pdl_wait();
+  pdl_launch_dependents();
+  const int n = T * k;
+  // positions of dropped pairs (bad ids) are never read: no row for them
+  int tok = -1;
+  if (pos >= n && pos < n + T)
+    tok = pos - n;
+  else if (pos < n && pos < __ldcg(a.r.offsets + E))
+    tok = __ldcg(a.r.perm + pos) / k;
+  const uint4 *src = reinterpret_cast<const uint4 *>(a.xn + (size_t)(tok < 0 ? 0 : tok) * H);
+  uint4 *dst = reinterpret_cast<uint4 *>(a.xg + (size_t)pos * H);
+  for (int q = lane; tok >= 0 && q < H / 16; q += 32) {
+    const uint4 v0 = __ldcg(src + 2 * q), v1 = __ldcg(src + 2 * q + 1);
+    const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t out[8];
+    operand_quarter<true>(in, out);
+    dst[2 * q] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[2 * q + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) trace_max(a.trace, kTrExit);
+}
+
+// ------------------------------------------------------------------ expert GEMM
+constexpr int kGemmCons = fused::kCons;                 // 16 dequantisation / epilogue warps
+constexpr int kGemmProd = kGemmCons;                    // producer warp
+constexpr int kGemmMma = kGemmCons + 1;                 // tcgen05 issue warp
+constexpr int kGemmThreads = (kGemmCons + 2) * 32;      // 576
+constexpr int kTileRows = dense::kRows;                 // 128 weight rows per unit
+constexpr int kMaxStages = 8;
+
+// Shared-memory plan of a GEMM block (offsets from a 1024-aligned base).
+struct GemmPlan {
+  int stages, bstage, cstage, abuf;
+  int b0, c0, a0, s, bar, total;
+};
+__host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
+  GemmPlan P;
+  P.stages = stages;
+  P.bstage = kTileRows * 128;                   // 128 operand rows x 64 fp16
+  P.cstage = (down ? 1 : 2) * kTileRows * 32;   // 128 rows x 64 codes per matrix
+  P.abuf = (down ? 1 : 2) * kTileRows * 128;    // dequantised A per matrix
+  int o = 0;
+  P.b0 = o;
+  o += stages * P.bstage;
+  P.c0 = o;
+  o += stages * P.cstage;
+  P.a0 = o;
+  o += 2 * P.abuf;
+  P.s = o;
+  o += (down ? 2 : 4) * kTileRows * G * 2;
+  o = (o + 15) & ~15;
+  P.bar = o;
+  o += 1024;  // barriers [0, 256), tensor-memory address at 256, column weights at 512
+  P.total = o + 1024;  // slack for the 1024-byte alignment of the base
+  return P;
+}
+__host__ inline int gemm_stages(int G, bool down) {
+  int s = down ? kMaxStages : 4;
+  while (s > 2 && gemm_plan(G, down, s).total > 227 * 1024) --s;
+  return s;
+}
+
+struct GemmParams {
+  dense::Maps m;  // 64-byte aligned: first
+  PromptArgs a;
+  int stages;
+};
+
+template <bool kDown>
+__global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __grid_constant__ GemmParams prm) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const PromptArgs &a = prm.a;
+  const int H = a.d.H, I = a.d.I, T = a.d.T, k = a.d.k;
+  const int K = kDown ? I : H, G = K / kGroup, M = kDown ? H : I;
+  const int ntile = (M + kTileRows - 1) / kTileRows;
+  constexpr int nm = kDown ? 1 : 2;  // matrices per unit
+  uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const GemmPlan P = gemm_plan(G, kDown, prm.stages);
+  const int S = P.stages;
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + P.bar);  // [S] TMA landed
+  uint64_t *empty = full + kMaxStages;                          // [S] MMAs done with a stage
+  uint64_t *adone = empty + kMaxStages;                         // [2] MMAs done with an A buffer
+  uint64_t *afull = adone + 2;                                  // [2] A buffer written (every warp)
+  uint64_t *sfull = afull + 2;                                  // scales of the unit landed
+  uint64_t *sempty = sfull + 1;                                 // scales consumed (every warp)
+  uint64_t *tfree = sempty + 1;                                 // epilogue done with tensor memory
+  uint64_t *tready = tfree + 1;                                 // tensor memory allocated
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(base + P.bar + 256);
+  float *s_w = reinterpret_cast<float *>(base + P.bar + 512);  // [128] routing weight per column
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool tracer = blockIdx.x == 0 && tid == 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&adone[0], 1);
+    mbar_init(&adone[1], 1);
+    mbar_init(&afull[0], kGemmCons);
+    mbar_init(&afull[1], kGemmCons);
+    mbar_init(sfull, 1);
+    mbar_init(sempty, kGemmCons);
+    mbar_init(tfree, 1);
+    mbar_init(tready, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tracer) trace_min(a.trace, kTrEntry);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tracer) trace_min(a.trace, kTrWaited);
+  const int nunits = __ldcg(a.n_ch) * ntile;
+
+  // ============================================================ producer warp
+  if (warp == kGemmProd) {
+    fused::fence_proxy_async_global();  // operand rows written by the previous launch are read by the TMA
+    bool ok = true;
+    int gi = 0, du = 0;  // K groups issued, units whose scales went out
+    const int nf = kDown ? 2 : 4;
+    auto field_off = [&](int f) -> size_t {
+      if (kDown) return f == 0 ? a.w.off.down_s : a.w.off.down_b;
+      return f == 0 ? a.w.off.gate_s : f == 1 ? a.w.off.gate_b : f == 2 ? a.w.off.up_s : a.w.off.up_b;
+    };
+    // the codes of one K group of a unit into L2 (no shared memory, no completion)
+    auto prefetch_group = [&](int e, int r0, int g) {
+      const int sh = e < 0 ? 1 : 0;
+      if (kDown) {
+        dense::tma_prefetch_3d(&prm.m.dq[sh], 32 * g, r0, sh ? 0 : e);
+      } else {
+        dense::tma_prefetch_3d(&prm.m.gq[sh], 32 * g, r0, sh ? 0 : e);
+        dense::tma_prefetch_3d(&prm.m.uq[sh], 32 * g, r0, sh ? 0 : e);
+      }
+    };
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const int ch = u / ntile, rt = u - ch * ntile;
+      const int e = __ldcg(a.ch_e + ch), beg = __ldcg(a.ch_beg + ch);
+      const int sh = e < 0 ? 1 : 0;
+      const uint8_t *blob = sh ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
+      const int r0 = rt * kTileRows, nrows = min(kTileRows, M - r0);
+      // the block's next unit (the next tile of the sweep): its first K
+      // groups and its scales into L2 while this unit runs
+      const int un = u + gridDim.x;
+      if (un < nunits && lane == 0) {
+        const int chn = un / ntile, rtn = un - chn * ntile, en = __ldcg(a.ch_e + chn);
+        const uint8_t *bn = en < 0 ? a.w.shared : a.w.experts + (size_t)en * a.w.stride;
+        const int r0n = rtn * kTileRows, nrn = min(kTileRows, M - r0n);
+        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(en, r0n, g);
+        for (int f = 0; f < nf; ++f) prefetch_l2(bn + field_off(f) + (size_t)r0n * G * 2, (uint32_t)(nrn * G * 2));
+      }
+      if (du >= 1) ok = __all_sync(0xffffffffu, mbar_wait_idle(sempty, (du - 1) & 1, 32));
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(sfull, (uint32_t)(nf * nrows * G * 2));
+      __syncwarp();
+      if (lane < nf)
+        bulk_g2s(base + P.s + lane * kTileRows * G * 2, blob + field_off(lane) + (size_t)r0 * G * 2,
+                 (uint32_t)(nrows * G * 2), sfull);
+      ++du;
+      if (lane == 0)  // this unit's first groups (later ones: kAhead ahead of their TMA below)
+        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(e, r0, g);
+      for (int g = 0; g < G && ok; ++g, ++gi) {
+        const int st = gi % S;
+        if (gi >= S) ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[st], ((gi / S) - 1) & 1, 32));
+        if (!ok) break;
+        if (lane == 0) {
+          if (g + dense::kAhead < G) prefetch_group(e, r0, g + dense::kAhead);
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(P.bstage + P.cstage));
+          dense::tma_load_2d(base + P.b0 + st * P.bstage, kDown ? &prm.m.h : &prm.m.x, 64 * g, beg, &full[st]);
+          uint8_t *cd = base + P.c0 + st * P.cstage;
+          if (kDown) {
+            dense::tma_load_3d(cd, &prm.m.dq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
+          } else {
+            dense::tma_load_3d(cd, &prm.m.gq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
+            dense::tma_load_3d(cd + kTileRows * 32, &prm.m.uq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // copies in flight land before the block's shared memory is released
+    if (lane == 0) {
+      if (!ok) set_error(a.err, kErrTimeout);
+      for (int j = gi - S > 0 ? gi - S : 0; j < gi; ++j) mbar_wait_idle(&full[j % S], (j / S) & 1);
+      if (du >= 1) mbar_wait_idle(sfull, (du - 1) & 1);
+    }
+    return;
+  }
+
+  // ============================================================ MMA warp
+  // Owns the tensor memory (gate in columns 0..127, up in 128..255; down
+  // uses the first 128) and issues each K group's tcgen05.mma once the
+  // consumers have written its A tile.
+  if (warp == kGemmMma) {
+    dense::tc_alloc(s_tmem, 256);
+    dense::tc_fence_before();
+    __syncwarp();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
+    if (lane == 0) mbar_arrive_expect_tx(tready, 0);
+    bool ok = true;
+    int gi = 0, du = 0;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+      const int ch = u / ntile;
+      const int N = (__ldcg(a.ch_cnt + ch) + 15) & ~15;  // MMA N: the chunk's rows, padded to 16
+      const uint32_t idesc = dense::idesc_f16(kTileRows, N);
+      if (du >= 1) ok = __all_sync(0xffffffffu, mbar_wait_idle(tfree, (du - 1) & 1, 32));  // accumulators read out
+      ++du;
+      dense::tc_fence_after();
+      for (int g = 0; g < G && ok; ++g, ++gi) {
+        const int st = gi % S, ab = gi & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (gi / S) & 1) && mbar_wait(&afull[ab], (gi >> 1) & 1));
+        if (!ok) break;
+        dense::tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = dense::sdesc(smem_addr(base + P.b0 + st * P.bstage) + ks * 32, 16, 1024, 2);
+#pragma unroll
+            for (int m = 0; m < nm; ++m) {
+              const uint64_t ad =
+                  dense::sdesc(smem_addr(base + P.a0 + ab * P.abuf + m * kTileRows * 128) + ks * 32, 16, 1024, 2);
+              dense::tc_mma(tmem + m * 128, ad, bd, idesc, (g > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          dense::tc_commit(&empty[st]);  // the TMA stage may be refilled
+          dense::tc_commit(&adone[ab]);  // the A buffer may be rewritten; after the last group: unit done
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) set_error(a.err, kErrTimeout);
+    // tensor memory back once the last MMAs completed and the last epilogue read them (bounded waits)
+    if (gi > 0) mbar_wait(&adone[(gi - 1) & 1], ((gi - 1) >> 1) & 1);
+    if (du > 0) mbar_wait_idle(tfree, (du - 1) & 1, 64);
+    dense::tc_fence_after();
+    __syncwarp();
+    dense::tc_dealloc(tmem, 256);
+    return;
+  }
+
+  // ============================================================ consumers
+  const uint16_t *sb = reinterpret_cast<const uint16_t *>(base + P.s);
+  const int npairs = T * k;
+  uint32_t tmem = 0;
+  bool have_tmem = false, okd = true;
+  int gi = 0, du = 0;
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+    const int ch = u / ntile, rt = u - ch * ntile;
+    const int beg = __ldcg(a.ch_beg + ch), cnt = __ldcg(a.ch_cnt + ch);
+    const int r0 = rt * kTileRows, nrows = min(kTileRows, M - r0);
+    const int N = (cnt + 15) & ~15;
+    if (kDown)
+      for (int n = tid; n < cnt; n += kGemmCons * 32)
+        s_w[n] = beg + n >= npairs ? 1.0f : __ldcg(a.r.wts + __ldcg(a.r.perm + beg + n));
+    fused::cons_sync();  // the column weights are in place before any warp's epilogue reads them
+    okd = okd && mbar_wait(sfull, du & 1);
+    ++du;
+    for (int g = 0; g < G; ++g, ++gi) {
+      const int st = gi % S, ab = gi & 1;
+      okd = okd && mbar_wait(&full[st], (gi / S) & 1);
+      if (gi >= 2) okd = okd && mbar_wait(&adone[ab], ((gi >> 1) - 1) & 1);
+      if (okd) {
+        const uint8_t *cb = base + P.c0 + st * P.cstage;
+        uint8_t *abuf = base + P.a0 + ab * P.abuf;
+        const int rr = tid & 127;
+        if (!kDown) {
+          const int m = tid >> 8, hh = (tid >> 7) & 1;  // matrix (gate, up), half of the group
+          const uint4 cw = *reinterpret_cast<const uint4 *>(cb + m * kTileRows * 32 + rr * 32 + hh * 16);
+          const float sf = bf16_bits_to_float(sb[(2 * m) * kTileRows * G + rr * G + g]);
+          const float bf = bf16_bits_to_float(sb[(2 * m + 1) * kTileRows * G + rr * G + g]);
+          const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
+          // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
+          uint8_t *row = abuf + m * kTileRows * 128 + rr * 128;
+          const int sw = rr & 7, j0 = 4 * hh;
+          *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
+          *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
+          *reinterpret_cast<uint4 *>(row + ((j0 + 2) ^ sw) * 16) = dense::dequant_word(cw.z, s2, b2, b16);
+          *reinterpret_cast<uint4 *>(row + ((j0 + 3) ^ sw) * 16) = dense::dequant_word(cw.w, s2, b2, b16);
+        } else {
+          const int qq = tid >> 7;  // quarter of the group
+          const uint2 cw = *reinterpret_cast<const uint2 *>(cb + rr * 32 + qq * 8);
+          const float sf = bf16_bits_to_float(sb[rr * G + g]);
+          const float bf = bf16_bits_to_float(sb[kTileRows * G + rr * G + g]);
+          const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
+          uint8_t *row = abuf + rr * 128;
+          const int sw = rr & 7, j0 = 2 * qq;
+          *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
+          *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
+        }
+      }
+      dense::fence_async_smem();  // the A tiles, written by threads, are read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&afull[ab], 0);  // this warp's part of the A tile is in place
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(sempty, 0);  // this warp is done with the unit's scales
+    okd = okd && mbar_wait(&adone[(gi - 1) & 1], ((gi - 1) >> 1) & 1);  // every MMA of the unit done
+    if (!have_tmem) {
+      okd = okd && mbar_wait(tready, 0);
+      tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
+      have_tmem = true;
+    }
+    okd = __all_sync(0xffffffffu, okd);  // tcgen05.ld below is warp-collective
+    dense::tc_fence_after();
+    // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (weight
+    // rows) and columns 32 (w / 4) .. +31 (the chunk's rows)
+    const int w4 = warp & 3, cbk = warp >> 2, rr = 32 * w4 + lane;
+    if (okd && 32 * cbk < N) {
+      const uint32_t ta = tmem + ((uint32_t)(32 * w4) << 16) + 32 * cbk;
+      for (int hf = 0; hf < 2; ++hf) {  // 16 columns at a time
+        if (!kDown) {
+          float gv[16], uv[16];
+          dense::tc_ld16(ta + 16 * hf, gv);
+          dense::tc_ld16(ta + 128 + 16 * hf, uv);
+          if (rr < nrows) {
+            const int i = r0 + rr;
+            bool odd = false;
+            const int slot = dense::operand_slot(i & 63, odd);
+            __half *dst = a.hg + (i & ~63) + slot;
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = 32 * cbk + 16 * hf + j;
+              if (n < cnt) {
+                const float hv = gelu_tanh(gv[j]) * uv[j];
+                bad = bad || !(fabsf(hv) <= 65504.0f);
+                dst[(size_t)(beg + n) * I] = __float2half_rn(odd ? hv * 0.0625f : hv);  // odd words / 16
+              }
+            }
+            if (bad) set_error(a.err, kErrNonFinite);
+          }
+        } else {
+          float dv[16];
+          dense::tc_ld16(ta + 16 * hf, dv);
+          if (rr < nrows) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = 32 * cbk + 16 * hf + j;
+              if (n < cnt) a.obuf[(size_t)(beg + n) * H + r0 + rr] = s_w[n] * dv[j];
+            }
+          }
+        }
+      }
+    }
+    dense::tc_fence_before();
+    if (!fused::cons_sync_and(okd)) {
+      if (tid == 0) set_error(a.err, kErrTimeout);
+      break;
+    }
+    if (tid == 0) mbar_arrive_expect_tx(tfree, 0);  // the MMA warp may overwrite the accumulators
+  }
+  if (tracer) trace_max(a.trace, kTrExit);
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// A tensor map over a row-major tensor (dims[0] innermost, byte strides of
+// dims 1..); elements outside the tensor read as zero.
+bool encode_map(EncodeTiledFn f, CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *ptr,
+                const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return f(m, dt, (cuuint32_t)rank, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           sw, sw == CU_TENSOR_MAP_SWIZZLE_NONE ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand rows of x and h per sorted position (fp16, boxes of 64 elements x
+// 128 rows with the 128-byte swizzle), the codes of gate, up and down
+// (boxes of 32 bytes x 128 rows of one expert) for the routed experts (3-D
+// over the fixed-stride blobs) and the shared expert.
+bool prompt_maps(const PromptArgs &a, dense::Maps &m) {
+  const EncodeTiledFn f = encode_tiled();
+  if (!f) return false;
+  const cuuint64_t H = a.d.H, I = a.d.I, E = a.d.E, npos = (cuuint64_t)a.d.T * (a.d.k + 1);
+  const cuuint32_t bx[2] = {64, (cuuint32_t)kTileRows};
+  bool ok = true;
+  {
+    const cuuint64_t dims[2] = {H, npos}, str[1] = {H * 2};
+    ok = ok && encode_map(f, &m.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.xg, dims, str, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  {
+    const cuuint64_t dims[2] = {I, npos}, str[1] = {I * 2};
+    ok = ok && encode_map(f, &m.h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.hg, dims, str, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const cuuint32_t bq[3] = {32, (cuuint32_t)kTileRows, 1};
+  auto codes = [&](CUtensorMap *mm, size_t off, cuuint64_t row_bytes, cuuint64_t rows) {
+    const cuuint64_t dr[3] = {row_bytes, rows, E}, sr[2] = {row_bytes, a.w.stride};
+    const cuuint64_t ds[3] = {row_bytes, rows, 1}, ss[2] = {row_bytes, row_bytes * rows};
+    return encode_map(f, &mm[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w.experts + off, dr, sr, bq,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_map(f, &mm[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w.shared + off, ds, ss, bq,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  };
+  ok = ok && codes(m.gq, a.w.off.gate_q, H / 2, I) && codes(m.uq, a.w.off.up_q, H / 2, I) &&
+       codes(m.dq, a.w.off.down_q, I / 2, H);
+  return ok;
+}
+}  // namespace
+
+int prompt_max_chunks(int T, int k, int E) {
+  return (T * k + kPromptChunk - 1) / kPromptChunk + E + (T + kPromptChunk - 1) / kPromptChunk;
+}
+
+bool prompt_supported(const Dims &d) {
+  if (rt_layout(d.H, d.E).total > 227 * 1024) return false;
+  return gemm_plan(d.H / kGroup, false, gemm_stages(d.H / kGroup, false)).total <= 227 * 1024 &&
+         gemm_plan(d.I / kGroup, true, gemm_stages(d.I / kGroup, true)).total <= 227 * 1024;
+}
+
+cudaError_t prompt_set_attributes() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(prompt_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)))
+    return e;
+  if ((e = cudaFuncSetAttribute(prompt_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)))
+    return e;
+  return cudaFuncSetAttribute(prompt_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+cudaError_t launch_prompt(const PromptArgs &a, uint16_t *y, bool add_residual, int n_sm, cudaStream_t st, bool pdl) {
+  const int T = a.d.T, k = a.d.k;
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  prm.a = a;
+  if (!prompt_maps(a, prm.m)) return cudaErrorInvalidValue;
+  auto with_trace = [&](int i) {
+    PromptArgs b = a;
+    if (b.trace) b.trace += 4 * i;
+    return b;
+  };
+  cudaError_t e = launch_k(prompt_router_kernel, dim3((T + kRtTok - 1) / kRtTok), dim3(kRtThreads),
+                           (size_t)rt_layout(a.d.H, a.d.E).total, st, pdl, with_trace(0));
+  if (e == cudaSuccess) e = launch_k(prompt_sort_kernel, dim3(1), dim3(kSortThreads), 0, st, pdl, with_trace(1));
+  if (e == cudaSuccess) {
+    const int npos = T * (k + 1);
+    e = launch_k(prompt_gather_kernel, dim3((npos + kGatherThreads / 32 - 1) / (kGatherThreads / 32)),
+                 dim3(kGatherThreads), 0, st, pdl, with_trace(2));
+  }
+  const int gu_st = gemm_stages(a.d.H / kGroup, false), dn_st = gemm_stages(a.d.I / kGroup, true);
+  if (e == cudaSuccess) {
+    prm.a = with_trace(3);
+    prm.stages = gu_st;
+    e = launch_k(prompt_gemm_kernel<false>, dim3(n_sm), dim3(kGemmThreads),
+                 (size_t)gemm_plan(a.d.H / kGroup, false, gu_st).total, st, pdl, prm);
+  }
+  if (e == cudaSuccess) {
+    prm.a = with_trace(4);
+    prm.stages = dn_st;
+    e = launch_k(prompt_gemm_kernel<true>, dim3(n_sm), dim3(kGemmThreads),
+                 (size_t)gemm_plan(a.d.I / kGroup, true, dn_st).total, st, pdl, prm);
+  }
+  if (e == cudaSuccess) {
+    FfnArgs c;
+    memset(&c, 0, sizeof(c));
+    c.w = a.w;
+    c.d = a.d;
+    c.r = a.r;
+    c.obuf = a.obuf;
+    c.y = y;
+    c.hres = add_residual ? a.hres : nullptr;
+    c.include_shared = 1;
+    c.err = a.err;
+    c.trace = a.trace ? a.trace + 4 * 5 : nullptr;
+    e = launch_combine(c, st, pdl);
+  }
+  return e;
+}
+
+}  // namespace moe

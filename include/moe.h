@@ -218,6 +218,41 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
                                int32_t *ids_out, float *logits_out, void *ws, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* ---- whole-prompt layer (section "Prefill": layer-major execution; the
+ * token/expert pairs grouped into bounded routed-MoE work; experts streamed
+ * in tiles of at most eight, the next tile fetched while the current tile's
+ * work is queued; shared and routed branches combined before the tail).
+ *
+ * The same function as moe_layer_forward_residual, for a prompt of up to
+ * MOE_PROMPT_MAX_ROWS rows in one call:
+ *   hidden <- bf16(hidden + MoE(rmsnorm(hidden)))   (or the layer's tail)
+ * row by row.  Rows are routed independently; all rows' token/expert pairs
+ * are grouped per expert and cut into chunks of at most 128 rows of one
+ * expert, and every (chunk, 128 weight rows) is one unit of a persistent
+ * tensor-core GEMM (tcgen05.mma, weights dequantised once per unit into fp16
+ * on chip: w = q * s + b rounded once to fp16).  Units run the shared
+ * expert first, then experts in ascending id, i.e. tile after tile of eight
+ * experts, so an expert's weights come from HBM about once per layer and
+ * its later chunks read them from L2; each SM prefetches its next unit's
+ * weights into L2 while the current one runs.
+ *   hidden    bf16 [n_rows, H] in/out
+ *   n_rows    1 <= n_rows <= MOE_PROMPT_MAX_ROWS
+ *   y_out, x_out, ids_out, logits_out: nullable, as in
+ *             moe_layer_forward_residual ([n_rows, ...])
+ *   ws        moe_prompt_workspace_bytes(dims, n_rows) bytes, 256-aligned
+ *             (about 0.7 GB at 4096 rows of the target shape: the operand,
+ *             h and fp32 expert-output rows of every sorted position)
+ * Six launches (router, grouping, operand gather, gate/up GEMM, down GEMM,
+ * combine; a seventh for a layer tail), none of which waits for another
+ * block, so the call may share the device.  Errors as for the other layer
+ * calls; MOE_ERR_UNSUPPORTED when the shape's tiles do not fit on chip.
+ * Capturable in a CUDA graph (the tensor maps are kernel parameters). */
+#define MOE_PROMPT_MAX_ROWS 4096
+size_t moe_prompt_workspace_bytes(const moe_dims *dims, int n_rows);
+int moe_layer_forward_prompt(moe_handle *h, void *hidden, int n_rows, const moe_layer_weights *w,
+                             void *y_out, void *x_out, int32_t *ids_out, float *logits_out,
+                             void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* n_layers single-token layers of a residual stack in one call (the decode
  * step of the section "Decode": every layer's router input is the residual
  * stream normalised, its block output is added back):

@@ -52,6 +52,27 @@ def test_workspace_bytes(lib):
         assert lib.moe_workspace_bytes(ctypes.byref(bad), 1) == 0
 
 
+def test_prompt_workspace_bytes(lib):
+    """The whole-prompt layer's workspace: every sorted position's operand row
+    (fp16 [T*k + T, H]), h row (fp16 [.., I]) and fp32 expert output row, the
+    normalised rows and the routing; zero outside 1 <= n_rows <= 4096."""
+    d = bq.make_dims(2816, 704, 128, 8)
+    sizes = [lib.moe_prompt_workspace_bytes(ctypes.byref(d), t) for t in (1, 129, 1000, 4096)]
+    assert all(s > 0 and s % 256 == 0 for s in sizes)
+    assert sizes == sorted(sizes)
+    npos = 4096 * 9
+    assert sizes[3] >= npos * (2816 * 2 + 704 * 2 + 2816 * 4) + 4096 * 2816 * 2
+    assert sizes[3] < 1 << 30
+    for t in (0, -1, bq.MOE_PROMPT_MAX_ROWS + 1):
+        assert lib.moe_prompt_workspace_bytes(ctypes.byref(d), t) == 0
+    for bad in (bq.make_dims(2816, 704, 128, 8, group=32), bq.make_dims(2816, 704, 129, 8),
+                bq.make_dims(8192, 704, 128, 8)):
+        assert lib.moe_prompt_workspace_bytes(ctypes.byref(bad), 16) == 0
+    # every supported small shape has a plan
+    for dims in ((64, 64, 1, 1), (128, 64, 8, 2), (192, 128, 16, 8), (4096, 2048, 128, 8)):
+        assert lib.moe_prompt_workspace_bytes(ctypes.byref(bq.make_dims(*dims)), 33) > 0, dims
+
+
 def test_check_weights(lib):
     d = bq.make_dims(2816, 704, 128, 8)
     w = _weights(d)
@@ -92,6 +113,8 @@ def test_calls_without_handle_are_rejected(lib):
     layers = (bq.LayerWeights * 2)(w, w)
     assert lib.moe_layer_forward_stack(None, V(1 << 40), 2, layers, V(1 << 40), 1 << 30,
                                        None) == bq.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward_prompt(None, V(1 << 40), 300, ctypes.byref(w), None, None, None, None, V(1 << 40),
+                                        1 << 30, None) == bq.MOE_ERR_INVALID_ARG
     assert lib.moe_get_error(None, None) == bq.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == bq.MOE_ERR_INVALID_ARG
     hw = bq.make_head_weights(262144, 2816, 1 << 40, 1 << 41, 1 << 42)
