@@ -52,6 +52,9 @@ SUB_STEPS = {"layer1": 64, "batch64": 32, "prefill128": 32, "prefill30": 8}
 # the tied 4-bit head (vocabulary 262,144 x hidden 2816, group-64 affine) on one
 # decoded token: greedy token only, softcap 30
 HEAD_V, HEAD_STEPS, HEAD_SOFTCAP = 262144, 32, 30.0
+# the whole-prompt layer: a 4096-row prompt (32 chunks of 128) through the
+# 30-layer stack layer-major, each layer one moe_layer_forward_prompt call
+PROMPT_ROWS, PROMPT_STEPS = 4096, 4
 # expert offload: a 4-layer decode stack (Zipf-skewed routing, the pages'
 # premise) with each layer's routed experts in pinned host memory behind 16
 # device slots per layer
@@ -416,6 +419,7 @@ def run_ours(args, spec, rank, world, device):
                            "achieved_gbs": round(o["achieved"], 1), "frac": round(o["frac"], 4),
                            "traffic": otraffic,
                            "gpu_launches": r["launches_per_call"] * r["calls_per_step"] * steps}
+        subs["prompt30"] = time_prompt(moe, layers.weights(WORKLOADS["prefill30"]), device, world)
         subs["head"] = time_head(moe, device, hbm, world)
         subs["offload"] = time_offload(moe, device, world)
         line["workloads"] = subs
@@ -423,6 +427,109 @@ def run_ours(args, spec, rank, world, device):
         line["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
     moe.close()
     return line
+
+
+def prompt_flops(n_rows: int) -> int:
+    """Algorithmic FLOPs of one whole-prompt layer call: the router (2 T E H)
+    and the gate, up and down contractions of every routed pair and every
+    shared row (2 (T k + T) 3 I H)."""
+    return 2 * n_rows * E * H + 2 * n_rows * (K + 1) * 3 * I * H
+
+
+def time_prompt(moe, weights, device, world):
+    """A PROMPT_ROWS-row prompt through the 30-layer stack (Zipf-skewed
+    routing), one moe_layer_forward_prompt call per layer, the 30 calls of a
+    step in one CUDA graph; CUDA events around each replay (inputs: a fresh
+    RMS-normalised prompt per step, 433 MB of weights per layer > L2).  Also
+    the per-call duration (events around each of the 30 calls, no graph)
+    and, from the launch trace of one call, the two GEMM launches' spans."""
+    import torch
+    from synth import gen
+
+    T = PROMPT_ROWS
+    steps_total = 3 + PROMPT_STEPS
+    inputs = torch.from_numpy(np.stack([gen.hidden_states(5000, s, T, H, rms_normalize=True)
+                                        for s in range(steps_total)]).view(np.int16)).to(device)
+    h = torch.empty((T, H), dtype=torch.int16, device=device)
+    ws = torch.empty(moe.prompt_workspace_bytes(weights[0].dims, T), dtype=torch.uint8, device=device)
+    st = torch.cuda.Stream(device)
+
+    def step_calls():
+        for w in weights:
+            moe.layer_forward_prompt(h, T, w, ws, stream=st)
+
+    h.copy_(inputs[0])
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(st):
+        step_calls()  # warm the code path once outside capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            step_calls()
+    torch.cuda.synchronize(device)
+    assert moe.get_error() == 0, "prompt layer call reported an error"
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps_total)]
+    with torch.cuda.stream(st):
+        for s in range(steps_total):
+            h.copy_(inputs[s], non_blocking=True)
+            kev[s][0].record(st)
+            g.replay()
+            kev[s][1].record(st)
+    torch.cuda.synchronize(device)
+    assert moe.get_error() == 0, "prompt layer call reported an error"
+    step_s = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in kev[3:]) / 1e3, world, device)
+    # per call, events around each call (no graph)
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in weights]
+    with torch.cuda.stream(st):
+        h.copy_(inputs[0], non_blocking=True)
+        for (a, b), w in zip(cev, weights):
+            a.record(st)
+            moe.layer_forward_prompt(h, T, w, ws, stream=st)
+            b.record(st)
+    torch.cuda.synchronize(device)
+    call_s = statistics.median(a.elapsed_time(b) for a, b in cev) / 1e3
+    # per-launch spans of one call from the trace slots (first block past its
+    # dependency wait to the last block's exit, device global timer)
+    trace = torch.zeros(4 * 8, dtype=torch.int64, device=device)
+    moe.set_trace(trace, 8)
+    with torch.cuda.stream(st):
+        moe.layer_forward_prompt(h, T, weights[0], ws, stream=st)
+    torch.cuda.synchronize(device)
+    moe.set_trace(None, 0)
+    v = [int(q) & 0xFFFFFFFFFFFFFFFF for q in trace.cpu().tolist()]
+    m64 = 0xFFFFFFFFFFFFFFFF
+    names = ("router", "sort", "gather", "gemm_gate_up", "gemm_down", "combine")
+    spans = {n: round(((v[4 * i + 3] - (v[4 * i + 1] ^ m64)) / 1e3), 1) if v[4 * i + 1] and v[4 * i + 3] else None
+             for i, n in enumerate(names)}
+    launches = sum(1 for i in range(6) if v[4 * i])
+    flops = prompt_flops(T)
+    gemm_us = (spans["gemm_gate_up"] or 0) + (spans["gemm_down"] or 0)
+    peak = tensor_peak()
+    del ws, inputs
+    return {"workload": "prefill, 30-layer MoE stack, a %d-row prompt per step (32 chunks of 128), Zipf(1.1) logit "
+                        "offsets per layer, each layer one whole-prompt call (all chunks' pairs grouped per expert, "
+                        "expert tiles of eight in order)" % T,
+            "value": round(world * T / step_s, 3), "unit": "rows/s", "steps": PROMPT_STEPS, "warmup": 3,
+            "ms_per_step": round(step_s * 1e3, 4), "layer_call_us": round(call_s * 1e6, 2),
+            "launches_per_call": launches, "launch_spans_us": spans,
+            "roofline": {"bound": "tensor", "unit": "TFLOP/s", "peak": peak[0], "peak_kind": peak[1],
+                         "algorithmic_flops_per_call": flops,
+                         "achieved_call": round(flops / call_s / 1e12, 1),
+                         "frac_call": round(flops / call_s / 1e12 / peak[0], 4),
+                         "achieved_gemm": round((flops - 2 * T * E * H) / (gemm_us * 1e-6) / 1e12, 1) if gemm_us else None,
+                         "frac_gemm": round((flops - 2 * T * E * H) / (gemm_us * 1e-6) / 1e12 / peak[0], 4)
+                         if gemm_us else None},
+            "gpu_launches": launches * len(weights) * PROMPT_STEPS}
+
+
+def tensor_peak():
+    """Dense fp16/bf16 tensor peak (TFLOP/s): the measured sustained figure
+    (a kernel timed inside a long step), else the fallback."""
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops_sustained"]), "measured sustained bf16 (fp16 runs at the same rate)"
+    except Exception:
+        return 1700.0, "fallback sustained bf16"
 
 
 def time_head(moe, device, hbm, world):

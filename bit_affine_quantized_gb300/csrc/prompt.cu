@@ -52,13 +52,13 @@ namespace {
 constexpr int kRtTok = 16;        // rows per router block (one m16 tile)
 constexpr int kRtThreads = 256;   // 8 warps, 16 experts (two n8 tiles) each
 constexpr int kRtGroups = 2;      // 64-wide K groups per code stage
-constexpr int kRtStages = 3;
 constexpr int kRtCodePitch = 64 * kRtGroups + 16;  // bytes per expert row of a stage: rows 4 banks apart
+constexpr int kRowVec = 16;       // 16-byte vectors of one row per lane (H <= 4096)
 
 struct RtLayout {
-  int xp, x, xs, sb, codes, total;
+  int xp, x, xs, sb, sbp, codes, total;  // sbp: byte offset of the biases after the scales (16-aligned)
 };
-__host__ __device__ inline RtLayout rt_layout(int H, int E) {
+__host__ __device__ inline RtLayout rt_layout(int H, int E, int kRtStages) {
   const int G = H / kGroup;
   RtLayout L;
   L.xp = 2 * H + 16;  // fp16 row pitch: consecutive rows 4 banks apart
@@ -68,7 +68,8 @@ __host__ __device__ inline RtLayout rt_layout(int H, int E) {
   L.xs = o;
   o += kRtTok * G * 4;
   L.sb = o;
-  o = (o + 2 * E * G * 2 + 15) & ~15;
+  L.sbp = (E * G * 2 + 15) & ~15;
+  o += 2 * L.sbp;
   L.codes = o;
   o += kRtStages * E * kRtCodePitch;
   L.total = o;
@@ -93,13 +94,16 @@ __device__ __forceinline__ uint32_t codes8_f16x2(uint32_t pair) {
   return r;
 }
 
+// kRtStages: code stages in flight (deeper when the row tile leaves room)
+template <int kRtStages>
 __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int H = a.d.H, E = a.d.E, T = a.d.T, k = a.d.k, G = H / kGroup;
-  const RtLayout L = rt_layout(H, E);
+  const RtLayout L = rt_layout(H, E, kRtStages);
   uint8_t *sx = smem + L.x;
   float *sxs = reinterpret_cast<float *>(smem + L.xs);
-  uint16_t *ssb = reinterpret_cast<uint16_t *>(smem + L.sb);  // scales [E][G], then biases [E][G]
+  uint16_t *ssb = reinterpret_cast<uint16_t *>(smem + L.sb);            // scales [E][G]
+  uint16_t *sbb = reinterpret_cast<uint16_t *>(smem + L.sb + L.sbp);    // biases [E][G]
   uint8_t *scodes = smem + L.codes;
   float *slogit = reinterpret_cast<float *>(scodes);  // [kRtTok][E], after the K loop
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -120,11 +124,20 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
     }
     cp_async_commit();
   };
-  for (int s = 0; s < kRtStages - 1; ++s) load_stage(s);
-  for (int i = tid; i < E * G; i += kRtThreads) {
-    ssb[i] = __ldg(a.w.router_s + i);
-    ssb[E * G + i] = __ldg(a.w.router_b + i);
+  // scales and biases: 16-byte asynchronous copies (with the first code stage), the tail plainly
+  {
+    const int n16 = E * G * 2 / 16;
+    for (int i = tid; i < 2 * n16; i += kRtThreads) {
+      const int f = i >= n16, j = i - f * n16;
+      cp_async16(reinterpret_cast<uint8_t *>(f ? sbb : ssb) + 16 * j,
+                 reinterpret_cast<const uint8_t *>(f ? a.w.router_b : a.w.router_s) + 16 * j);
+    }
+    for (int i = 8 * n16 + tid; i < E * G; i += kRtThreads) {
+      ssb[i] = __ldg(a.w.router_s + i);
+      sbb[i] = __ldg(a.w.router_b + i);
+    }
   }
+  for (int s = 0; s < kRtStages - 1; ++s) load_stage(s);
   pdl_wait();
   pdl_launch_dependents();
   if (blockIdx.x == 0 && tid == 0) trace_min(a.trace, kTrWaited);
@@ -139,16 +152,22 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
       for (int g = lane; g < G; g += 32) sxs[rl * G + g] = 0.f;
       continue;
     }
-    const uint16_t *src = a.hres + (size_t)(t0 + rl) * H;
-    float ss = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(src) + v);
-      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.hres + (size_t)(t0 + rl) * H);
+    uint4 u[kRowVec];  // the whole row, every load in flight at once
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
-        ss = fmaf(lo, lo, ss);
-        ss = fmaf(hi, hi, ss);
+    for (int i = 0; i < kRowVec; ++i)
+      if (lane + 32 * i < nvec) u[i] = __ldcg(src + lane + 32 * i);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) {
+      if (lane + 32 * i < nvec) {
+        const uint32_t w4[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(w4[q] << 16), hi = __uint_as_float(w4[q] & 0xFFFF0000u);
+          ss = fmaf(lo, lo, ss);
+          ss = fmaf(hi, hi, ss);
+        }
       }
     }
 #pragma unroll
@@ -156,12 +175,12 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
     const float inv = 1.0f / sqrtf(ss / (float)H + 1e-6f);
     const float isq = rsqrtf((float)H);
     // lanes 8q .. 8q+7 hold the eight vectors of one 64-group (nvec is a multiple of 8)
-    for (int v0 = 0; v0 < nvec; v0 += 32) {
-      const int v = v0 + lane;
+#pragma unroll
+    for (int i = 0; i < kRowVec; ++i) {
+      const int v = lane + 32 * i;
       float gs = 0.f;
       if (v < nvec) {
-        const uint4 u = __ldcg(reinterpret_cast<const uint4 *>(src) + v);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t w4[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
         uint32_t ob[4], oh[4];
         uint4 rv = make_uint4(0u, 0u, 0u, 0u);
         if (a.w.router_scale) rv = __ldg(reinterpret_cast<const uint4 *>(a.w.router_scale) + v);
@@ -235,7 +254,7 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
           for (int i = 0; i < 4; ++i) {
             const int e = n0 + 8 * nt + 2 * c + (i & 1);
             const int ee = e < E ? e : E - 1;  // columns past E are discarded below
-            const float sc = bf16_bits_to_float(ssb[ee * G + g]), bi = bf16_bits_to_float(ssb[E * G + ee * G + g]);
+            const float sc = bf16_bits_to_float(ssb[ee * G + g]), bi = bf16_bits_to_float(sbb[ee * G + g]);
             tot[nt][i] = fmaf(bi, (i >> 1) ? x1 : x0, fmaf(sc, acc[nt][i], tot[nt][i]));
           }
       }
@@ -272,6 +291,8 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
 // ------------------------------------------------------------------ grouping
 constexpr int kSortThreads = 1024;
 constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortPer = kPromptMaxRows * kMaxTopK / (kSortWarps * 32);  // ids per lane
+static_assert(kSortPer * kSortWarps * 32 >= kPromptMaxRows * kMaxTopK, "every pair has a lane");
 
 // Exclusive scan of v over the 32 lanes of one warp; returns the lane's
 // prefix and writes the total to *sum (every lane).
@@ -287,6 +308,19 @@ __device__ __forceinline__ int warp_excl_scan(int v, int *sum) {
   return incl - v;
 }
 
+// Lanes of the warp holding the same valid key e (E <= 128: seven key bits,
+// one ballot each); a lane without a valid key is its own only peer.
+__device__ __forceinline__ unsigned key_peers(int e, bool ok) {
+  unsigned peers = __ballot_sync(0xffffffffu, ok);
+#pragma unroll
+  for (int b = 0; b < 7; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned bb = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? bb : ~bb;
+  }
+  return ok ? peers : (1u << (threadIdx.x & 31));
+}
+
 __global__ void __launch_bounds__(kSortThreads) prompt_sort_kernel(const PromptArgs a) {
   __shared__ int s_hist[kSortWarps][kMaxExperts];  // pairs per (warp segment, expert), then segment bases
   __shared__ int s_off[kMaxExperts + 1];
@@ -296,18 +330,26 @@ __global__ void __launch_bounds__(kSortThreads) prompt_sort_kernel(const PromptA
   if (tid == 0) trace_min(a.trace, kTrEntry);
   pdl_wait();
   pdl_launch_dependents();
+  if (tid == 0) trace_min(a.trace, kTrWaited);
   for (int i = tid; i < kSortWarps * kMaxExperts; i += kSortThreads) (&s_hist[0][0])[i] = 0;
   __syncthreads();
   // each warp owns one contiguous segment of the pairs, 32 at a time in order
-  const int seg = (n + kSortWarps - 1) / kSortWarps;
+  const int seg = (n + kSortWarps - 1) / kSortWarps;  // <= kSortPer * 32
   const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+  int ev[kSortPer];  // the segment's ids, every load in flight at once
+#pragma unroll
+  for (int q = 0; q < kSortPer; ++q) {
+    const int p = s0 + 32 * q + lane;
+    ev[q] = p < s1 ? __ldcg(a.r.ids + p) : -1;
+  }
   bool bad = false;
-  for (int b = s0; b < s1; b += 32) {
-    const int p = b + lane;
-    const int e = p < s1 ? __ldcg(a.r.ids + p) : -1;
+#pragma unroll
+  for (int q = 0; q < kSortPer; ++q) {
+    if (s0 + 32 * q >= s1) break;  // warp-uniform
+    const int p = s0 + 32 * q + lane, e = ev[q];
     const bool ok = p < s1 && e >= 0 && e < E;
     bad = bad || (p < s1 && !ok);
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : (1 << 30) + lane);
+    const unsigned peers = key_peers(e, ok);
     if (ok && (peers & lanemask_lt()) == 0) s_hist[warp][e] += __popc(peers);
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(a.err, kErrBadId);
@@ -350,11 +392,12 @@ __global__ void __launch_bounds__(kSortThreads) prompt_sort_kernel(const PromptA
     }
   }
   __syncthreads();
-  for (int b = s0; b < s1; b += 32) {
-    const int p = b + lane;
-    const int e = p < s1 ? __ldcg(a.r.ids + p) : -1;
+#pragma unroll
+  for (int q = 0; q < kSortPer; ++q) {
+    if (s0 + 32 * q >= s1) break;  // warp-uniform
+    const int p = s0 + 32 * q + lane, e = ev[q];
     const bool ok = p < s1 && e >= 0 && e < E;
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : (1 << 30) + lane);
+    const unsigned peers = key_peers(e, ok);
     if (ok) {
       const int q = s_hist[warp][e] + __popc(peers & lanemask_lt());
       a.r.perm[q] = p;
@@ -418,6 +461,7 @@ __global__ void __launch_bounds__(kGatherThreads) prompt_gather_kernel(const Pro
   if (blockIdx.x == 0 && threadIdx.x == 0) trace_min(a.trace, kTrEntry);
   pdl_wait();
   pdl_launch_dependents();
+  if (blockIdx.x == 0 && threadIdx.x == 0) trace_min(a.trace, kTrWaited);
   const int n = T * k;
   // positions of dropped pairs (bad ids) are never read: no row for them
   int tok = -1;
@@ -427,22 +471,38 @@ __global__ void __launch_bounds__(kGatherThreads) prompt_gather_kernel(const Pro
     tok = __ldcg(a.r.perm + pos) / k;
   const uint4 *src = reinterpret_cast<const uint4 *>(a.xn + (size_t)(tok < 0 ? 0 : tok) * H);
   uint4 *dst = reinterpret_cast<uint4 *>(a.xg + (size_t)pos * H);
-  for (int q = lane; tok >= 0 && q < H / 16; q += 32) {
-    const uint4 v0 = __ldcg(src + 2 * q), v1 = __ldcg(src + 2 * q + 1);
-    const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t out[8];
-    operand_quarter<true>(in, out);
-    dst[2 * q] = make_uint4(out[0], out[1], out[2], out[3]);
-    dst[2 * q + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+  uint4 v[2 * kRowVec / 2];  // quarters lane, lane + 32, ... (H <= 4096: 8 per lane), loaded at once
+  constexpr int kQ = kRowVec / 2;
+#pragma unroll
+  for (int i = 0; i < kQ; ++i) {
+    const int q = lane + 32 * i;
+    if (tok >= 0 && q < H / 16) {
+      v[2 * i] = __ldcg(src + 2 * q);
+      v[2 * i + 1] = __ldcg(src + 2 * q + 1);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kQ; ++i) {
+    const int q = lane + 32 * i;
+    if (tok >= 0 && q < H / 16) {
+      const uint32_t in[8] = {v[2 * i].x, v[2 * i].y, v[2 * i].z, v[2 * i].w,
+                              v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
+      uint32_t out[8];
+      operand_quarter<true>(in, out);
+      dst[2 * q] = make_uint4(out[0], out[1], out[2], out[3]);
+      dst[2 * q + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
   }
   if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) trace_max(a.trace, kTrExit);
 }
 
 // ------------------------------------------------------------------ expert GEMM
-constexpr int kGemmCons = fused::kCons;                 // 16 dequantisation / epilogue warps
+constexpr int kGemmCons = fused::kCons;                 // 16 dequantisation warps
 constexpr int kGemmProd = kGemmCons;                    // producer warp
 constexpr int kGemmMma = kGemmCons + 1;                 // tcgen05 issue warp
-constexpr int kGemmThreads = (kGemmCons + 2) * 32;      // 576
+constexpr int kGemmEpi0 = kGemmCons + 2;                // 4 epilogue warps (tensor-memory lane quarters 2, 3, 0, 1)
+constexpr int kGemmEpiWarps = 4;
+constexpr int kGemmThreads = (kGemmCons + 2 + kGemmEpiWarps) * 32;  // 704
 constexpr int kTileRows = dense::kRows;                 // 128 weight rows per unit
 constexpr int kMaxStages = 8;
 
@@ -468,7 +528,7 @@ __host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
   o += (down ? 2 : 4) * kTileRows * G * 2;
   o = (o + 15) & ~15;
   P.bar = o;
-  o += 1024;  // barriers [0, 256), tensor-memory address at 256, column weights at 512
+  o += 256;  // barriers [0, 216), tensor-memory address at 240
   P.total = o + 1024;  // slack for the 1024-byte alignment of the base
   return P;
 }
@@ -484,6 +544,19 @@ struct GemmParams {
   int stages;
 };
 
+// Prefetch of a 2-D tensor box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// Persistent GEMM over the units (chunk, 128 weight rows), u = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  Roles: the producer warp streams each K
+// group's operand rows and codes (TMA) through `stages` buffers; 16 warps
+// dequantise the codes into a double-buffered fp16 A tile; the MMA warp
+// issues the group's tcgen05.mma into one of two accumulator sets in tensor
+// memory (units alternate between them); 4 epilogue warps read a finished
+// unit's accumulators while the next unit's MMAs run.
 template <bool kDown>
 __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __grid_constant__ GemmParams prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -491,20 +564,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   const int H = a.d.H, I = a.d.I, T = a.d.T, k = a.d.k;
   const int K = kDown ? I : H, G = K / kGroup, M = kDown ? H : I;
   const int ntile = (M + kTileRows - 1) / kTileRows;
-  constexpr int nm = kDown ? 1 : 2;  // matrices per unit
+  constexpr int nm = kDown ? 1 : 2;                // matrices per unit
+  constexpr uint32_t kAccCols = 128 * nm;          // tensor-memory columns of one accumulator set
+  constexpr uint32_t kTmemCols = 2 * kAccCols;     // two sets: 256 (down) or 512 (gate/up)
   uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const GemmPlan P = gemm_plan(G, kDown, prm.stages);
   const int S = P.stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(base + P.bar);  // [S] TMA landed
   uint64_t *empty = full + kMaxStages;                          // [S] MMAs done with a stage
   uint64_t *adone = empty + kMaxStages;                         // [2] MMAs done with an A buffer
-  uint64_t *afull = adone + 2;                                  // [2] A buffer written (every warp)
+  uint64_t *afull = adone + 2;                                  // [2] A buffer written (every dequant warp)
   uint64_t *sfull = afull + 2;                                  // scales of the unit landed
-  uint64_t *sempty = sfull + 1;                                 // scales consumed (every warp)
-  uint64_t *tfree = sempty + 1;                                 // epilogue done with tensor memory
-  uint64_t *tready = tfree + 1;                                 // tensor memory allocated
-  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(base + P.bar + 256);
-  float *s_w = reinterpret_cast<float *>(base + P.bar + 512);  // [128] routing weight per column
+  uint64_t *sempty = sfull + 1;                                 // scales consumed (every dequant warp)
+  uint64_t *tfull = sempty + 1;                                 // [2] accumulator set complete
+  uint64_t *tempty = tfull + 2;                                 // [2] accumulator set read out (every epilogue warp)
+  uint64_t *tready = tempty + 2;                                // tensor memory allocated
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(base + P.bar + 240);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool tracer = blockIdx.x == 0 && tid == 0;
 
@@ -513,13 +588,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&adone[0], 1);
-    mbar_init(&adone[1], 1);
-    mbar_init(&afull[0], kGemmCons);
-    mbar_init(&afull[1], kGemmCons);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&adone[i], 1);
+      mbar_init(&afull[i], kGemmCons);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kGemmEpiWarps);
+    }
     mbar_init(sfull, 1);
     mbar_init(sempty, kGemmCons);
-    mbar_init(tfree, 1);
     mbar_init(tready, 1);
     fence_mbar_init();
   }
@@ -529,6 +605,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   pdl_launch_dependents();
   if (tracer) trace_min(a.trace, kTrWaited);
   const int nunits = __ldcg(a.n_ch) * ntile;
+  const int npairs = T * k;
 
   // ============================================================ producer warp
   if (warp == kGemmProd) {
@@ -536,12 +613,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     bool ok = true;
     int gi = 0, du = 0;  // K groups issued, units whose scales went out
     const int nf = kDown ? 2 : 4;
+    const CUtensorMap *bmap = kDown ? &prm.m.h : &prm.m.x;
     auto field_off = [&](int f) -> size_t {
       if (kDown) return f == 0 ? a.w.off.down_s : a.w.off.down_b;
       return f == 0 ? a.w.off.gate_s : f == 1 ? a.w.off.gate_b : f == 2 ? a.w.off.up_s : a.w.off.up_b;
     };
-    // the codes of one K group of a unit into L2 (no shared memory, no completion)
-    auto prefetch_group = [&](int e, int r0, int g) {
+    // one K group of a unit into L2: its codes and its operand rows (no shared memory, no completion)
+    auto prefetch_group = [&](int e, int r0, int beg, int g) {
       const int sh = e < 0 ? 1 : 0;
       if (kDown) {
         dense::tma_prefetch_3d(&prm.m.dq[sh], 32 * g, r0, sh ? 0 : e);
@@ -549,6 +627,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
         dense::tma_prefetch_3d(&prm.m.gq[sh], 32 * g, r0, sh ? 0 : e);
         dense::tma_prefetch_3d(&prm.m.uq[sh], 32 * g, r0, sh ? 0 : e);
       }
+      tma_prefetch_2d(bmap, 64 * g, beg);
     };
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const int ch = u / ntile, rt = u - ch * ntile;
@@ -560,10 +639,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       // groups and its scales into L2 while this unit runs
       const int un = u + gridDim.x;
       if (un < nunits && lane == 0) {
-        const int chn = un / ntile, rtn = un - chn * ntile, en = __ldcg(a.ch_e + chn);
+        const int chn = un / ntile, rtn = un - chn * ntile, en = __ldcg(a.ch_e + chn), bgn = __ldcg(a.ch_beg + chn);
         const uint8_t *bn = en < 0 ? a.w.shared : a.w.experts + (size_t)en * a.w.stride;
         const int r0n = rtn * kTileRows, nrn = min(kTileRows, M - r0n);
-        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(en, r0n, g);
+        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(en, r0n, bgn, g);
         for (int f = 0; f < nf; ++f) prefetch_l2(bn + field_off(f) + (size_t)r0n * G * 2, (uint32_t)(nrn * G * 2));
       }
       if (du >= 1) ok = __all_sync(0xffffffffu, mbar_wait_idle(sempty, (du - 1) & 1, 32));
@@ -575,15 +654,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
                  (uint32_t)(nrows * G * 2), sfull);
       ++du;
       if (lane == 0)  // this unit's first groups (later ones: kAhead ahead of their TMA below)
-        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(e, r0, g);
+        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(e, r0, beg, g);
       for (int g = 0; g < G && ok; ++g, ++gi) {
         const int st = gi % S;
         if (gi >= S) ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[st], ((gi / S) - 1) & 1, 32));
         if (!ok) break;
         if (lane == 0) {
-          if (g + dense::kAhead < G) prefetch_group(e, r0, g + dense::kAhead);
+          if (g + dense::kAhead < G) prefetch_group(e, r0, beg, g + dense::kAhead);
           mbar_arrive_expect_tx(&full[st], (uint32_t)(P.bstage + P.cstage));
-          dense::tma_load_2d(base + P.b0 + st * P.bstage, kDown ? &prm.m.h : &prm.m.x, 64 * g, beg, &full[st]);
+          dense::tma_load_2d(base + P.b0 + st * P.bstage, bmap, 64 * g, beg, &full[st]);
           uint8_t *cd = base + P.c0 + st * P.cstage;
           if (kDown) {
             dense::tma_load_3d(cd, &prm.m.dq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
@@ -605,11 +684,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   }
 
   // ============================================================ MMA warp
-  // Owns the tensor memory (gate in columns 0..127, up in 128..255; down
-  // uses the first 128) and issues each K group's tcgen05.mma once the
-  // consumers have written its A tile.
+  // Owns the tensor memory: accumulator set b at columns b * kAccCols (gate
+  // first, then up).  Issues each K group's tcgen05.mma once the dequant
+  // warps have written its A tile.
   if (warp == kGemmMma) {
-    dense::tc_alloc(s_tmem, 256);
+    dense::tc_alloc(s_tmem, kTmemCols);
     dense::tc_fence_before();
     __syncwarp();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
@@ -620,9 +699,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       const int ch = u / ntile;
       const int N = (__ldcg(a.ch_cnt + ch) + 15) & ~15;  // MMA N: the chunk's rows, padded to 16
       const uint32_t idesc = dense::idesc_f16(kTileRows, N);
-      if (du >= 1) ok = __all_sync(0xffffffffu, mbar_wait_idle(tfree, (du - 1) & 1, 32));  // accumulators read out
+      const int tb = du & 1;
+      // the set's previous unit read out by the epilogue
+      if (du >= 2) ok = __all_sync(0xffffffffu, mbar_wait_idle(&tempty[tb], ((du >> 1) - 1) & 1, 32));
       ++du;
       dense::tc_fence_after();
+      const uint32_t acc = tmem + tb * kAccCols;
       for (int g = 0; g < G && ok; ++g, ++gi) {
         const int st = gi % S, ab = gi & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (gi / S) & 1) && mbar_wait(&afull[ab], (gi >> 1) & 1));
@@ -636,41 +718,103 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
             for (int m = 0; m < nm; ++m) {
               const uint64_t ad =
                   dense::sdesc(smem_addr(base + P.a0 + ab * P.abuf + m * kTileRows * 128) + ks * 32, 16, 1024, 2);
-              dense::tc_mma(tmem + m * 128, ad, bd, idesc, (g > 0 || ks > 0) ? 1u : 0u);
+              dense::tc_mma(acc + m * 128, ad, bd, idesc, (g > 0 || ks > 0) ? 1u : 0u);
             }
           }
-          dense::tc_commit(&empty[st]);  // the TMA stage may be refilled
-          dense::tc_commit(&adone[ab]);  // the A buffer may be rewritten; after the last group: unit done
+          dense::tc_commit(&empty[st]);               // the TMA stage may be refilled
+          dense::tc_commit(&adone[ab]);               // the A buffer may be rewritten
+          if (g == G - 1) dense::tc_commit(&tfull[tb]);  // the unit's accumulators are complete
         }
         __syncwarp();
       }
     }
     if (!ok && lane == 0) set_error(a.err, kErrTimeout);
-    // tensor memory back once the last MMAs completed and the last epilogue read them (bounded waits)
+    // tensor memory back once the last MMAs completed and the epilogue read them (bounded waits)
     if (gi > 0) mbar_wait(&adone[(gi - 1) & 1], ((gi - 1) >> 1) & 1);
-    if (du > 0) mbar_wait_idle(tfree, (du - 1) & 1, 64);
+    if (du > 0) mbar_wait_idle(&tempty[(du - 1) & 1], ((du - 1) >> 1) & 1, 64);
     dense::tc_fence_after();
     __syncwarp();
-    dense::tc_dealloc(tmem, 256);
+    dense::tc_dealloc(tmem, kTmemCols);
     return;
   }
 
-  // ============================================================ consumers
+  // ============================================================ epilogue warps
+  // Warp w reads tensor-memory lanes 32 (w % 4) .. +31: weight rows r0 + rr.
+  // Gate/up: h = gelu_tanh(gate) * up per (row, column), stored fp16 in the
+  // operand order of the down units at the chunk's positions.  Down: the
+  // routing weight of each column's pair times the output row, fp32.
+  if (warp >= kGemmEpi0) {
+    bool ok = mbar_wait(tready, 0);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
+    const int rr = 32 * (warp & 3) + lane;
+    int du = 0;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++du) {
+      const int ch = u / ntile, rt = u - ch * ntile;
+      const int beg = __ldcg(a.ch_beg + ch), cnt = __ldcg(a.ch_cnt + ch);
+      const int r0 = rt * kTileRows, nrows = min(kTileRows, M - r0);
+      const int tb = du & 1;
+      // routing weights of columns lane, lane + 32, ... (down; shared rows: 1)
+      float wq[4] = {1.f, 1.f, 1.f, 1.f};
+      if (kDown)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int n = 32 * q + lane;
+          if (n < cnt && beg + n < npairs) wq[q] = __ldcg(a.r.wts + __ldcg(a.r.perm + beg + n));
+        }
+      ok = __all_sync(0xffffffffu, mbar_wait(&tfull[tb], (du >> 1) & 1));
+      if (!ok) break;
+      dense::tc_fence_after();
+      const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + tb * kAccCols;
+      const int i = r0 + rr;
+      bool odd = false;
+      const int slot = dense::operand_slot(i & 63, odd);
+      bool bad = false;
+      for (int c0 = 0; c0 < cnt; c0 += 16) {  // 16 columns at a time (warp-uniform)
+        if (!kDown) {
+          float gv[16], uv[16];
+          dense::tc_ld16(ta + c0, gv);
+          dense::tc_ld16(ta + 128 + c0, uv);
+          if (rr < nrows) {
+            __half *dst = a.hg + (size_t)(beg + c0) * I + (i & ~63) + slot;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < cnt) {
+                const float hv = gelu_tanh(gv[j]) * uv[j];
+                bad = bad || !(fabsf(hv) <= 65504.0f);
+                dst[(size_t)j * I] = __float2half_rn(odd ? hv * 0.0625f : hv);  // odd words / 16
+              }
+            }
+          }
+        } else {
+          float dv[16];
+          dense::tc_ld16(ta + c0, dv);
+          float *dst = a.obuf + (size_t)(beg + c0) * H + r0 + rr;
+          const int q = c0 >> 5;  // the 16 columns share one group of 32 weights
+          const float wsel = q == 0 ? wq[0] : q == 1 ? wq[1] : q == 2 ? wq[2] : wq[3];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = c0 + j;
+            const float w = __shfl_sync(0xffffffffu, wsel, n & 31);
+            if (n < cnt && rr < nrows) dst[(size_t)j * H] = w * dv[j];
+          }
+        }
+      }
+      if (bad) set_error(a.err, kErrNonFinite);
+      dense::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&tempty[tb], 0);  // this warp is done with the set
+    }
+    if (!ok && lane == 0) set_error(a.err, kErrTimeout);
+    if (tracer || (blockIdx.x == 0 && warp == kGemmEpi0 && lane == 0)) trace_max(a.trace, kTrExit);
+    return;
+  }
+
+  // ============================================================ dequantisation warps
   const uint16_t *sb = reinterpret_cast<const uint16_t *>(base + P.s);
-  const int npairs = T * k;
-  uint32_t tmem = 0;
-  bool have_tmem = false, okd = true;
+  bool okd = true;
   int gi = 0, du = 0;
-  for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-    const int ch = u / ntile, rt = u - ch * ntile;
-    const int beg = __ldcg(a.ch_beg + ch), cnt = __ldcg(a.ch_cnt + ch);
-    const int r0 = rt * kTileRows, nrows = min(kTileRows, M - r0);
-    const int N = (cnt + 15) & ~15;
-    if (kDown)
-      for (int n = tid; n < cnt; n += kGemmCons * 32)
-        s_w[n] = beg + n >= npairs ? 1.0f : __ldcg(a.r.wts + __ldcg(a.r.perm + beg + n));
-    fused::cons_sync();  // the column weights are in place before any warp's epilogue reads them
-    okd = okd && mbar_wait(sfull, du & 1);
+  for (int u = blockIdx.x; u < nunits && okd; u += gridDim.x) {
+    okd = mbar_wait(sfull, du & 1);
     ++du;
     for (int g = 0; g < G; ++g, ++gi) {
       const int st = gi % S, ab = gi & 1;
@@ -711,62 +855,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     }
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(sempty, 0);  // this warp is done with the unit's scales
-    okd = okd && mbar_wait(&adone[(gi - 1) & 1], ((gi - 1) >> 1) & 1);  // every MMA of the unit done
-    if (!have_tmem) {
-      okd = okd && mbar_wait(tready, 0);
-      tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
-      have_tmem = true;
-    }
-    okd = __all_sync(0xffffffffu, okd);  // tcgen05.ld below is warp-collective
-    dense::tc_fence_after();
-    // epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (weight
-    // rows) and columns 32 (w / 4) .. +31 (the chunk's rows)
-    const int w4 = warp & 3, cbk = warp >> 2, rr = 32 * w4 + lane;
-    if (okd && 32 * cbk < N) {
-      const uint32_t ta = tmem + ((uint32_t)(32 * w4) << 16) + 32 * cbk;
-      for (int hf = 0; hf < 2; ++hf) {  // 16 columns at a time
-        if (!kDown) {
-          float gv[16], uv[16];
-          dense::tc_ld16(ta + 16 * hf, gv);
-          dense::tc_ld16(ta + 128 + 16 * hf, uv);
-          if (rr < nrows) {
-            const int i = r0 + rr;
-            bool odd = false;
-            const int slot = dense::operand_slot(i & 63, odd);
-            __half *dst = a.hg + (i & ~63) + slot;
-            bool bad = false;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = 32 * cbk + 16 * hf + j;
-              if (n < cnt) {
-                const float hv = gelu_tanh(gv[j]) * uv[j];
-                bad = bad || !(fabsf(hv) <= 65504.0f);
-                dst[(size_t)(beg + n) * I] = __float2half_rn(odd ? hv * 0.0625f : hv);  // odd words / 16
-              }
-            }
-            if (bad) set_error(a.err, kErrNonFinite);
-          }
-        } else {
-          float dv[16];
-          dense::tc_ld16(ta + 16 * hf, dv);
-          if (rr < nrows) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = 32 * cbk + 16 * hf + j;
-              if (n < cnt) a.obuf[(size_t)(beg + n) * H + r0 + rr] = s_w[n] * dv[j];
-            }
-          }
-        }
-      }
-    }
-    dense::tc_fence_before();
-    if (!fused::cons_sync_and(okd)) {
-      if (tid == 0) set_error(a.err, kErrTimeout);
-      break;
-    }
-    if (tid == 0) mbar_arrive_expect_tx(tfree, 0);  // the MMA warp may overwrite the accumulators
+    okd = __all_sync(0xffffffffu, okd);
   }
-  if (tracer) trace_max(a.trace, kTrExit);
+  if (!okd && lane == 0) set_error(a.err, kErrTimeout);
 }
 
 // ------------------------------------------------------------------ host side
@@ -832,15 +923,20 @@ int prompt_max_chunks(int T, int k, int E) {
   return (T * k + kPromptChunk - 1) / kPromptChunk + E + (T + kPromptChunk - 1) / kPromptChunk;
 }
 
+// code stages of the router: six when the row tile leaves room, else three
+static int rt_stages(const Dims &d) { return rt_layout(d.H, d.E, 6).total <= 227 * 1024 ? 6 : 3; }
+
 bool prompt_supported(const Dims &d) {
-  if (rt_layout(d.H, d.E).total > 227 * 1024) return false;
+  if (rt_layout(d.H, d.E, 3).total > 227 * 1024) return false;
   return gemm_plan(d.H / kGroup, false, gemm_stages(d.H / kGroup, false)).total <= 227 * 1024 &&
          gemm_plan(d.I / kGroup, true, gemm_stages(d.I / kGroup, true)).total <= 227 * 1024;
 }
 
 cudaError_t prompt_set_attributes() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(prompt_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)))
+  if ((e = cudaFuncSetAttribute(prompt_router_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)))
+    return e;
+  if ((e = cudaFuncSetAttribute(prompt_router_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)))
     return e;
   if ((e = cudaFuncSetAttribute(prompt_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024)))
     return e;
@@ -858,8 +954,10 @@ cudaError_t launch_prompt(const PromptArgs &a, uint16_t *y, bool add_residual, i
     if (b.trace) b.trace += 4 * i;
     return b;
   };
-  cudaError_t e = launch_k(prompt_router_kernel, dim3((T + kRtTok - 1) / kRtTok), dim3(kRtThreads),
-                           (size_t)rt_layout(a.d.H, a.d.E).total, st, pdl, with_trace(0));
+  const int rst = rt_stages(a.d);
+  cudaError_t e = launch_k(rst == 6 ? prompt_router_kernel<6> : prompt_router_kernel<3>,
+                           dim3((T + kRtTok - 1) / kRtTok), dim3(kRtThreads),
+                           (size_t)rt_layout(a.d.H, a.d.E, rst).total, st, pdl, with_trace(0));
   if (e == cudaSuccess) e = launch_k(prompt_sort_kernel, dim3(1), dim3(kSortThreads), 0, st, pdl, with_trace(1));
   if (e == cudaSuccess) {
     const int npos = T * (k + 1);
