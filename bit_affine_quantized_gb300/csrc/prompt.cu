@@ -509,14 +509,19 @@ constexpr int kMaxStages = 8;
 // Shared-memory plan of a GEMM block (offsets from a 1024-aligned base).
 struct GemmPlan {
   int stages, bstage, cstage, abuf;
-  int b0, c0, a0, s, bar, total;
+  int b0, c0, a0, bar, total;
 };
+// Both kernels run two 128-row weight matrices per unit against one operand
+// tile: gate and up rows r0 .. r0+127 (gate/up), or W_down rows r0 .. r0+127
+// and r0+128 .. r0+255 (down).
 __host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
+  (void)G;
+  (void)down;
   GemmPlan P;
   P.stages = stages;
-  P.bstage = kTileRows * 128;                   // 128 operand rows x 64 fp16
-  P.cstage = (down ? 1 : 2) * kTileRows * 32;   // 128 rows x 64 codes per matrix
-  P.abuf = (down ? 1 : 2) * kTileRows * 128;    // dequantised A per matrix
+  P.bstage = kTileRows * 128;       // 128 operand rows x 64 fp16
+  P.cstage = 2 * kTileRows * 32;    // 128 rows x 64 codes per matrix
+  P.abuf = 2 * kTileRows * 128;     // dequantised A per matrix
   int o = 0;
   P.b0 = o;
   o += stages * P.bstage;
@@ -524,16 +529,13 @@ __host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
   o += stages * P.cstage;
   P.a0 = o;
   o += 2 * P.abuf;
-  P.s = o;
-  o += (down ? 2 : 4) * kTileRows * G * 2;
-  o = (o + 15) & ~15;
   P.bar = o;
   o += 256;  // barriers [0, 216), tensor-memory address at 240
   P.total = o + 1024;  // slack for the 1024-byte alignment of the base
   return P;
 }
 __host__ inline int gemm_stages(int G, bool down) {
-  int s = down ? kMaxStages : 4;
+  int s = kMaxStages;
   while (s > 2 && gemm_plan(G, down, s).total > 227 * 1024) --s;
   return s;
 }
@@ -563,10 +565,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   const PromptArgs &a = prm.a;
   const int H = a.d.H, I = a.d.I, T = a.d.T, k = a.d.k;
   const int K = kDown ? I : H, G = K / kGroup, M = kDown ? H : I;
-  const int ntile = (M + kTileRows - 1) / kTileRows;
-  constexpr int nm = kDown ? 1 : 2;                // matrices per unit
+  constexpr int kUnitRows = kDown ? 2 * kTileRows : kTileRows;  // rows of M one unit covers
+  const int ntile = (M + kUnitRows - 1) / kUnitRows;
+  constexpr int nm = 2;                            // matrices per unit
   constexpr uint32_t kAccCols = 128 * nm;          // tensor-memory columns of one accumulator set
-  constexpr uint32_t kTmemCols = 2 * kAccCols;     // two sets: 256 (down) or 512 (gate/up)
+  constexpr uint32_t kTmemCols = 2 * kAccCols;     // two sets
   uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const GemmPlan P = gemm_plan(G, kDown, prm.stages);
   const int S = P.stages;
@@ -574,9 +577,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   uint64_t *empty = full + kMaxStages;                          // [S] MMAs done with a stage
   uint64_t *adone = empty + kMaxStages;                         // [2] MMAs done with an A buffer
   uint64_t *afull = adone + 2;                                  // [2] A buffer written (every dequant warp)
-  uint64_t *sfull = afull + 2;                                  // scales of the unit landed
-  uint64_t *sempty = sfull + 1;                                 // scales consumed (every dequant warp)
-  uint64_t *tfull = sempty + 1;                                 // [2] accumulator set complete
+  uint64_t *tfull = afull + 2;                                  // [2] accumulator set complete
   uint64_t *tempty = tfull + 2;                                 // [2] accumulator set read out (every epilogue warp)
   uint64_t *tready = tempty + 2;                                // tensor memory allocated
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(base + P.bar + 240);
@@ -594,8 +595,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kGemmEpiWarps);
     }
-    mbar_init(sfull, 1);
-    mbar_init(sempty, kGemmCons);
     mbar_init(tready, 1);
     fence_mbar_init();
   }
@@ -611,61 +610,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   if (warp == kGemmProd) {
     fused::fence_proxy_async_global();  // operand rows written by the previous launch are read by the TMA
     bool ok = true;
-    int gi = 0, du = 0;  // K groups issued, units whose scales went out
-    const int nf = kDown ? 2 : 4;
+    int gi = 0;  // K groups issued
     const CUtensorMap *bmap = kDown ? &prm.m.h : &prm.m.x;
+    // field f = 2 m + (0: scale, 1: bias) of matrix m; its first weight row
     auto field_off = [&](int f) -> size_t {
-      if (kDown) return f == 0 ? a.w.off.down_s : a.w.off.down_b;
+      if (kDown) return (f & 1) ? a.w.off.down_b : a.w.off.down_s;
       return f == 0 ? a.w.off.gate_s : f == 1 ? a.w.off.gate_b : f == 2 ? a.w.off.up_s : a.w.off.up_b;
     };
-    // one K group of a unit into L2: its codes and its operand rows (no shared memory, no completion)
-    auto prefetch_group = [&](int e, int r0, int beg, int g) {
-      const int sh = e < 0 ? 1 : 0;
-      if (kDown) {
-        dense::tma_prefetch_3d(&prm.m.dq[sh], 32 * g, r0, sh ? 0 : e);
-      } else {
-        dense::tma_prefetch_3d(&prm.m.gq[sh], 32 * g, r0, sh ? 0 : e);
-        dense::tma_prefetch_3d(&prm.m.uq[sh], 32 * g, r0, sh ? 0 : e);
+    auto mrow = [&](int r0, int m) { return kDown ? r0 + kTileRows * m : r0; };
+    auto mrows = [&](int r0, int m) { return max(0, min(kTileRows, M - mrow(r0, m))); };
+    // a unit's weights into L2: the codes, scales and biases of its rows of
+    // both matrices are contiguous ranges of the blob (a few bulk requests)
+    auto prefetch_unit = [&](const uint8_t *bn, int r0n) {
+      const size_t qo0 = kDown ? a.w.off.down_q : a.w.off.gate_q, qo1 = kDown ? a.w.off.down_q : a.w.off.up_q;
+      for (int mm = 0; mm < 2; ++mm) {
+        const int rows = mrows(r0n, mm);
+        if (rows == 0) continue;
+        const size_t qrow = (size_t)K / 2;  // code bytes per row
+        const uint8_t *q = bn + (mm ? qo1 : qo0) + (size_t)mrow(r0n, mm) * qrow;
+        for (size_t o = 0; o < rows * qrow; o += 65536)
+          prefetch_l2(q + o, (uint32_t)min((size_t)65536, rows * qrow - o));
+        for (int f = 2 * mm; f < 2 * mm + 2; ++f)
+          prefetch_l2(bn + field_off(f) + (size_t)mrow(r0n, mm) * G * 2, (uint32_t)(rows * G * 2));
       }
-      tma_prefetch_2d(bmap, 64 * g, beg);
     };
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const int ch = u / ntile, rt = u - ch * ntile;
       const int e = __ldcg(a.ch_e + ch), beg = __ldcg(a.ch_beg + ch);
       const int sh = e < 0 ? 1 : 0;
       const uint8_t *blob = sh ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
-      const int r0 = rt * kTileRows, nrows = min(kTileRows, M - r0);
-      // the block's next unit (the next tile of the sweep): its first K
-      // groups and its scales into L2 while this unit runs
-      const int un = u + gridDim.x;
-      if (un < nunits && lane == 0) {
-        const int chn = un / ntile, rtn = un - chn * ntile, en = __ldcg(a.ch_e + chn), bgn = __ldcg(a.ch_beg + chn);
-        const uint8_t *bn = en < 0 ? a.w.shared : a.w.experts + (size_t)en * a.w.stride;
-        const int r0n = rtn * kTileRows, nrn = min(kTileRows, M - r0n);
-        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(en, r0n, bgn, g);
-        for (int f = 0; f < nf; ++f) prefetch_l2(bn + field_off(f) + (size_t)r0n * G * 2, (uint32_t)(nrn * G * 2));
+      const int r0 = rt * kUnitRows;
+      // the block's next unit (the next tile of the sweep): its weights
+      // into L2 while this unit runs; the first unit's own
+      if (lane == 0) {
+        if (u == (int)blockIdx.x) prefetch_unit(blob, r0);
+        const int un = u + gridDim.x;
+        if (un < nunits) {
+          const int chn = un / ntile, en = __ldcg(a.ch_e + chn);
+          prefetch_unit(en < 0 ? a.w.shared : a.w.experts + (size_t)en * a.w.stride, (un - chn * ntile) * kUnitRows);
+        }
       }
-      if (du >= 1) ok = __all_sync(0xffffffffu, mbar_wait_idle(sempty, (du - 1) & 1, 32));
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(sfull, (uint32_t)(nf * nrows * G * 2));
-      __syncwarp();
-      if (lane < nf)
-        bulk_g2s(base + P.s + lane * kTileRows * G * 2, blob + field_off(lane) + (size_t)r0 * G * 2,
-                 (uint32_t)(nrows * G * 2), sfull);
-      ++du;
-      if (lane == 0)  // this unit's first groups (later ones: kAhead ahead of their TMA below)
-        for (int g = 0; g < G && g < dense::kAhead; ++g) prefetch_group(e, r0, beg, g);
       for (int g = 0; g < G && ok; ++g, ++gi) {
         const int st = gi % S;
         if (gi >= S) ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[st], ((gi / S) - 1) & 1, 32));
         if (!ok) break;
         if (lane == 0) {
-          if (g + dense::kAhead < G) prefetch_group(e, r0, beg, g + dense::kAhead);
           mbar_arrive_expect_tx(&full[st], (uint32_t)(P.bstage + P.cstage));
           dense::tma_load_2d(base + P.b0 + st * P.bstage, bmap, 64 * g, beg, &full[st]);
           uint8_t *cd = base + P.c0 + st * P.cstage;
-          if (kDown) {
+          if (kDown) {  // both halves (rows past H read as zero)
             dense::tma_load_3d(cd, &prm.m.dq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
+            dense::tma_load_3d(cd + kTileRows * 32, &prm.m.dq[sh], 32 * g, r0 + kTileRows, sh ? 0 : e, &full[st]);
           } else {
             dense::tma_load_3d(cd, &prm.m.gq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
             dense::tma_load_3d(cd + kTileRows * 32, &prm.m.uq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
@@ -678,7 +673,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     if (lane == 0) {
       if (!ok) set_error(a.err, kErrTimeout);
       for (int j = gi - S > 0 ? gi - S : 0; j < gi; ++j) mbar_wait_idle(&full[j % S], (j / S) & 1);
-      if (du >= 1) mbar_wait_idle(sfull, (du - 1) & 1);
     }
     return;
   }
@@ -751,7 +745,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++du) {
       const int ch = u / ntile, rt = u - ch * ntile;
       const int beg = __ldcg(a.ch_beg + ch), cnt = __ldcg(a.ch_cnt + ch);
-      const int r0 = rt * kTileRows, nrows = min(kTileRows, M - r0);
+      const int r0 = rt * kUnitRows, nrows = min(kTileRows, M - r0);
       const int tb = du & 1;
       // routing weights of columns lane, lane + 32, ... (down; shared rows: 1)
       float wq[4] = {1.f, 1.f, 1.f, 1.f};
@@ -786,16 +780,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
             }
           }
         } else {
-          float dv[16];
-          dense::tc_ld16(ta + c0, dv);
-          float *dst = a.obuf + (size_t)(beg + c0) * H + r0 + rr;
           const int q = c0 >> 5;  // the 16 columns share one group of 32 weights
           const float wsel = q == 0 ? wq[0] : q == 1 ? wq[1] : q == 2 ? wq[2] : wq[3];
+#pragma unroll 1
+          for (int m = 0; m < 2; ++m) {  // output rows r0 + 128 m + rr
+            float dv[16];
+            dense::tc_ld16(ta + 128 * m + c0, dv);
+            const int row = r0 + kTileRows * m + rr;
+            float *dst = a.obuf + (size_t)(beg + c0) * H + row;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = c0 + j;
-            const float w = __shfl_sync(0xffffffffu, wsel, n & 31);
-            if (n < cnt && rr < nrows) dst[(size_t)j * H] = w * dv[j];
+            for (int j = 0; j < 16; ++j) {
+              const int n = c0 + j;
+              const float w = __shfl_sync(0xffffffffu, wsel, n & 31);
+              if (n < cnt && row < M) dst[(size_t)j * H] = w * dv[j];
+            }
           }
         }
       }
@@ -810,51 +808,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   }
 
   // ============================================================ dequantisation warps
-  const uint16_t *sb = reinterpret_cast<const uint16_t *>(base + P.s);
+  // Thread: matrix m (gate / up, or the two halves of W_down), half hh of
+  // the K group, weight row rr.  Its row's scale and bias come from global
+  // memory (the 32-byte sector of a row holds 16 groups: after the first
+  // group of a sector the loads hit L1), one group ahead of their use.
+  const int m = tid >> 8, hh = (tid >> 7) & 1, rr = tid & 127;
   bool okd = true;
-  int gi = 0, du = 0;
+  int gi = 0;
   for (int u = blockIdx.x; u < nunits && okd; u += gridDim.x) {
-    okd = mbar_wait(sfull, du & 1);
-    ++du;
+    const int ch = u / ntile, rt = u - ch * ntile;
+    const int e = __ldcg(a.ch_e + ch);
+    const uint8_t *blob = e < 0 ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
+    const int wrow = (kDown ? rt * kUnitRows + kTileRows * m : rt * kUnitRows) + rr;
+    const bool rvalid = wrow < M;
+    const size_t so = kDown ? a.w.off.down_s : (m ? a.w.off.up_s : a.w.off.gate_s);
+    const size_t bo = kDown ? a.w.off.down_b : (m ? a.w.off.up_b : a.w.off.gate_b);
+    const uint16_t *srow = reinterpret_cast<const uint16_t *>(blob + so) + (size_t)(rvalid ? wrow : 0) * G;
+    const uint16_t *brow = reinterpret_cast<const uint16_t *>(blob + bo) + (size_t)(rvalid ? wrow : 0) * G;
+    uint16_t sn = __ldg(srow), bn = __ldg(brow);
     for (int g = 0; g < G; ++g, ++gi) {
       const int st = gi % S, ab = gi & 1;
+      const uint16_t sc = sn, bc = bn;
+      if (g + 1 < G) {
+        sn = __ldg(srow + g + 1);
+        bn = __ldg(brow + g + 1);
+      }
       okd = okd && mbar_wait(&full[st], (gi / S) & 1);
       if (gi >= 2) okd = okd && mbar_wait(&adone[ab], ((gi >> 1) - 1) & 1);
       if (okd) {
         const uint8_t *cb = base + P.c0 + st * P.cstage;
         uint8_t *abuf = base + P.a0 + ab * P.abuf;
-        const int rr = tid & 127;
-        if (!kDown) {
-          const int m = tid >> 8, hh = (tid >> 7) & 1;  // matrix (gate, up), half of the group
-          const uint4 cw = *reinterpret_cast<const uint4 *>(cb + m * kTileRows * 32 + rr * 32 + hh * 16);
-          const float sf = bf16_bits_to_float(sb[(2 * m) * kTileRows * G + rr * G + g]);
-          const float bf = bf16_bits_to_float(sb[(2 * m + 1) * kTileRows * G + rr * G + g]);
-          const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
-          // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
-          uint8_t *row = abuf + m * kTileRows * 128 + rr * 128;
-          const int sw = rr & 7, j0 = 4 * hh;
-          *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
-          *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
-          *reinterpret_cast<uint4 *>(row + ((j0 + 2) ^ sw) * 16) = dense::dequant_word(cw.z, s2, b2, b16);
-          *reinterpret_cast<uint4 *>(row + ((j0 + 3) ^ sw) * 16) = dense::dequant_word(cw.w, s2, b2, b16);
-        } else {
-          const int qq = tid >> 7;  // quarter of the group
-          const uint2 cw = *reinterpret_cast<const uint2 *>(cb + rr * 32 + qq * 8);
-          const float sf = bf16_bits_to_float(sb[rr * G + g]);
-          const float bf = bf16_bits_to_float(sb[kTileRows * G + rr * G + g]);
-          const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
-          uint8_t *row = abuf + rr * 128;
-          const int sw = rr & 7, j0 = 2 * qq;
-          *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
-          *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
-        }
+        const uint4 cw = *reinterpret_cast<const uint4 *>(cb + m * kTileRows * 32 + rr * 32 + hh * 16);
+        const float sf = bf16_bits_to_float(sc);
+        const float bf = bf16_bits_to_float(bc);
+        const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
+        // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
+        uint8_t *row = abuf + m * kTileRows * 128 + rr * 128;
+        const int sw = rr & 7, j0 = 4 * hh;
+        *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + ((j0 + 2) ^ sw) * 16) = dense::dequant_word(cw.z, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + ((j0 + 3) ^ sw) * 16) = dense::dequant_word(cw.w, s2, b2, b16);
       }
       dense::fence_async_smem();  // the A tiles, written by threads, are read by the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&afull[ab], 0);  // this warp's part of the A tile is in place
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(sempty, 0);  // this warp is done with the unit's scales
     okd = __all_sync(0xffffffffu, okd);
   }
   if (!okd && lane == 0) set_error(a.err, kErrTimeout);
