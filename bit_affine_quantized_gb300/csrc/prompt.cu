@@ -504,7 +504,8 @@ constexpr int kGemmEpi0 = kGemmCons + 2;                // 4 epilogue warps (ten
 constexpr int kGemmEpiWarps = 4;
 constexpr int kGemmThreads = (kGemmCons + 2 + kGemmEpiWarps) * 32;  // 704
 constexpr int kTileRows = dense::kRows;                 // 128 weight rows per unit
-constexpr int kMaxStages = 8;
+constexpr int kStages = 6;  // TMA stages (operand rows + codes of one K group)
+constexpr int kABuf = 2;    // dequantised A tiles in flight (the dequant warps run kABuf - 1 groups ahead)
 
 // Shared-memory plan of a GEMM block (offsets from a 1024-aligned base).
 struct GemmPlan {
@@ -528,29 +529,19 @@ __host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
   P.c0 = o;
   o += stages * P.cstage;
   P.a0 = o;
-  o += 2 * P.abuf;
+  o += kABuf * P.abuf;
   P.bar = o;
-  o += 256;  // barriers [0, 216), tensor-memory address at 240
+  o += 320;  // barriers [0, 8 (20 + 2 kABuf + 1)), tensor-memory address at 304
   P.total = o + 1024;  // slack for the 1024-byte alignment of the base
   return P;
 }
-__host__ inline int gemm_stages(int G, bool down) {
-  int s = kMaxStages;
-  while (s > 2 && gemm_plan(G, down, s).total > 227 * 1024) --s;
-  return s;
-}
+constexpr int kGemmSmem = kStages * (kTileRows * 128 + 2 * kTileRows * 32) + kABuf * 2 * kTileRows * 128 + 320 + 1024;
+static_assert(kGemmSmem <= 227 * 1024, "the GEMM plan fits one block per SM");
 
 struct GemmParams {
   dense::Maps m;  // 64-byte aligned: first
   PromptArgs a;
-  int stages;
 };
-
-// Prefetch of a 2-D tensor box into L2 (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(c0), "r"(c1)
-               : "memory");
-}
 
 // Persistent GEMM over the units (chunk, 128 weight rows), u = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  Roles: the producer warp streams each K
@@ -571,16 +562,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   constexpr uint32_t kAccCols = 128 * nm;          // tensor-memory columns of one accumulator set
   constexpr uint32_t kTmemCols = 2 * kAccCols;     // two sets
   uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const GemmPlan P = gemm_plan(G, kDown, prm.stages);
-  const int S = P.stages;
+  const GemmPlan P = gemm_plan(G, kDown, kStages);
+  constexpr int S = kStages;
   uint64_t *full = reinterpret_cast<uint64_t *>(base + P.bar);  // [S] TMA landed
-  uint64_t *empty = full + kMaxStages;                          // [S] MMAs done with a stage
-  uint64_t *adone = empty + kMaxStages;                         // [2] MMAs done with an A buffer
-  uint64_t *afull = adone + 2;                                  // [2] A buffer written (every dequant warp)
-  uint64_t *tfull = afull + 2;                                  // [2] accumulator set complete
+  uint64_t *empty = full + S;                                   // [S] MMAs done with a stage
+  uint64_t *adone = empty + S;                                  // [kABuf] MMAs done with an A buffer
+  uint64_t *afull = adone + kABuf;                              // [kABuf] A buffer written (every dequant warp)
+  uint64_t *tfull = afull + kABuf;                              // [2] accumulator set complete
   uint64_t *tempty = tfull + 2;                                 // [2] accumulator set read out (every epilogue warp)
   uint64_t *tready = tempty + 2;                                // tensor memory allocated
-  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(base + P.bar + 240);
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(base + P.bar + 304);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool tracer = blockIdx.x == 0 && tid == 0;
 
@@ -589,9 +580,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kABuf; ++i) {
       mbar_init(&adone[i], 1);
       mbar_init(&afull[i], kGemmCons);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kGemmEpiWarps);
     }
@@ -610,7 +603,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   if (warp == kGemmProd) {
     fused::fence_proxy_async_global();  // operand rows written by the previous launch are read by the TMA
     bool ok = true;
-    int gi = 0;  // K groups issued
+    int gi = 0, st = 0, ph = 0;  // K groups issued; next stage and its use parity
     const CUtensorMap *bmap = kDown ? &prm.m.h : &prm.m.x;
     // field f = 2 m + (0: scale, 1: bias) of matrix m; its first weight row
     auto field_off = [&](int f) -> size_t {
@@ -651,8 +644,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
         }
       }
       for (int g = 0; g < G && ok; ++g, ++gi) {
-        const int st = gi % S;
-        if (gi >= S) ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[st], ((gi / S) - 1) & 1, 32));
+        if (gi >= S) ok = __all_sync(0xffffffffu, mbar_wait_idle(&empty[st], ph ^ 1, 32));
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[st], (uint32_t)(P.bstage + P.cstage));
@@ -667,6 +659,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
           }
         }
         __syncwarp();
+        if (++st == S) {
+          st = 0;
+          ph ^= 1;
+        }
       }
     }
     // copies in flight land before the block's shared memory is released
@@ -688,7 +684,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(s_tmem);
     if (lane == 0) mbar_arrive_expect_tx(tready, 0);
     bool ok = true;
-    int gi = 0, du = 0;
+    int gi = 0, du = 0, st = 0, ph = 0, ab = 0, aph = 0;
+    // shared-memory descriptors of stage 0's operand rows and A buffer 0;
+    // the others are these plus their byte offsets / 16
+    const uint64_t bdesc0 = dense::sdesc(smem_addr(base + P.b0), 16, 1024, 2);
+    const uint64_t adesc0 = dense::sdesc(smem_addr(base + P.a0), 16, 1024, 2);
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
       const int ch = u / ntile;
       const int N = (__ldcg(a.ch_cnt + ch) + 15) & ~15;  // MMA N: the chunk's rows, padded to 16
@@ -700,31 +700,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       dense::tc_fence_after();
       const uint32_t acc = tmem + tb * kAccCols;
       for (int g = 0; g < G && ok; ++g, ++gi) {
-        const int st = gi % S, ab = gi & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (gi / S) & 1) && mbar_wait(&afull[ab], (gi >> 1) & 1));
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph) && mbar_wait(&afull[ab], aph));
         if (!ok) break;
         dense::tc_fence_after();
         if (lane == 0) {
+          const uint64_t bd0 = bdesc0 + (uint64_t)((st * P.bstage) >> 4);
+          const uint64_t ad0 = adesc0 + (uint64_t)((ab * P.abuf) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = dense::sdesc(smem_addr(base + P.b0 + st * P.bstage) + ks * 32, 16, 1024, 2);
+          for (int ks = 0; ks < 4; ++ks)  // K = 16 per MMA: 32 bytes further along each row
 #pragma unroll
-            for (int m = 0; m < nm; ++m) {
-              const uint64_t ad =
-                  dense::sdesc(smem_addr(base + P.a0 + ab * P.abuf + m * kTileRows * 128) + ks * 32, 16, 1024, 2);
-              dense::tc_mma(acc + m * 128, ad, bd, idesc, (g > 0 || ks > 0) ? 1u : 0u);
-            }
-          }
+            for (int m = 0; m < nm; ++m)
+              dense::tc_mma(acc + m * 128, ad0 + (uint64_t)(((m * kTileRows * 128) >> 4) + 2 * ks), bd0 + 2 * ks, idesc,
+                            (g > 0 || ks > 0) ? 1u : 0u);
           dense::tc_commit(&empty[st]);               // the TMA stage may be refilled
           dense::tc_commit(&adone[ab]);               // the A buffer may be rewritten
           if (g == G - 1) dense::tc_commit(&tfull[tb]);  // the unit's accumulators are complete
         }
         __syncwarp();
+        if (++st == S) {
+          st = 0;
+          ph ^= 1;
+        }
+        if (++ab == kABuf) {
+          ab = 0;
+          aph ^= 1;
+        }
       }
     }
     if (!ok && lane == 0) set_error(a.err, kErrTimeout);
     // tensor memory back once the last MMAs completed and the epilogue read them (bounded waits)
-    if (gi > 0) mbar_wait(&adone[(gi - 1) & 1], ((gi - 1) >> 1) & 1);
+    if (gi > 0) mbar_wait(&adone[(gi - 1) % kABuf], ((gi - 1) / kABuf) & 1);
     if (du > 0) mbar_wait_idle(&tempty[(du - 1) & 1], ((du - 1) >> 1) & 1, 64);
     dense::tc_fence_after();
     __syncwarp();
@@ -814,7 +819,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   // group of a sector the loads hit L1), one group ahead of their use.
   const int m = tid >> 8, hh = (tid >> 7) & 1, rr = tid & 127;
   bool okd = true;
-  int gi = 0;
+  int gi = 0, st = 0, ph = 0, ab = 0, aph = 0;
   for (int u = blockIdx.x; u < nunits && okd; u += gridDim.x) {
     const int ch = u / ntile, rt = u - ch * ntile;
     const int e = __ldcg(a.ch_e + ch);
@@ -827,14 +832,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     const uint16_t *brow = reinterpret_cast<const uint16_t *>(blob + bo) + (size_t)(rvalid ? wrow : 0) * G;
     uint16_t sn = __ldg(srow), bn = __ldg(brow);
     for (int g = 0; g < G; ++g, ++gi) {
-      const int st = gi % S, ab = gi & 1;
       const uint16_t sc = sn, bc = bn;
       if (g + 1 < G) {
         sn = __ldg(srow + g + 1);
         bn = __ldg(brow + g + 1);
       }
-      okd = okd && mbar_wait(&full[st], (gi / S) & 1);
-      if (gi >= 2) okd = okd && mbar_wait(&adone[ab], ((gi >> 1) - 1) & 1);
+      okd = okd && mbar_wait(&full[st], ph);
+      if (gi >= kABuf) okd = okd && mbar_wait(&adone[ab], aph ^ 1);
       if (okd) {
         const uint8_t *cb = base + P.c0 + st * P.cstage;
         uint8_t *abuf = base + P.a0 + ab * P.abuf;
@@ -853,6 +857,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       dense::fence_async_smem();  // the A tiles, written by threads, are read by the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&afull[ab], 0);  // this warp's part of the A tile is in place
+      if (++st == S) {
+        st = 0;
+        ph ^= 1;
+      }
+      if (++ab == kABuf) {
+        ab = 0;
+        aph ^= 1;
+      }
     }
     okd = __all_sync(0xffffffffu, okd);
   }
@@ -927,8 +939,7 @@ static int rt_stages(const Dims &d) { return rt_layout(d.H, d.E, 6).total <= 227
 
 bool prompt_supported(const Dims &d) {
   if (rt_layout(d.H, d.E, 3).total > 227 * 1024) return false;
-  return gemm_plan(d.H / kGroup, false, gemm_stages(d.H / kGroup, false)).total <= 227 * 1024 &&
-         gemm_plan(d.I / kGroup, true, gemm_stages(d.I / kGroup, true)).total <= 227 * 1024;
+  return true;  // the GEMM plan does not depend on the shape (checked at compile time)
 }
 
 cudaError_t prompt_set_attributes() {
@@ -963,18 +974,13 @@ cudaError_t launch_prompt(const PromptArgs &a, uint16_t *y, bool add_residual, i
     e = launch_k(prompt_gather_kernel, dim3((npos + kGatherThreads / 32 - 1) / (kGatherThreads / 32)),
                  dim3(kGatherThreads), 0, st, pdl, with_trace(2));
   }
-  const int gu_st = gemm_stages(a.d.H / kGroup, false), dn_st = gemm_stages(a.d.I / kGroup, true);
   if (e == cudaSuccess) {
     prm.a = with_trace(3);
-    prm.stages = gu_st;
-    e = launch_k(prompt_gemm_kernel<false>, dim3(n_sm), dim3(kGemmThreads),
-                 (size_t)gemm_plan(a.d.H / kGroup, false, gu_st).total, st, pdl, prm);
+    e = launch_k(prompt_gemm_kernel<false>, dim3(n_sm), dim3(kGemmThreads), (size_t)kGemmSmem, st, pdl, prm);
   }
   if (e == cudaSuccess) {
     prm.a = with_trace(4);
-    prm.stages = dn_st;
-    e = launch_k(prompt_gemm_kernel<true>, dim3(n_sm), dim3(kGemmThreads),
-                 (size_t)gemm_plan(a.d.I / kGroup, true, dn_st).total, st, pdl, prm);
+    e = launch_k(prompt_gemm_kernel<true>, dim3(n_sm), dim3(kGemmThreads), (size_t)kGemmSmem, st, pdl, prm);
   }
   if (e == cudaSuccess) {
     FfnArgs c;
