@@ -503,26 +503,36 @@ constexpr int kGemmMma = kGemmCons + 1;                 // tcgen05 issue warp
 constexpr int kGemmEpi0 = kGemmCons + 2;                // 4 epilogue warps (tensor-memory lane quarters 2, 3, 0, 1)
 constexpr int kGemmEpiWarps = 4;
 constexpr int kGemmThreads = (kGemmCons + 2 + kGemmEpiWarps) * 32;  // 704
-constexpr int kTileRows = dense::kRows;                 // 128 weight rows per unit
-constexpr int kStages = 6;  // TMA stages (operand rows + codes of one K group)
-constexpr int kABuf = 2;    // dequantised A tiles in flight (the dequant warps run kABuf - 1 groups ahead)
+constexpr int kTileRows = dense::kRows;                 // rows of one weight matrix (the MMA M)
+// 128-row weight matrices per unit, all against one operand tile: gate and
+// up for kMats / 2 row tiles of I (gate/up), or kMats row tiles of H (down).
+// More matrices per operand tile means fewer operand bytes per flop.
+constexpr int kMats = 2;
+constexpr int kSets = 512 / (128 * kMats);  // accumulator sets in tensor memory (units alternate between them)
+constexpr int kABuf = 2;                    // dequantised A tiles in flight
+constexpr int gemm_smem(int stages) {
+  return stages * (kTileRows * 128 + kMats * kTileRows * 32) + kABuf * kMats * kTileRows * 128 + 320 + 1024;
+}
+constexpr int pick_stages() {
+  int st = 8;
+  while (st > 2 && gemm_smem(st) > 227 * 1024) --st;
+  return st;
+}
+constexpr int kStages = pick_stages();  // TMA stages (operand rows + codes of one K group)
 
 // Shared-memory plan of a GEMM block (offsets from a 1024-aligned base).
 struct GemmPlan {
   int stages, bstage, cstage, abuf;
   int b0, c0, a0, bar, total;
 };
-// Both kernels run two 128-row weight matrices per unit against one operand
-// tile: gate and up rows r0 .. r0+127 (gate/up), or W_down rows r0 .. r0+127
-// and r0+128 .. r0+255 (down).
 __host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
   (void)G;
   (void)down;
   GemmPlan P;
   P.stages = stages;
-  P.bstage = kTileRows * 128;       // 128 operand rows x 64 fp16
-  P.cstage = 2 * kTileRows * 32;    // 128 rows x 64 codes per matrix
-  P.abuf = 2 * kTileRows * 128;     // dequantised A per matrix
+  P.bstage = kTileRows * 128;           // 128 operand rows x 64 fp16
+  P.cstage = kMats * kTileRows * 32;    // 128 rows x 64 codes per matrix
+  P.abuf = kMats * kTileRows * 128;     // dequantised A of every matrix
   int o = 0;
   P.b0 = o;
   o += stages * P.bstage;
@@ -535,7 +545,7 @@ __host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
   P.total = o + 1024;  // slack for the 1024-byte alignment of the base
   return P;
 }
-constexpr int kGemmSmem = kStages * (kTileRows * 128 + 2 * kTileRows * 32) + kABuf * 2 * kTileRows * 128 + 320 + 1024;
+constexpr int kGemmSmem = gemm_smem(kStages);
 static_assert(kGemmSmem <= 227 * 1024, "the GEMM plan fits one block per SM");
 
 struct GemmParams {
@@ -543,24 +553,46 @@ struct GemmParams {
   PromptArgs a;
 };
 
+// Bounded wait for the phase with the given parity that suspends the thread
+// in hardware (mbarrier.try_wait with a suspend-time hint) instead of
+// polling, so waiting warps take no issue slots from the warps sharing their
+// scheduler; false after limit_ns of global time.
+__device__ __forceinline__ bool mbar_wait_susp(uint64_t *bar, uint32_t parity,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+    if (ok) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Persistent GEMM over the units (chunk, 128 weight rows), u = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  Roles: the producer warp streams each K
 // group's operand rows and codes (TMA) through `stages` buffers; 16 warps
-// dequantise the codes into a double-buffered fp16 A tile; the MMA warp
-// issues the group's tcgen05.mma into one of two accumulator sets in tensor
-// memory (units alternate between them); 4 epilogue warps read a finished
-// unit's accumulators while the next unit's MMAs run.
+// dequantise the codes of the unit's kMats weight matrices into a
+// double-buffered fp16 A tile; the MMA warp issues the group's tcgen05.mma
+// into the unit's accumulator set in tensor memory; 4 epilogue warps read a
+// finished set (with two sets, while the next unit's MMAs run).
 template <bool kDown>
 __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __grid_constant__ GemmParams prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const PromptArgs &a = prm.a;
   const int H = a.d.H, I = a.d.I, T = a.d.T, k = a.d.k;
   const int K = kDown ? I : H, G = K / kGroup, M = kDown ? H : I;
-  constexpr int kUnitRows = kDown ? 2 * kTileRows : kTileRows;  // rows of M one unit covers
+  constexpr int kUnitRows = kDown ? kMats * kTileRows : kMats / 2 * kTileRows;  // rows of M one unit covers
   const int ntile = (M + kUnitRows - 1) / kUnitRows;
-  constexpr int nm = 2;                            // matrices per unit
+  constexpr int nm = kMats;                        // matrices per unit
   constexpr uint32_t kAccCols = 128 * nm;          // tensor-memory columns of one accumulator set
-  constexpr uint32_t kTmemCols = 2 * kAccCols;     // two sets
+  constexpr uint32_t kTmemCols = kSets * kAccCols; // 512
+  // matrix m of a unit: its first weight row past the unit's r0, and which
+  // weights (gate/up: m even gate, m odd up, of row tile m / 2)
+  auto moff = [](int m) { return kTileRows * (kDown ? m : (m >> 1)); };
   uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const GemmPlan P = gemm_plan(G, kDown, kStages);
   constexpr int S = kStages;
@@ -605,26 +637,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     bool ok = true;
     int gi = 0, st = 0, ph = 0;  // K groups issued; next stage and its use parity
     const CUtensorMap *bmap = kDown ? &prm.m.h : &prm.m.x;
-    // field f = 2 m + (0: scale, 1: bias) of matrix m; its first weight row
-    auto field_off = [&](int f) -> size_t {
-      if (kDown) return (f & 1) ? a.w.off.down_b : a.w.off.down_s;
-      return f == 0 ? a.w.off.gate_s : f == 1 ? a.w.off.gate_b : f == 2 ? a.w.off.up_s : a.w.off.up_b;
-    };
-    auto mrow = [&](int r0, int m) { return kDown ? r0 + kTileRows * m : r0; };
-    auto mrows = [&](int r0, int m) { return max(0, min(kTileRows, M - mrow(r0, m))); };
-    // a unit's weights into L2: the codes, scales and biases of its rows of
-    // both matrices are contiguous ranges of the blob (a few bulk requests)
+    auto q_off = [&](int m) -> size_t { return kDown ? a.w.off.down_q : (m & 1) ? a.w.off.up_q : a.w.off.gate_q; };
+    auto s_off = [&](int m) -> size_t { return kDown ? a.w.off.down_s : (m & 1) ? a.w.off.up_s : a.w.off.gate_s; };
+    auto b_off = [&](int m) -> size_t { return kDown ? a.w.off.down_b : (m & 1) ? a.w.off.up_b : a.w.off.gate_b; };
+    auto mrows = [&](int r0, int m) { return max(0, min(kTileRows, M - (r0 + moff(m)))); };
+    // a unit's weights into L2: the codes, scales and biases of each
+    // matrix's rows are contiguous ranges of the blob (a few bulk requests)
     auto prefetch_unit = [&](const uint8_t *bn, int r0n) {
-      const size_t qo0 = kDown ? a.w.off.down_q : a.w.off.gate_q, qo1 = kDown ? a.w.off.down_q : a.w.off.up_q;
-      for (int mm = 0; mm < 2; ++mm) {
+      for (int mm = 0; mm < nm; ++mm) {
         const int rows = mrows(r0n, mm);
         if (rows == 0) continue;
         const size_t qrow = (size_t)K / 2;  // code bytes per row
-        const uint8_t *q = bn + (mm ? qo1 : qo0) + (size_t)mrow(r0n, mm) * qrow;
+        const uint8_t *q = bn + q_off(mm) + (size_t)(r0n + moff(mm)) * qrow;
         for (size_t o = 0; o < rows * qrow; o += 65536)
           prefetch_l2(q + o, (uint32_t)min((size_t)65536, rows * qrow - o));
-        for (int f = 2 * mm; f < 2 * mm + 2; ++f)
-          prefetch_l2(bn + field_off(f) + (size_t)mrow(r0n, mm) * G * 2, (uint32_t)(rows * G * 2));
+        prefetch_l2(bn + s_off(mm) + (size_t)(r0n + moff(mm)) * G * 2, (uint32_t)(rows * G * 2));
+        prefetch_l2(bn + b_off(mm) + (size_t)(r0n + moff(mm)) * G * 2, (uint32_t)(rows * G * 2));
       }
     };
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
@@ -650,12 +678,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
           mbar_arrive_expect_tx(&full[st], (uint32_t)(P.bstage + P.cstage));
           dense::tma_load_2d(base + P.b0 + st * P.bstage, bmap, 64 * g, beg, &full[st]);
           uint8_t *cd = base + P.c0 + st * P.cstage;
-          if (kDown) {  // both halves (rows past H read as zero)
-            dense::tma_load_3d(cd, &prm.m.dq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
-            dense::tma_load_3d(cd + kTileRows * 32, &prm.m.dq[sh], 32 * g, r0 + kTileRows, sh ? 0 : e, &full[st]);
-          } else {
-            dense::tma_load_3d(cd, &prm.m.gq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
-            dense::tma_load_3d(cd + kTileRows * 32, &prm.m.uq[sh], 32 * g, r0, sh ? 0 : e, &full[st]);
+#pragma unroll
+          for (int m = 0; m < nm; ++m) {  // every matrix (rows past M read as zero)
+            const CUtensorMap *qm = kDown ? &prm.m.dq[sh] : (m & 1) ? &prm.m.uq[sh] : &prm.m.gq[sh];
+            dense::tma_load_3d(cd + m * kTileRows * 32, qm, 32 * g, r0 + moff(m), sh ? 0 : e, &full[st]);
           }
         }
         __syncwarp();
@@ -693,14 +719,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       const int ch = u / ntile;
       const int N = (__ldcg(a.ch_cnt + ch) + 15) & ~15;  // MMA N: the chunk's rows, padded to 16
       const uint32_t idesc = dense::idesc_f16(kTileRows, N);
-      const int tb = du & 1;
+      const int tb = du % kSets;
       // the set's previous unit read out by the epilogue
-      if (du >= 2) ok = __all_sync(0xffffffffu, mbar_wait_idle(&tempty[tb], ((du >> 1) - 1) & 1, 32));
+      if (du >= kSets) ok = __all_sync(0xffffffffu, mbar_wait_idle(&tempty[tb], ((du / kSets) - 1) & 1, 32));
       ++du;
       dense::tc_fence_after();
       const uint32_t acc = tmem + tb * kAccCols;
       for (int g = 0; g < G && ok; ++g, ++gi) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph) && mbar_wait(&afull[ab], aph));
+        ok = __all_sync(0xffffffffu, mbar_wait_susp(&full[st], ph) && mbar_wait_susp(&afull[ab], aph));
         if (!ok) break;
         dense::tc_fence_after();
         if (lane == 0) {
@@ -730,7 +756,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     if (!ok && lane == 0) set_error(a.err, kErrTimeout);
     // tensor memory back once the last MMAs completed and the epilogue read them (bounded waits)
     if (gi > 0) mbar_wait(&adone[(gi - 1) % kABuf], ((gi - 1) / kABuf) & 1);
-    if (du > 0) mbar_wait_idle(&tempty[(du - 1) & 1], ((du - 1) >> 1) & 1, 64);
+    if (du > 0) mbar_wait_idle(&tempty[(du - 1) % kSets], ((du - 1) / kSets) & 1, 64);
     dense::tc_fence_after();
     __syncwarp();
     dense::tc_dealloc(tmem, kTmemCols);
@@ -750,8 +776,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++du) {
       const int ch = u / ntile, rt = u - ch * ntile;
       const int beg = __ldcg(a.ch_beg + ch), cnt = __ldcg(a.ch_cnt + ch);
-      const int r0 = rt * kUnitRows, nrows = min(kTileRows, M - r0);
-      const int tb = du & 1;
+      const int r0 = rt * kUnitRows;
+      const int tb = du % kSets;
       // routing weights of columns lane, lane + 32, ... (down; shared rows: 1)
       float wq[4] = {1.f, 1.f, 1.f, 1.f};
       if (kDown)
@@ -760,27 +786,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
           const int n = 32 * q + lane;
           if (n < cnt && beg + n < npairs) wq[q] = __ldcg(a.r.wts + __ldcg(a.r.perm + beg + n));
         }
-      ok = __all_sync(0xffffffffu, mbar_wait(&tfull[tb], (du >> 1) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait_susp(&tfull[tb], (du / kSets) & 1));
       if (!ok) break;
       dense::tc_fence_after();
       const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + tb * kAccCols;
-      const int i = r0 + rr;
-      bool odd = false;
-      const int slot = dense::operand_slot(i & 63, odd);
       bool bad = false;
       for (int c0 = 0; c0 < cnt; c0 += 16) {  // 16 columns at a time (warp-uniform)
         if (!kDown) {
-          float gv[16], uv[16];
-          dense::tc_ld16(ta + c0, gv);
-          dense::tc_ld16(ta + 128 + c0, uv);
-          if (rr < nrows) {
-            __half *dst = a.hg + (size_t)(beg + c0) * I + (i & ~63) + slot;
+#pragma unroll 1
+          for (int hr = 0; hr < nm / 2; ++hr) {  // row tile hr: gate in matrix 2 hr, up in 2 hr + 1
+            float gv[16], uv[16];
+            dense::tc_ld16(ta + 256 * hr + c0, gv);
+            dense::tc_ld16(ta + 256 * hr + 128 + c0, uv);
+            const int i = r0 + kTileRows * hr + rr;
+            if (i < M) {
+              bool odd = false;
+              const int slot = dense::operand_slot(i & 63, odd);
+              __half *dst = a.hg + (size_t)(beg + c0) * I + (i & ~63) + slot;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (c0 + j < cnt) {
-                const float hv = gelu_tanh(gv[j]) * uv[j];
-                bad = bad || !(fabsf(hv) <= 65504.0f);
-                dst[(size_t)j * I] = __float2half_rn(odd ? hv * 0.0625f : hv);  // odd words / 16
+              for (int j = 0; j < 16; ++j) {
+                if (c0 + j < cnt) {
+                  const float hv = gelu_tanh(gv[j]) * uv[j];
+                  bad = bad || !(fabsf(hv) <= 65504.0f);
+                  dst[(size_t)j * I] = __float2half_rn(odd ? hv * 0.0625f : hv);  // odd words / 16
+                }
               }
             }
           }
@@ -788,7 +817,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
           const int q = c0 >> 5;  // the 16 columns share one group of 32 weights
           const float wsel = q == 0 ? wq[0] : q == 1 ? wq[1] : q == 2 ? wq[2] : wq[3];
 #pragma unroll 1
-          for (int m = 0; m < 2; ++m) {  // output rows r0 + 128 m + rr
+          for (int m = 0; m < nm; ++m) {  // output rows r0 + 128 m + rr
             float dv[16];
             dense::tc_ld16(ta + 128 * m + c0, dv);
             const int row = r0 + kTileRows * m + rr;
@@ -813,46 +842,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   }
 
   // ============================================================ dequantisation warps
-  // Thread: matrix m (gate / up, or the two halves of W_down), half hh of
-  // the K group, weight row rr.  Its row's scale and bias come from global
+  // Thread: matrices mp, mp + 2, ... (mp = tid / 256), half hh of the K
+  // group, weight row rr of each.  A row's scale and bias come from global
   // memory (the 32-byte sector of a row holds 16 groups: after the first
   // group of a sector the loads hit L1), one group ahead of their use.
-  const int m = tid >> 8, hh = (tid >> 7) & 1, rr = tid & 127;
+  constexpr int kPer = nm / 2;  // matrices per thread
+  const int mp = tid >> 8, hh = (tid >> 7) & 1, rr = tid & 127;
   bool okd = true;
   int gi = 0, st = 0, ph = 0, ab = 0, aph = 0;
   for (int u = blockIdx.x; u < nunits && okd; u += gridDim.x) {
     const int ch = u / ntile, rt = u - ch * ntile;
     const int e = __ldcg(a.ch_e + ch);
     const uint8_t *blob = e < 0 ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
-    const int wrow = (kDown ? rt * kUnitRows + kTileRows * m : rt * kUnitRows) + rr;
-    const bool rvalid = wrow < M;
-    const size_t so = kDown ? a.w.off.down_s : (m ? a.w.off.up_s : a.w.off.gate_s);
-    const size_t bo = kDown ? a.w.off.down_b : (m ? a.w.off.up_b : a.w.off.gate_b);
-    const uint16_t *srow = reinterpret_cast<const uint16_t *>(blob + so) + (size_t)(rvalid ? wrow : 0) * G;
-    const uint16_t *brow = reinterpret_cast<const uint16_t *>(blob + bo) + (size_t)(rvalid ? wrow : 0) * G;
-    uint16_t sn = __ldg(srow), bn = __ldg(brow);
+    const uint16_t *srow[kPer], *brow[kPer];
+    uint16_t sn[kPer], bn[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int m = mp + 2 * j;
+      const int wrow = rt * kUnitRows + moff(m) + rr;
+      const bool rvalid = wrow < M;
+      const size_t so = kDown ? a.w.off.down_s : ((m & 1) ? a.w.off.up_s : a.w.off.gate_s);
+      const size_t bo = kDown ? a.w.off.down_b : ((m & 1) ? a.w.off.up_b : a.w.off.gate_b);
+      srow[j] = reinterpret_cast<const uint16_t *>(blob + so) + (size_t)(rvalid ? wrow : 0) * G;
+      brow[j] = reinterpret_cast<const uint16_t *>(blob + bo) + (size_t)(rvalid ? wrow : 0) * G;
+      sn[j] = __ldg(srow[j]);
+      bn[j] = __ldg(brow[j]);
+    }
     for (int g = 0; g < G; ++g, ++gi) {
-      const uint16_t sc = sn, bc = bn;
-      if (g + 1 < G) {
-        sn = __ldg(srow + g + 1);
-        bn = __ldg(brow + g + 1);
+      uint16_t sc[kPer], bc[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        sc[j] = sn[j];
+        bc[j] = bn[j];
+        if (g + 1 < G) {
+          sn[j] = __ldg(srow[j] + g + 1);
+          bn[j] = __ldg(brow[j] + g + 1);
+        }
       }
-      okd = okd && mbar_wait(&full[st], ph);
-      if (gi >= kABuf) okd = okd && mbar_wait(&adone[ab], aph ^ 1);
+      okd = okd && mbar_wait_susp(&full[st], ph);
+      if (gi >= kABuf) okd = okd && mbar_wait_susp(&adone[ab], aph ^ 1);
       if (okd) {
         const uint8_t *cb = base + P.c0 + st * P.cstage;
         uint8_t *abuf = base + P.a0 + ab * P.abuf;
-        const uint4 cw = *reinterpret_cast<const uint4 *>(cb + m * kTileRows * 32 + rr * 32 + hh * 16);
-        const float sf = bf16_bits_to_float(sc);
-        const float bf = bf16_bits_to_float(bc);
-        const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
-        // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
-        uint8_t *row = abuf + m * kTileRows * 128 + rr * 128;
         const int sw = rr & 7, j0 = 4 * hh;
-        *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
-        *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
-        *reinterpret_cast<uint4 *>(row + ((j0 + 2) ^ sw) * 16) = dense::dequant_word(cw.z, s2, b2, b16);
-        *reinterpret_cast<uint4 *>(row + ((j0 + 3) ^ sw) * 16) = dense::dequant_word(cw.w, s2, b2, b16);
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int m = mp + 2 * j;
+          const uint4 cw = *reinterpret_cast<const uint4 *>(cb + m * kTileRows * 32 + rr * 32 + hh * 16);
+          const float sf = bf16_bits_to_float(sc[j]);
+          const float bf = bf16_bits_to_float(bc[j]);
+          const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
+          // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
+          uint8_t *row = abuf + m * kTileRows * 128 + rr * 128;
+          *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
+          *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
+          *reinterpret_cast<uint4 *>(row + ((j0 + 2) ^ sw) * 16) = dense::dequant_word(cw.z, s2, b2, b16);
+          *reinterpret_cast<uint4 *>(row + ((j0 + 3) ^ sw) * 16) = dense::dequant_word(cw.w, s2, b2, b16);
+        }
       }
       dense::fence_async_smem();  // the A tiles, written by threads, are read by the tensor cores
       __syncwarp();
