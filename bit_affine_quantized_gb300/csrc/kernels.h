@@ -160,9 +160,10 @@ struct FillArgs {
 cudaError_t launch_fill_slots(const FillArgs &a, cudaStream_t st);
 
 // Whole-prompt layer (prompt.cu): up to kPromptMaxRows rows through one
-// layer; the expert work in chunks of at most kPromptChunk rows of one expert.
+// layer; the expert work in chunks of at most kPromptChunk rows of one expert
+// (the N of one tcgen05.mma).
 constexpr int kPromptMaxRows = 4096;
-constexpr int kPromptChunk = 128;
+constexpr int kPromptChunk = 256;
 struct PromptArgs {
   LayerPtrs w;
   Dims d;                   // T = the prompt's rows

@@ -19,7 +19,7 @@
 //                         integers, per-group affine correction in fp32),
 //                         top-k and softmax per row.
 //   prompt_sort_kernel    one block: stable counting sort of all pairs by
-//                         expert, then the bounded chunks (at most 128 rows
+//                         expert, then the bounded chunks (at most 256 rows
 //                         of one expert) in tile order: the shared expert,
 //                         then experts 0-7, 8-15, ...
 //   prompt_gather_kernel  the normalised rows at their sorted positions, in
@@ -508,29 +508,39 @@ constexpr int kTileRows = dense::kRows;                 // rows of one weight ma
 // up for kMats / 2 row tiles of I (gate/up), or kMats row tiles of H (down).
 // More matrices per operand tile means fewer operand bytes per flop.
 constexpr int kMats = 2;
-constexpr int kSets = 512 / (128 * kMats);  // accumulator sets in tensor memory (units alternate between them)
-constexpr int kABuf = 2;                    // dequantised A tiles in flight
-constexpr int gemm_smem(int stages) {
-  return stages * (kTileRows * 128 + kMats * kTileRows * 32) + kABuf * kMats * kTileRows * 128 + 320 + 1024;
+constexpr int kABuf = 2;                         // dequantised A tiles in flight
+constexpr int gemm_smem(int n, int stages) {
+  return stages * (n * 128 + kMats * kTileRows * 32) + kABuf * kMats * kTileRows * 128 + 320 + 1024;
 }
-constexpr int pick_stages() {
+constexpr int pick_stages(int n) {
   int st = 8;
-  while (st > 2 && gemm_smem(st) > 227 * 1024) --st;
+  while (st > 2 && gemm_smem(n, st) > 227 * 1024) --st;
   return st;
 }
-constexpr int kStages = pick_stages();  // TMA stages (operand rows + codes of one K group)
+// Per kernel: N = the chunk rows one unit takes (the MMA N and the
+// tensor-memory columns per matrix), units per chunk and weight tile,
+// accumulator sets, TMA stages, shared memory.  Measured on GB300: whole
+// 256-row chunks with one accumulator set beat 128-row parts with two sets
+// for both kernels (down: 267 against 272 us at 4096 rows).
+template <bool kDown>
+struct GemmShape {
+  static constexpr int N = kPromptChunk;
+  static constexpr int Sub = kPromptChunk / N;      // units per chunk and weight tile
+  static constexpr int Sets = 512 / (N * kMats);
+  static constexpr int Stages = pick_stages(N);
+  static constexpr int Smem = gemm_smem(N, Stages);
+  static_assert(Sets >= 1 && Smem <= 227 * 1024, "the unit's accumulators and stages fit");
+};
 
 // Shared-memory plan of a GEMM block (offsets from a 1024-aligned base).
 struct GemmPlan {
   int stages, bstage, cstage, abuf;
   int b0, c0, a0, bar, total;
 };
-__host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
-  (void)G;
-  (void)down;
+__host__ __device__ inline GemmPlan gemm_plan(int n, int stages) {
   GemmPlan P;
   P.stages = stages;
-  P.bstage = kTileRows * 128;           // 128 operand rows x 64 fp16
+  P.bstage = n * 128;                   // the unit's operand rows x 64 fp16
   P.cstage = kMats * kTileRows * 32;    // 128 rows x 64 codes per matrix
   P.abuf = kMats * kTileRows * 128;     // dequantised A of every matrix
   int o = 0;
@@ -545,8 +555,6 @@ __host__ __device__ inline GemmPlan gemm_plan(int G, bool down, int stages) {
   P.total = o + 1024;  // slack for the 1024-byte alignment of the base
   return P;
 }
-constexpr int kGemmSmem = gemm_smem(kStages);
-static_assert(kGemmSmem <= 227 * 1024, "the GEMM plan fits one block per SM");
 
 struct GemmParams {
   dense::Maps m;  // 64-byte aligned: first
@@ -588,14 +596,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   constexpr int kUnitRows = kDown ? kMats * kTileRows : kMats / 2 * kTileRows;  // rows of M one unit covers
   const int ntile = (M + kUnitRows - 1) / kUnitRows;
   constexpr int nm = kMats;                        // matrices per unit
-  constexpr uint32_t kAccCols = 128 * nm;          // tensor-memory columns of one accumulator set
+  constexpr int kNmax = GemmShape<kDown>::N;        // rows of a unit (MMA N bound)
+  constexpr int kSub = GemmShape<kDown>::Sub;       // units per (chunk, weight tile)
+  constexpr int kSets = GemmShape<kDown>::Sets;
+  constexpr uint32_t kAccCols = kNmax * nm;        // tensor-memory columns of one accumulator set
   constexpr uint32_t kTmemCols = kSets * kAccCols; // 512
   // matrix m of a unit: its first weight row past the unit's r0, and which
   // weights (gate/up: m even gate, m odd up, of row tile m / 2)
   auto moff = [](int m) { return kTileRows * (kDown ? m : (m >> 1)); };
   uint8_t *base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const GemmPlan P = gemm_plan(G, kDown, kStages);
-  constexpr int S = kStages;
+  const GemmPlan P = gemm_plan(kNmax, GemmShape<kDown>::Stages);
+  constexpr int S = GemmShape<kDown>::Stages;
   uint64_t *full = reinterpret_cast<uint64_t *>(base + P.bar);  // [S] TMA landed
   uint64_t *empty = full + S;                                   // [S] MMAs done with a stage
   uint64_t *adone = empty + S;                                  // [kABuf] MMAs done with an A buffer
@@ -628,7 +639,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   pdl_wait();
   pdl_launch_dependents();
   if (tracer) trace_min(a.trace, kTrWaited);
-  const int nunits = __ldcg(a.n_ch) * ntile;
+  const int nunits = __ldcg(a.n_ch) * ntile * kSub;
+  // unit u: chunk, weight tile, part of the chunk (consecutive units share the
+  // weight tile, so its codes come from HBM once); rows beg .. beg + cnt - 1
+  // of the sorted positions, none when the chunk is shorter than the part
+  struct UnitPos {
+    int ch, rt, beg, cnt;
+  };
+  auto unit_pos = [&](int u) {
+    UnitPos q;
+    q.ch = u / (ntile * kSub);
+    const int rem = u - q.ch * ntile * kSub;
+    q.rt = rem / kSub;
+    const int sub = rem - q.rt * kSub;
+    q.beg = __ldcg(a.ch_beg + q.ch) + sub * kNmax;
+    q.cnt = min(kNmax, __ldcg(a.ch_cnt + q.ch) - sub * kNmax);
+    return q;
+  };
   const int npairs = T * k;
 
   // ============================================================ producer warp
@@ -656,8 +683,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
       }
     };
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const int ch = u / ntile, rt = u - ch * ntile;
-      const int e = __ldcg(a.ch_e + ch), beg = __ldcg(a.ch_beg + ch);
+      const UnitPos q = unit_pos(u);
+      if (q.cnt <= 0) continue;
+      const int ch = q.ch, rt = q.rt, beg = q.beg;
+      const int e = __ldcg(a.ch_e + ch);
       const int sh = e < 0 ? 1 : 0;
       const uint8_t *blob = sh ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
       const int r0 = rt * kUnitRows;
@@ -667,8 +696,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
         if (u == (int)blockIdx.x) prefetch_unit(blob, r0);
         const int un = u + gridDim.x;
         if (un < nunits) {
-          const int chn = un / ntile, en = __ldcg(a.ch_e + chn);
-          prefetch_unit(en < 0 ? a.w.shared : a.w.experts + (size_t)en * a.w.stride, (un - chn * ntile) * kUnitRows);
+          const UnitPos qn = unit_pos(un);
+          const int en = __ldcg(a.ch_e + qn.ch);
+          prefetch_unit(en < 0 ? a.w.shared : a.w.experts + (size_t)en * a.w.stride, qn.rt * kUnitRows);
         }
       }
       for (int g = 0; g < G && ok; ++g, ++gi) {
@@ -716,8 +746,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     const uint64_t bdesc0 = dense::sdesc(smem_addr(base + P.b0), 16, 1024, 2);
     const uint64_t adesc0 = dense::sdesc(smem_addr(base + P.a0), 16, 1024, 2);
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-      const int ch = u / ntile;
-      const int N = (__ldcg(a.ch_cnt + ch) + 15) & ~15;  // MMA N: the chunk's rows, padded to 16
+      const UnitPos q = unit_pos(u);
+      if (q.cnt <= 0) continue;
+      const int N = (q.cnt + 15) & ~15;  // MMA N: the unit's rows, padded to 16
       const uint32_t idesc = dense::idesc_f16(kTileRows, N);
       const int tb = du % kSets;
       // the set's previous unit read out by the epilogue
@@ -736,7 +767,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
           for (int ks = 0; ks < 4; ++ks)  // K = 16 per MMA: 32 bytes further along each row
 #pragma unroll
             for (int m = 0; m < nm; ++m)
-              dense::tc_mma(acc + m * 128, ad0 + (uint64_t)(((m * kTileRows * 128) >> 4) + 2 * ks), bd0 + 2 * ks, idesc,
+              dense::tc_mma(acc + m * kNmax, ad0 + (uint64_t)(((m * kTileRows * 128) >> 4) + 2 * ks), bd0 + 2 * ks, idesc,
                             (g > 0 || ks > 0) ? 1u : 0u);
           dense::tc_commit(&empty[st]);               // the TMA stage may be refilled
           dense::tc_commit(&adone[ab]);               // the A buffer may be rewritten
@@ -774,15 +805,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     const int rr = 32 * (warp & 3) + lane;
     int du = 0;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++du) {
-      const int ch = u / ntile, rt = u - ch * ntile;
-      const int beg = __ldcg(a.ch_beg + ch), cnt = __ldcg(a.ch_cnt + ch);
-      const int r0 = rt * kUnitRows;
+      const UnitPos q = unit_pos(u);
+      if (q.cnt <= 0) {
+        --du;  // no unit: the accumulator sets do not advance
+        continue;
+      }
+      const int beg = q.beg, cnt = q.cnt;
+      const int r0 = q.rt * kUnitRows;
       const int tb = du % kSets;
       // routing weights of columns lane, lane + 32, ... (down; shared rows: 1)
-      float wq[4] = {1.f, 1.f, 1.f, 1.f};
+      float wq[kNmax / 32];
+#pragma unroll
+      for (int q = 0; q < kNmax / 32; ++q) wq[q] = 1.f;
       if (kDown)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < kNmax / 32; ++q) {
           const int n = 32 * q + lane;
           if (n < cnt && beg + n < npairs) wq[q] = __ldcg(a.r.wts + __ldcg(a.r.perm + beg + n));
         }
@@ -796,8 +833,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
 #pragma unroll 1
           for (int hr = 0; hr < nm / 2; ++hr) {  // row tile hr: gate in matrix 2 hr, up in 2 hr + 1
             float gv[16], uv[16];
-            dense::tc_ld16(ta + 256 * hr + c0, gv);
-            dense::tc_ld16(ta + 256 * hr + 128 + c0, uv);
+            dense::tc_ld16(ta + 2 * kNmax * hr + c0, gv);
+            dense::tc_ld16(ta + 2 * kNmax * hr + kNmax + c0, uv);
             const int i = r0 + kTileRows * hr + rr;
             if (i < M) {
               bool odd = false;
@@ -815,11 +852,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
           }
         } else {
           const int q = c0 >> 5;  // the 16 columns share one group of 32 weights
-          const float wsel = q == 0 ? wq[0] : q == 1 ? wq[1] : q == 2 ? wq[2] : wq[3];
+          float wsel = wq[0];
+#pragma unroll
+          for (int i = 1; i < kNmax / 32; ++i)
+            if (q == i) wsel = wq[i];
 #pragma unroll 1
           for (int m = 0; m < nm; ++m) {  // output rows r0 + 128 m + rr
             float dv[16];
-            dense::tc_ld16(ta + 128 * m + c0, dv);
+            dense::tc_ld16(ta + kNmax * m + c0, dv);
             const int row = r0 + kTileRows * m + rr;
             float *dst = a.obuf + (size_t)(beg + c0) * H + row;
 #pragma unroll
@@ -851,7 +891,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   bool okd = true;
   int gi = 0, st = 0, ph = 0, ab = 0, aph = 0;
   for (int u = blockIdx.x; u < nunits && okd; u += gridDim.x) {
-    const int ch = u / ntile, rt = u - ch * ntile;
+    const UnitPos q = unit_pos(u);
+    if (q.cnt <= 0) continue;
+    const int ch = q.ch, rt = q.rt;
     const int e = __ldcg(a.ch_e + ch);
     const uint8_t *blob = e < 0 ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
     const uint16_t *srow[kPer], *brow[kPer];
@@ -944,22 +986,22 @@ bool encode_map(EncodeTiledFn f, CUtensorMap *m, CUtensorMapDataType dt, int ran
 }
 
 // Operand rows of x and h per sorted position (fp16, boxes of 64 elements x
-// 128 rows with the 128-byte swizzle), the codes of gate, up and down
+// kNmax rows with the 128-byte swizzle), the codes of gate, up and down
 // (boxes of 32 bytes x 128 rows of one expert) for the routed experts (3-D
 // over the fixed-stride blobs) and the shared expert.
 bool prompt_maps(const PromptArgs &a, dense::Maps &m) {
   const EncodeTiledFn f = encode_tiled();
   if (!f) return false;
   const cuuint64_t H = a.d.H, I = a.d.I, E = a.d.E, npos = (cuuint64_t)a.d.T * (a.d.k + 1);
-  const cuuint32_t bx[2] = {64, (cuuint32_t)kTileRows};
+  const cuuint32_t bxg[2] = {64, (cuuint32_t)GemmShape<false>::N}, bxd[2] = {64, (cuuint32_t)GemmShape<true>::N};
   bool ok = true;
   {
     const cuuint64_t dims[2] = {H, npos}, str[1] = {H * 2};
-    ok = ok && encode_map(f, &m.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.xg, dims, str, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_map(f, &m.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.xg, dims, str, bxg, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   {
     const cuuint64_t dims[2] = {I, npos}, str[1] = {I * 2};
-    ok = ok && encode_map(f, &m.h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.hg, dims, str, bx, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_map(f, &m.h, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.hg, dims, str, bxd, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   const cuuint32_t bq[3] = {32, (cuuint32_t)kTileRows, 1};
   auto codes = [&](CUtensorMap *mm, size_t off, cuuint64_t row_bytes, cuuint64_t rows) {
@@ -1022,11 +1064,13 @@ cudaError_t launch_prompt(const PromptArgs &a, uint16_t *y, bool add_residual, i
   }
   if (e == cudaSuccess) {
     prm.a = with_trace(3);
-    e = launch_k(prompt_gemm_kernel<false>, dim3(n_sm), dim3(kGemmThreads), (size_t)kGemmSmem, st, pdl, prm);
+    e = launch_k(prompt_gemm_kernel<false>, dim3(n_sm), dim3(kGemmThreads), (size_t)GemmShape<false>::Smem, st, pdl,
+                 prm);
   }
   if (e == cudaSuccess) {
     prm.a = with_trace(4);
-    e = launch_k(prompt_gemm_kernel<true>, dim3(n_sm), dim3(kGemmThreads), (size_t)kGemmSmem, st, pdl, prm);
+    e = launch_k(prompt_gemm_kernel<true>, dim3(n_sm), dim3(kGemmThreads), (size_t)GemmShape<true>::Smem, st, pdl,
+                 prm);
   }
   if (e == cudaSuccess) {
     FfnArgs c;

@@ -227,7 +227,7 @@ int moe_layer_forward_residual(moe_handle *h, void *hidden, int n_tokens,
  * MOE_PROMPT_MAX_ROWS rows in one call:
  *   hidden <- bf16(hidden + MoE(rmsnorm(hidden)))   (or the layer's tail)
  * row by row.  Rows are routed independently; all rows' token/expert pairs
- * are grouped per expert and cut into chunks of at most 128 rows of one
+ * are grouped per expert and cut into chunks of at most 256 rows of one
  * expert, and every (chunk, 128 weight rows) is one unit of a persistent
  * tensor-core GEMM (tcgen05.mma, weights dequantised once per unit into fp16
  * on chip: w = q * s + b rounded once to fp16).  Units run the shared

@@ -85,12 +85,12 @@ def test_prompt_matches_oracle(moe, layer0, layer0_zipf, n_rows, zipf):
 
 def test_prompt_full_size(moe, layer0_zipf):
     """4096 rows (32 chunks of 128) with Zipf-skewed routing: the head experts
-    get several hundred rows, i.e. several bounded chunks each."""
+    get several hundred rows, i.e. several bounded units of up to 256 rows each."""
     n = bq.MOE_PROMPT_MAX_ROWS
     h0 = hidden(4242, 0, n, rms=False)
     out = run_prompt(moe, layer0_zipf, h0)
     counts = np.bincount(out["ids"].ravel(), minlength=E)
-    assert counts.max() > 2 * 128, "the skew should give some expert more than two chunks"
+    assert counts.max() > 2 * 256, "the skew should give some expert more than two bounded units of 256 rows"
     rng = np.random.default_rng(11)
     rows = np.sort(np.concatenate([[0, 127, 128, n - 1], rng.choice(n, 28, replace=False)]))
     check_block(out, layer0_zipf, h0, K, rows=rows)
