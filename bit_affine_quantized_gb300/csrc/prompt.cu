@@ -14,7 +14,7 @@
 // through is the GPU's L2: every expert's weights are read once per layer for
 // all of the prompt's rows instead of once per 128-row chunk.
 //
-//   prompt_router_kernel  16 rows per block: rmsnorm, the 8-bit router on the
+//   prompt_router_kernel  16 rows per block (16 warps): rmsnorm, the 8-bit router on the
 //                         tensor cores (mma.m16n8k16, codes as exact fp16
 //                         integers, per-group affine correction in fp32),
 //                         top-k and softmax per row.
@@ -50,7 +50,8 @@ namespace {
 
 // ------------------------------------------------------------------ router
 constexpr int kRtTok = 16;        // rows per router block (one m16 tile)
-constexpr int kRtThreads = 256;   // 8 warps, 16 experts (two n8 tiles) each
+constexpr int kRtThreads = 512;   // 16 warps, 8 experts (one n8 tile) each
+constexpr int kRtNT = kMaxExperts / 8 / (kRtThreads / 32);  // n8 tiles per warp
 constexpr int kRtGroups = 2;      // 64-wide K groups per code stage
 constexpr int kRtCodePitch = 64 * kRtGroups + 16;  // bytes per expert row of a stage: rows 4 banks apart
 constexpr int kRowVec = 16;       // 16-byte vectors of one row per lane (H <= 4096)
@@ -212,12 +213,12 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
     }
   }
 
-  // logits: warp w owns experts 16w .. 16w+15 (two n8 tiles) for all 16 rows
+  // logits: warp w owns experts 8 kRtNT w .. + 8 kRtNT - 1 for all 16 rows
   const int r = lane >> 2, c = lane & 3;
-  const int n0 = 16 * warp;
-  float tot[2][4];
+  const int n0 = 8 * kRtNT * warp;
+  float tot[kRtNT][4];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int nt = 0; nt < kRtNT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) tot[nt][i] = 0.f;
   for (int s = 0; s < nst; ++s) {
@@ -229,7 +230,9 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
     if (n0 < E) {
       for (int gl = 0; gl < ng; ++gl) {
         const int g = g0 + gl;
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float acc[kRtNT][4];
+#pragma unroll
+        for (int nt = 0; nt < kRtNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const int kk = 64 * g + 16 * ks;
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
           A[2] = *reinterpret_cast<const uint32_t *>(sx + r * L.xp + 2 * (kk + 8 + 2 * c));
           A[3] = *reinterpret_cast<const uint32_t *>(sx + (r + 8) * L.xp + 2 * (kk + 8 + 2 * c));
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
+          for (int nt = 0; nt < kRtNT; ++nt) {
             // experts past E (E not a multiple of 16) read expert E - 1: columns discarded below
             const uint8_t *crow = cs + min(n0 + 8 * nt + r, E - 1) * kRtCodePitch + 64 * gl + 16 * ks + 2 * c;
             const uint32_t b0 = codes8_f16x2(*reinterpret_cast<const uint16_t *>(crow));
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
         }
         const float x0 = sxs[r * G + g], x1 = sxs[(r + 8) * G + g];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < kRtNT; ++nt)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int e = n0 + 8 * nt + 2 * c + (i & 1);
@@ -263,7 +266,7 @@ __global__ void __launch_bounds__(kRtThreads) prompt_router_kernel(const PromptA
   cp_async_wait<0>();
   __syncthreads();  // the code stages become the logit table
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int nt = 0; nt < kRtNT; ++nt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int e = n0 + 8 * nt + 2 * c + (i & 1), rl = r + 8 * (i >> 1);
