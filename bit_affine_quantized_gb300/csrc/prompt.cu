@@ -11,29 +11,31 @@
 // units.
 //
 // Here the weights stay resident in HBM and the "cache" the tiles stream
-// through is the GPU's L2: every expert's weights are read once per layer for
-// all of the prompt's rows instead of once per 128-row chunk.
+// through is the GPU's L2: every expert's weights come from HBM about once per
+// layer for all of the prompt's rows instead of once per 128-row chunk.
 //
-//   prompt_router_kernel  16 rows per block (16 warps): rmsnorm, the 8-bit router on the
-//                         tensor cores (mma.m16n8k16, codes as exact fp16
-//                         integers, per-group affine correction in fp32),
-//                         top-k and softmax per row.
+//   prompt_router_kernel  16 rows per block, 16 warps: rmsnorm, the 8-bit
+//                         router on the tensor cores (mma.m16n8k16, codes as
+//                         exact fp16 integers, per-group affine correction in
+//                         fp32), top-k and softmax per row.
 //   prompt_sort_kernel    one block: stable counting sort of all pairs by
 //                         expert, then the bounded chunks (at most 256 rows
 //                         of one expert) in tile order: the shared expert,
 //                         then experts 0-7, 8-15, ...
 //   prompt_gather_kernel  the normalised rows at their sorted positions, in
 //                         the operand order of the dense dequantisation.
-//   prompt_gemm_kernel    persistent, one block per SM: units (chunk, 128
-//                         weight rows); per K group the producer warp loads
-//                         the chunk's operand rows and the 4-bit codes with
-//                         tensor TMA, 16 warps dequantise the codes into an
-//                         fp16 A tile, one thread issues tcgen05.mma (M = 128
-//                         weight rows, N = the chunk's rows) into tensor
-//                         memory; the epilogue applies GeGLU (gate/up) or the
-//                         routing weight (down).  Each block prefetches its
-//                         next unit's weights into L2 while the current unit
-//                         runs.
+//   prompt_gemm_kernel    persistent, one block per SM: a unit is one chunk
+//                         against two 128-row weight matrices (gate and up
+//                         rows of one 128-row tile of I, or two 128-row
+//                         halves of a 256-row tile of W_down); per K group
+//                         the producer warp loads the chunk's operand rows
+//                         and the 4-bit codes with tensor TMA, 16 warps
+//                         dequantise the codes into an fp16 A tile, one
+//                         thread issues tcgen05.mma (M = 128 weight rows,
+//                         N = the chunk's rows) into tensor memory, and 4
+//                         epilogue warps apply GeGLU (gate/up) or the routing
+//                         weight (down).  Each block prefetches its next
+//                         unit's weights into L2 while the current unit runs.
 //   combine_kernel        y[t] = sum of the token's weighted expert outputs
 //                         in selection order + the shared expert's, added to
 //                         the residual stream (ffn.cu).
@@ -583,9 +585,9 @@ __device__ __forceinline__ bool mbar_wait_susp(uint64_t *bar, uint32_t parity,
   }
 }
 
-// Persistent GEMM over the units (chunk, 128 weight rows), u = blockIdx.x,
+// Persistent GEMM over the units (chunk, weight tile), u = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  Roles: the producer warp streams each K
-// group's operand rows and codes (TMA) through `stages` buffers; 16 warps
+// group's operand rows and codes (TMA) through the stage buffers; 16 warps
 // dequantise the codes of the unit's kMats weight matrices into a
 // double-buffered fp16 A tile; the MMA warp issues the group's tcgen05.mma
 // into the unit's accumulator set in tensor memory; 4 epilogue warps read a
