@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
     }
     for (int i = 0; i < kABuf; ++i) {
       mbar_init(&adone[i], 1);
-      mbar_init(&afull[i], kGemmCons);
+      mbar_init(&afull[i], kGemmCons / 2);  // the half of the dequant warps that owns the buffer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -887,78 +887,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) prompt_gemm_kernel(const __gr
   }
 
   // ============================================================ dequantisation warps
-  // Thread: matrices mp, mp + 2, ... (mp = tid / 256), half hh of the K
-  // group, weight row rr of each.  A row's scale and bias come from global
-  // memory (the 32-byte sector of a row holds 16 groups: after the first
-  // group of a sector the loads hit L1), one group ahead of their use.
-  constexpr int kPer = nm / 2;  // matrices per thread
-  const int mp = tid >> 8, hh = (tid >> 7) & 1, rr = tid & 127;
+  // Two halves of 8 warps take alternate K groups (half h: the block's
+  // groups gi with gi % 2 == h, into A buffer h), so each warp's wait,
+  // fence and arrival cover a whole row per thread and the two halves
+  // overlap on consecutive groups.  Thread: matrix m (gate / up, or the two
+  // halves of W_down), weight row rr, all 64 codes of the group.  A row's
+  // scale and bias come from global memory (the 32-byte sector of a row holds
+  // 16 groups: after the first group of a sector the loads hit L1), one of
+  // the half's groups ahead of their use.
+  static_assert(nm == 2 && kABuf == 2, "one matrix per thread, one A buffer per half");
+  const int half = tid >> 8, m = (tid >> 7) & 1, rr = tid & 127;
   bool okd = true;
-  int gi = 0, st = 0, ph = 0, ab = 0, aph = 0;
+  int gi = 0;  // the block's K groups before this unit
   for (int u = blockIdx.x; u < nunits && okd; u += gridDim.x) {
     const UnitPos q = unit_pos(u);
     if (q.cnt <= 0) continue;
     const int ch = q.ch, rt = q.rt;
     const int e = __ldcg(a.ch_e + ch);
     const uint8_t *blob = e < 0 ? a.w.shared : a.w.experts + (size_t)e * a.w.stride;
-    const uint16_t *srow[kPer], *brow[kPer];
-    uint16_t sn[kPer], bn[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int m = mp + 2 * j;
-      const int wrow = rt * kUnitRows + moff(m) + rr;
-      const bool rvalid = wrow < M;
-      const size_t so = kDown ? a.w.off.down_s : ((m & 1) ? a.w.off.up_s : a.w.off.gate_s);
-      const size_t bo = kDown ? a.w.off.down_b : ((m & 1) ? a.w.off.up_b : a.w.off.gate_b);
-      srow[j] = reinterpret_cast<const uint16_t *>(blob + so) + (size_t)(rvalid ? wrow : 0) * G;
-      brow[j] = reinterpret_cast<const uint16_t *>(blob + bo) + (size_t)(rvalid ? wrow : 0) * G;
-      sn[j] = __ldg(srow[j]);
-      bn[j] = __ldg(brow[j]);
+    const int wrow = rt * kUnitRows + moff(m) + rr;
+    const bool rvalid = wrow < M;
+    const size_t so = kDown ? a.w.off.down_s : ((m & 1) ? a.w.off.up_s : a.w.off.gate_s);
+    const size_t bo = kDown ? a.w.off.down_b : ((m & 1) ? a.w.off.up_b : a.w.off.gate_b);
+    const uint16_t *srow = reinterpret_cast<const uint16_t *>(blob + so) + (size_t)(rvalid ? wrow : 0) * G;
+    const uint16_t *brow = reinterpret_cast<const uint16_t *>(blob + bo) + (size_t)(rvalid ? wrow : 0) * G;
+    const int g0 = half ^ (gi & 1);  // this half's first group of the unit
+    uint16_t sn = 0, bn = 0;
+    if (g0 < G) {
+      sn = __ldg(srow + g0);
+      bn = __ldg(brow + g0);
     }
-    for (int g = 0; g < G; ++g, ++gi) {
-      uint16_t sc[kPer], bc[kPer];
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        sc[j] = sn[j];
-        bc[j] = bn[j];
-        if (g + 1 < G) {
-          sn[j] = __ldg(srow[j] + g + 1);
-          bn[j] = __ldg(brow[j] + g + 1);
-        }
+    for (int g = g0; g < G; g += 2) {
+      const int gg = gi + g;  // the block's group index: stage, buffer and phases follow from it
+      const int st = gg % S, ph = (gg / S) & 1, ab = half;
+      const uint16_t sc = sn, bc = bn;
+      if (g + 2 < G) {
+        sn = __ldg(srow + g + 2);
+        bn = __ldg(brow + g + 2);
       }
       okd = okd && mbar_wait_susp(&full[st], ph);
-      if (gi >= kABuf) okd = okd && mbar_wait_susp(&adone[ab], aph ^ 1);
+      if (gg >= kABuf) okd = okd && mbar_wait_susp(&adone[ab], ((gg >> 1) - 1) & 1);
       if (okd) {
-        const uint8_t *cb = base + P.c0 + st * P.cstage;
-        uint8_t *abuf = base + P.a0 + ab * P.abuf;
-        const int sw = rr & 7, j0 = 4 * hh;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-          const int m = mp + 2 * j;
-          const uint4 cw = *reinterpret_cast<const uint4 *>(cb + m * kTileRows * 32 + rr * 32 + hh * 16);
-          const float sf = bf16_bits_to_float(sc[j]);
-          const float bf = bf16_bits_to_float(bc[j]);
-          const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
-          // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
-          uint8_t *row = abuf + m * kTileRows * 128 + rr * 128;
-          *reinterpret_cast<uint4 *>(row + ((j0 + 0) ^ sw) * 16) = dense::dequant_word(cw.x, s2, b2, b16);
-          *reinterpret_cast<uint4 *>(row + ((j0 + 1) ^ sw) * 16) = dense::dequant_word(cw.y, s2, b2, b16);
-          *reinterpret_cast<uint4 *>(row + ((j0 + 2) ^ sw) * 16) = dense::dequant_word(cw.z, s2, b2, b16);
-          *reinterpret_cast<uint4 *>(row + ((j0 + 3) ^ sw) * 16) = dense::dequant_word(cw.w, s2, b2, b16);
-        }
+        const uint8_t *cb = base + P.c0 + st * P.cstage + m * kTileRows * 32 + rr * 32;
+        uint8_t *row = base + P.a0 + ab * P.abuf + m * kTileRows * 128 + rr * 128;
+        const uint4 cw0 = *reinterpret_cast<const uint4 *>(cb), cw1 = *reinterpret_cast<const uint4 *>(cb + 16);
+        const float sf = bf16_bits_to_float(sc);
+        const float bf = bf16_bits_to_float(bc);
+        const uint32_t s2 = dense::f16x2_of(sf), b2 = dense::f16x2_of(bf), b16 = dense::f16x2_of(16.0f * bf);
+        // row rr of the 128-byte-swizzled tile: 16-byte chunk j at (j ^ (rr % 8))
+        const int sw = rr & 7;
+        *reinterpret_cast<uint4 *>(row + (0 ^ sw) * 16) = dense::dequant_word(cw0.x, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + (1 ^ sw) * 16) = dense::dequant_word(cw0.y, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + (2 ^ sw) * 16) = dense::dequant_word(cw0.z, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + (3 ^ sw) * 16) = dense::dequant_word(cw0.w, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + (4 ^ sw) * 16) = dense::dequant_word(cw1.x, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + (5 ^ sw) * 16) = dense::dequant_word(cw1.y, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + (6 ^ sw) * 16) = dense::dequant_word(cw1.z, s2, b2, b16);
+        *reinterpret_cast<uint4 *>(row + (7 ^ sw) * 16) = dense::dequant_word(cw1.w, s2, b2, b16);
       }
       dense::fence_async_smem();  // the A tiles, written by threads, are read by the tensor cores
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&afull[ab], 0);  // this warp's part of the A tile is in place
-      if (++st == S) {
-        st = 0;
-        ph ^= 1;
-      }
-      if (++ab == kABuf) {
-        ab = 0;
-        aph ^= 1;
-      }
     }
+    gi += G;
     okd = __all_sync(0xffffffffu, okd);
   }
   if (!okd && lane == 0) set_error(a.err, kErrTimeout);
